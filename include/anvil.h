@@ -1,0 +1,183 @@
+/*
+ * anvil.h -- C ABI of libanvil, the ANVIL bank step on GB300 (sm_103a).
+ *
+ * The operation is the one defined on the page "modded-nanogpt
+ * track_1_short/optim/anvil.py", function `anvil_cascade` and the constants
+ * above it (ANVIL_MAPS, RAIL_FAST_BETA / RAIL_SLOW_BETA / RAIL_FAST_WEIGHT,
+ * FROBENIUS_MARGIN / FROBENIUS_EPS).  For every matrix G of a bank [g, m, n]:
+ *
+ *   v0 <- v0 + (1 - fast_beta) (G - v0)          fast rail   (velocity[0])
+ *   v1 <- v1 + (1 - slow_beta) (G - v1)          slow rail   (velocity[1])
+ *   blend = w v0 + (1 - w) v1                    w = fast_weight
+ *   X  = bf16(G + momentum (blend - G))          Nesterov lookahead
+ *   tall (m > n): A = X^T X, update X <- a X + X B
+ *   wide (m <= n, square included): A = X X^T, update X <- a X + B X
+ *   d  = sqrt(trace of the bf16 first Gram) * margin + eps
+ *   X  <- bf16(X / d), A <- bf16(A / d^2)
+ *   for each map (a, b, c): [A = bf16(Gram(X)) after the first]
+ *       B = bf16(b A + c A A);  X <- bf16(a X + X B  |  a X + B X)
+ *   out = X
+ *
+ * Every number is computed on the GPU by this library's own kernels; there is
+ * no CPU path.  All calls are asynchronous on the given stream (a
+ * cudaStream_t / CUstream handle passed as void*; NULL = legacy default
+ * stream).  No call below allocates, frees or synchronises, except
+ * anvil_bank_step on its first use of a size (documented there) and the
+ * diagnostic anvil_device_error.  Errors are returned as status codes; no
+ * exception crosses the ABI.
+ */
+#ifndef ANVIL_H
+#define ANVIL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ANVIL_OK = 0,
+    ANVIL_ERR_INVALID_ARG = 1,       /* null pointer, g/m/n < 1, nmaps out of range, ... */
+    ANVIL_ERR_UNSUPPORTED_SHAPE = 2, /* a dimension above ANVIL_MAX_DIM / ANVIL_MAX_BATCH */
+    ANVIL_ERR_ALIGNMENT = 3,         /* pointer not aligned to its element size / workspace to 256 B */
+    ANVIL_ERR_ALIAS = 4,             /* a written buffer overlaps another buffer of the call */
+    ANVIL_ERR_WORKSPACE = 5,         /* workspace too small, or cannot be allocated during capture */
+    ANVIL_ERR_CUDA = 6,              /* a CUDA runtime/driver call or a launch failed */
+    ANVIL_ERR_TIMEOUT = 7,           /* a bounded device-side wait gave up (see anvil_device_error) */
+    ANVIL_ERR_DEVICE = 8             /* current device is not sm_103 (the kernels are sm_103a only) */
+} anvil_status;
+
+/* One quintic spectral map f(s) = a s + b s^3 + c s^5 (an ANVIL_MAPS entry). */
+typedef struct { float a, b, c; } anvil_map;
+
+/* Per-step scalars of one bank (the page's AnvilBank momentum / fast_beta /
+ * fast_weight, plus the slow rail's beta, RAIL_SLOW_BETA there). */
+typedef struct { float momentum, fast_beta, fast_weight, slow_beta; } anvil_scalars;
+
+/* One bank of g matrices of m x n.  All pointers are DEVICE pointers, row-major,
+ * caller-owned:
+ *   grad      [g, m, n]    fp32, read only (never written)
+ *   velocity  [2, g, m, n] fp32, read and written in place; rail 0 fast, rail 1 slow
+ *   out       [g, m, n]    bf16 bits, written
+ * grad and velocity must be 4-byte aligned, out 2-byte aligned; out must not
+ * overlap grad, velocity or any buffer of another bank in the same call.
+ * `scalars` is used when the call's device scalar array is NULL. */
+typedef struct {
+    const float* grad;
+    float* velocity;
+    uint16_t* out;
+    int g, m, n;
+    anvil_scalars scalars;
+} anvil_bank_desc;
+
+#define ANVIL_MAX_MAPS 16     /* maps per call */
+#define ANVIL_MAX_BANKS 8     /* banks per anvil_multi_bank_step call */
+#define ANVIL_MAX_DIM 16384   /* largest m or n */
+#define ANVIL_MAX_BATCH 65535 /* largest g */
+
+/* Writes the page's six ANVIL_MAPS into maps[0..5] (if cap >= 6) and returns 6. */
+int anvil_default_maps(anvil_map* maps, int cap);
+
+/* Bytes of device workspace anvil_multi_bank_step needs for these banks
+ * (0 if the descriptors are invalid).  Depends only on g, m, n of each bank. */
+size_t anvil_workspace_bytes(const anvil_bank_desc* banks, int nbanks);
+
+/* One ANVIL step over nbanks banks, every kernel grouped across the banks.
+ *   banks      host array of nbanks descriptors (1 <= nbanks <= ANVIL_MAX_BANKS)
+ *   d_scalars  DEVICE array of nbanks anvil_scalars read by the momentum kernel
+ *              when it runs (so a captured CUDA graph sees the current values),
+ *              or NULL to use banks[i].scalars, fixed at launch/capture time
+ *   maps       host array of nmaps maps (1 <= nmaps <= ANVIL_MAX_MAPS), applied in order
+ *   margin, eps  the normaliser d = sqrt(tr) * margin + eps (page: 1.05, 1e-6)
+ *   workspace  DEVICE scratch of at least anvil_workspace_bytes(banks, nbanks)
+ *              bytes, 256-byte aligned, owned by the caller; its contents on
+ *              entry do not matter, and two calls that overlap on the GPU must
+ *              not share it
+ * Allocates nothing and never synchronises, so it may be captured in a CUDA graph. */
+anvil_status anvil_multi_bank_step(const anvil_bank_desc* banks, int nbanks,
+                                   const anvil_scalars* d_scalars,
+                                   const anvil_map* maps, int nmaps, float margin, float eps,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* One bank with host scalars: the page's anvil_cascade signature with the slow
+ * beta, the maps, margin and eps made parameters.  Uses a workspace owned by the
+ * library, cached per device and grown on demand: a call that needs more than
+ * the cached size frees and allocates it (cudaFree / cudaMalloc, which
+ * synchronise the device), so make one call of the largest size before
+ * capturing this function in a CUDA graph; a call that would have to grow it
+ * while the stream is capturing returns ANVIL_ERR_WORKSPACE.
+ * maps = NULL selects the page's six ANVIL_MAPS. */
+anvil_status anvil_bank_step(const float* grad, float* velocity, int g, int m, int n,
+                             float momentum, float fast_beta, float fast_weight, float slow_beta,
+                             const anvil_map* maps, int nmaps, float margin, float eps,
+                             uint16_t* out, void* stream);
+
+/* Per-stage dumps of one bank step, for parity testing (not the hot path).
+ * DEVICE pointers, each optional (NULL = skip), in the page's layout:
+ *   X_raw [g, m, n] bf16            bf16 cast of the momentum lookahead
+ *   d     [g]       fp32            normaliser per matrix
+ *   X     [nmaps+1, g, m, n] bf16   normalised X, then X after each map
+ *   A, B  [nmaps, g, s, s] bf16     per map (s = min(m, n)); A[0] is the
+ *                                   normalised first Gram */
+typedef struct {
+    uint16_t* X_raw;
+    float* d;
+    uint16_t* X;
+    uint16_t* A;
+    uint16_t* B;
+} anvil_trace;
+
+/* anvil_multi_bank_step for one bank, plus the dumps.  Same arguments and
+ * workspace rules; out receives the same result as without tracing. */
+anvil_status anvil_bank_step_traced(const anvil_bank_desc* bank, const anvil_scalars* d_scalars,
+                                    const anvil_map* maps, int nmaps, float margin, float eps,
+                                    void* workspace, size_t workspace_bytes,
+                                    const anvil_trace* trace, void* stream);
+
+/* Reads (and, if clear != 0, resets) the current device's error word, which a
+ * kernel sets when one of its bounded waits gives up instead of hanging.
+ * Synchronises the device.  Returns ANVIL_OK, ANVIL_ERR_TIMEOUT or ANVIL_ERR_CUDA. */
+anvil_status anvil_device_error(int clear);
+
+/* Self-test of the bounded waits: launches one block that waits on a barrier
+ * nothing will ever complete, for at most timeout_us microseconds, after which
+ * it records a timeout in the device error word and returns.  It neither
+ * faults nor hangs the GPU. */
+anvil_status anvil_selftest_wait_timeout(unsigned timeout_us, void* stream);
+
+/* Per-launch timing for benchmarks.  Between anvil_profile_begin and
+ * anvil_profile_end, every kernel launch of anvil_multi_bank_step /
+ * anvil_bank_step on the calling process is bracketed by two CUDA events
+ * recorded on the call's stream (at most max_records launches; later ones are
+ * not timed).  begin creates the events (a host call: do not begin, or step
+ * with profiling on, while a stream is capturing).  end synchronises, writes up
+ * to cap records in launch order, destroys the events and returns how many
+ * launches were timed (negative on a CUDA error). */
+typedef enum {
+    ANVIL_KERNEL_MOMENTUM = 0,     /* momentum + cast + diagonal partials */
+    ANVIL_KERNEL_NORM_D = 1,       /* d per matrix */
+    ANVIL_KERNEL_NORMALIZE = 2,    /* X <- bf16(X / d) */
+    ANVIL_KERNEL_GRAM_NORM = 3,    /* first Gram, A = bf16(bf16(X X^T) / d^2) */
+    ANVIL_KERNEL_GRAM = 4,         /* A = bf16(X X^T) */
+    ANVIL_KERNEL_SQPOLY = 5,       /* B = bf16(b A + c A A) */
+    ANVIL_KERNEL_XUPDATE = 6,      /* X <- bf16(a X + B X) */
+    ANVIL_KERNEL_XUPDATE_OUT = 7   /* the last map's X-update, written to out */
+} anvil_kernel_kind;
+
+typedef struct { int kind; float ms; } anvil_profile_record;
+
+anvil_status anvil_profile_begin(int max_records);
+int anvil_profile_end(anvil_profile_record* records, int cap);
+
+/* Human-readable name of a status. */
+const char* anvil_status_string(anvil_status status);
+
+/* Text of the last CUDA error this library saw on this thread ("" if none). */
+const char* anvil_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ANVIL_H */

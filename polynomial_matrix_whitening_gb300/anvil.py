@@ -1,0 +1,269 @@
+"""Thin ctypes binding of libanvil (include/anvil.h), the ANVIL bank step on GB300.
+
+Argument marshalling only: every step of the computation runs in libanvil's CUDA
+kernels.  Importing this module loads ``libanvil.so`` from this package directory and
+raises ``ImportError`` if it has not been built (``python -c "import __graft_entry__ as
+g; g.build()"``, or ``python polynomial_matrix_whitening_gb300/build.py``); there is no
+fallback of any kind.
+
+Tensors are torch tensors on the current CUDA device: grad fp32 [g, m, n], velocity
+fp32 [2, g, m, n], out bf16 [g, m, n], all contiguous.  Calls are enqueued on
+``torch.cuda.current_stream()`` unless a stream is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libanvil.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "anvil.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libanvil.so is not built ({LIB_PATH}); run the package's build.py")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+STATUS = {0: "ANVIL_OK", 1: "ANVIL_ERR_INVALID_ARG", 2: "ANVIL_ERR_UNSUPPORTED_SHAPE",
+          3: "ANVIL_ERR_ALIGNMENT", 4: "ANVIL_ERR_ALIAS", 5: "ANVIL_ERR_WORKSPACE",
+          6: "ANVIL_ERR_CUDA", 7: "ANVIL_ERR_TIMEOUT", 8: "ANVIL_ERR_DEVICE"}
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_ALIGNMENT, ERR_ALIAS, ERR_WORKSPACE, \
+    ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(9)
+KERNEL_KINDS = ("momentum", "norm_d", "normalize", "gram_norm", "gram", "sqpoly", "xupdate",
+                "xupdate_out")
+MAX_MAPS, MAX_BANKS = 16, 8
+
+
+class AnvilError(RuntimeError):
+    def __init__(self, status, where=""):
+        self.status = status
+        detail = _lib.anvil_last_cuda_error().decode() if status == ERR_CUDA else ""
+        super().__init__(f"{where}: {STATUS.get(status, status)} {detail}".strip())
+
+
+class Map(ctypes.Structure):
+    _fields_ = [("a", ctypes.c_float), ("b", ctypes.c_float), ("c", ctypes.c_float)]
+
+
+class Scalars(ctypes.Structure):
+    _fields_ = [("momentum", ctypes.c_float), ("fast_beta", ctypes.c_float),
+                ("fast_weight", ctypes.c_float), ("slow_beta", ctypes.c_float)]
+
+
+class BankDesc(ctypes.Structure):
+    _fields_ = [("grad", ctypes.c_void_p), ("velocity", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("g", ctypes.c_int), ("m", ctypes.c_int), ("n", ctypes.c_int),
+                ("scalars", Scalars)]
+
+
+class Trace(ctypes.Structure):
+    _fields_ = [("X_raw", ctypes.c_void_p), ("d", ctypes.c_void_p), ("X", ctypes.c_void_p),
+                ("A", ctypes.c_void_p), ("B", ctypes.c_void_p)]
+
+
+class ProfileRecord(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("ms", ctypes.c_float)]
+
+
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_lib.anvil_default_maps.argtypes = [ctypes.POINTER(Map), _i]
+_lib.anvil_default_maps.restype = _i
+_lib.anvil_workspace_bytes.argtypes = [ctypes.POINTER(BankDesc), _i]
+_lib.anvil_workspace_bytes.restype = _sz
+_lib.anvil_multi_bank_step.argtypes = [ctypes.POINTER(BankDesc), _i, _vp, ctypes.POINTER(Map), _i,
+                                       _f, _f, _vp, _sz, _vp]
+_lib.anvil_multi_bank_step.restype = _i
+_lib.anvil_bank_step.argtypes = [_vp, _vp, _i, _i, _i, _f, _f, _f, _f, ctypes.POINTER(Map), _i,
+                                 _f, _f, _vp, _vp]
+_lib.anvil_bank_step.restype = _i
+_lib.anvil_bank_step_traced.argtypes = [ctypes.POINTER(BankDesc), _vp, ctypes.POINTER(Map), _i,
+                                        _f, _f, _vp, _sz, ctypes.POINTER(Trace), _vp]
+_lib.anvil_bank_step_traced.restype = _i
+_lib.anvil_device_error.argtypes = [_i]
+_lib.anvil_device_error.restype = _i
+_lib.anvil_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
+_lib.anvil_selftest_wait_timeout.restype = _i
+_lib.anvil_profile_begin.argtypes = [_i]
+_lib.anvil_profile_begin.restype = _i
+_lib.anvil_profile_end.argtypes = [ctypes.POINTER(ProfileRecord), _i]
+_lib.anvil_profile_end.restype = _i
+_lib.anvil_status_string.argtypes = [_i]
+_lib.anvil_status_string.restype = ctypes.c_char_p
+_lib.anvil_last_cuda_error.restype = ctypes.c_char_p
+
+
+def library():
+    """The loaded ctypes CDLL (for tests that call the C ABI directly)."""
+    return _lib
+
+
+def header_functions(path: str = HEADER):
+    """Names of the functions include/anvil.h declares."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(anvil_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(status, where):
+    if status != OK:
+        raise AnvilError(status, where)
+
+
+def default_maps():
+    """The page's six ANVIL_MAPS as (a, b, c) fp32 triples, as the library holds them."""
+    arr = (Map * 6)()
+    _lib.anvil_default_maps(arr, 6)
+    return [(m.a, m.b, m.c) for m in arr]
+
+
+def _maps_arg(maps):
+    if maps is None:
+        maps = default_maps()
+    maps = list(maps)
+    arr = (Map * len(maps))(*[Map(*[float(x) for x in m]) for m in maps])
+    return arr, len(maps)
+
+
+def _stream_arg(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _desc(grad, velocity, out, scalars=None):
+    import torch
+    assert grad.dtype == torch.float32 and velocity.dtype == torch.float32, "grad/velocity fp32"
+    assert out.dtype == torch.bfloat16, "out is bf16"
+    assert grad.is_contiguous() and velocity.is_contiguous() and out.is_contiguous()
+    g, m, n = grad.shape
+    assert velocity.shape == (2, g, m, n) and out.shape == (g, m, n)
+    s = scalars or {}
+    return BankDesc(grad.data_ptr(), velocity.data_ptr(), out.data_ptr(), g, m, n,
+                    Scalars(float(s.get("momentum", 0.95)), float(s.get("fast_beta", 0.85)),
+                            float(s.get("fast_weight", 0.4385)), float(s.get("slow_beta", 0.98))))
+
+
+def _raw_desc(g, m, n, grad=0, velocity=0, out=0):
+    return BankDesc(grad, velocity, out, g, m, n, Scalars(0.95, 0.85, 0.4385, 0.98))
+
+
+def workspace_bytes(shapes):
+    """Workspace bytes for banks of the given (g, m, n) shapes."""
+    descs = (BankDesc * len(shapes))(*[_raw_desc(*s) for s in shapes])
+    return int(_lib.anvil_workspace_bytes(descs, len(shapes)))
+
+
+def alloc_workspace(shapes, device=None):
+    """A device workspace (uint8 tensor, 256-byte aligned by the caching allocator)."""
+    import torch
+    nbytes = workspace_bytes(shapes)
+    if nbytes == 0:
+        raise AnvilError(ERR_INVALID_ARG, "workspace_bytes")
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+    assert ws.data_ptr() % 256 == 0
+    return ws
+
+
+class Bank:
+    """One bank of a multi-bank step: grad, velocity, out tensors and host scalars."""
+
+    def __init__(self, grad, velocity, out, momentum=0.95, fast_beta=0.85, fast_weight=0.4385,
+                 slow_beta=0.98):
+        self.grad, self.velocity, self.out = grad, velocity, out
+        self.scalars = dict(momentum=momentum, fast_beta=fast_beta, fast_weight=fast_weight,
+                            slow_beta=slow_beta)
+
+    @property
+    def shape(self):
+        return tuple(self.grad.shape)
+
+    def desc(self):
+        return _desc(self.grad, self.velocity, self.out, self.scalars)
+
+
+def multi_bank_step(banks, workspace, maps=None, margin=1.05, eps=1e-6, d_scalars=None,
+                    stream=None):
+    """One ANVIL step over several banks (one grouped launch per phase).
+
+    d_scalars: optional fp32 CUDA tensor [nbanks, 4] (momentum, fast_beta, fast_weight,
+    slow_beta) read on the device when the step runs (for CUDA-graph replays).
+    """
+    descs = (BankDesc * len(banks))(*[b.desc() for b in banks])
+    marr, nm = _maps_arg(maps)
+    dsp = None
+    if d_scalars is not None:
+        assert d_scalars.is_cuda and d_scalars.dtype.is_floating_point and d_scalars.is_contiguous()
+        assert tuple(d_scalars.shape) == (len(banks), 4)
+        dsp = d_scalars.data_ptr()
+    st = _lib.anvil_multi_bank_step(descs, len(banks), dsp, marr, nm, margin, eps,
+                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                    _stream_arg(stream))
+    _check(st, "anvil_multi_bank_step")
+
+
+def bank_step(grad, velocity, out, momentum=0.95, fast_beta=0.85, fast_weight=0.4385,
+              slow_beta=0.98, maps=None, margin=1.05, eps=1e-6, stream=None):
+    """One bank, host scalars, library-owned workspace (the page's anvil_cascade call)."""
+    _desc(grad, velocity, out)
+    g, m, n = grad.shape
+    marr, nm = (None, 0) if maps is None else _maps_arg(maps)
+    st = _lib.anvil_bank_step(grad.data_ptr(), velocity.data_ptr(), g, m, n, momentum, fast_beta,
+                              fast_weight, slow_beta, marr, nm, margin, eps, out.data_ptr(),
+                              _stream_arg(stream))
+    _check(st, "anvil_bank_step")
+
+
+def bank_step_traced(bank: Bank, workspace, maps=None, margin=1.05, eps=1e-6, stream=None):
+    """One bank step with per-stage dumps; returns a dict of torch tensors
+    (X_raw [g,m,n] bf16, d [g] fp32, X [nmaps+1,g,m,n] bf16, A/B [nmaps,g,s,s] bf16)."""
+    import torch
+    g, m, n = bank.shape
+    s = min(m, n)
+    marr, nm = _maps_arg(maps)
+    dev = bank.grad.device
+    t = {"X_raw": torch.empty((g, m, n), dtype=torch.bfloat16, device=dev),
+         "d": torch.empty((g,), dtype=torch.float32, device=dev),
+         "X": torch.empty((nm + 1, g, m, n), dtype=torch.bfloat16, device=dev),
+         "A": torch.empty((nm, g, s, s), dtype=torch.bfloat16, device=dev),
+         "B": torch.empty((nm, g, s, s), dtype=torch.bfloat16, device=dev)}
+    tr = Trace(*(t[k].data_ptr() for k in ("X_raw", "d", "X", "A", "B")))
+    desc = bank.desc()
+    st = _lib.anvil_bank_step_traced(ctypes.byref(desc), None, marr, nm, margin, eps,
+                                     workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                     ctypes.byref(tr),
+                                     _stream_arg(stream))
+    _check(st, "anvil_bank_step_traced")
+    return t
+
+
+def device_error(clear=True):
+    """Status of the device error word (ANVIL_OK or ANVIL_ERR_TIMEOUT); synchronises."""
+    return _lib.anvil_device_error(1 if clear else 0)
+
+
+def selftest_wait_timeout(timeout_us, stream=None):
+    _check(_lib.anvil_selftest_wait_timeout(int(timeout_us), _stream_arg(stream)),
+           "anvil_selftest_wait_timeout")
+
+
+class profile:
+    """Context manager: per-launch CUDA-event timings of the steps run inside it.
+    After exit, ``records`` is a list of (kernel kind name, milliseconds)."""
+
+    def __init__(self, max_records=4096):
+        self.max_records = max_records
+        self.records = []
+
+    def __enter__(self):
+        _check(_lib.anvil_profile_begin(self.max_records), "anvil_profile_begin")
+        return self
+
+    def __exit__(self, *exc):
+        arr = (ProfileRecord * self.max_records)()
+        n = _lib.anvil_profile_end(arr, self.max_records)
+        if n < 0:
+            raise AnvilError(ERR_CUDA, "anvil_profile_end")
+        self.records = [(KERNEL_KINDS[arr[i].kind], arr[i].ms) for i in range(n)]
+        return False

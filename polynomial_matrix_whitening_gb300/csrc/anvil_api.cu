@@ -1,0 +1,663 @@
+// anvil_api.cu -- libanvil's C ABI (include/anvil.h): argument checks, the call-wide
+// workspace layout, TMA tensor maps, and the launch sequence of one ANVIL step
+// (page "modded-nanogpt track_1_short/optim/anvil.py", anvil_cascade):
+//
+//   momentum + cast (+ diagonal partials)   -> Y0 = X_raw
+//   d = sqrt(tr) * margin + eps             (tr from the bf16 diagonal of the first Gram)
+//   A = bf16(bf16(Y0 Y0^T) / d^2)           first Gram, on the unnormalised X
+//   Y0 <- bf16(Y0 / d)
+//   map k = 0..nmaps-1, reading Y[k%2], writing Y[(k+1)%2] (out for the last map):
+//     [k > 0] A = bf16(Y Y^T);  B = bf16(b A + c A A);  Y' = bf16(a Y + B Y)
+//
+// Every phase is one grouped launch over all banks of the call (two when more than
+// four banks), 4 + 3 * nmaps launches in all, on the caller's stream.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/anvil.h"
+#include "anvil_internal.h"
+
+using namespace anvil;
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+anvil_status cuda_fail(cudaError_t e, const char* where) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
+    return ANVIL_ERR_CUDA;
+}
+
+// ANVIL_MAPS as printed on the page (the ANVIL section of anvil.py, record #360).
+const anvil_map kAnvilMaps[6] = {
+    {3.923798038567f, -6.095026865488f, 3.905234618423f},
+    {3.278126713798f, -3.328923386476f, 0.989127286973f},
+    {3.505298394150f, -5.137358782410f, 1.968325560615f},
+    {2.815058591845f, -3.685181239622f, 1.417196497642f},
+    {2.245503932403f, -2.443826979899f, 0.963091710461f},
+    {2.256537145403f, -2.166840097229f, 0.929501253245f},
+};
+
+// ---------------------------------------------------------------- per-device set-up
+struct DeviceState {
+    bool ready = false;
+    anvil_status status = ANVIL_OK;
+    unsigned* err = nullptr;
+};
+std::mutex g_dev_mutex;
+DeviceState g_dev[64];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Checks the device is sm_103, sets kernel attributes, finds the error word and the
+// tensor-map encoder.  Once per device; no allocation, no synchronisation.
+anvil_status device_setup(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return ANVIL_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)))
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if (major != 10 || minor != 3) {
+            snprintf(g_last_error, sizeof(g_last_error),
+                     "device %d is sm_%d%d; libanvil is built for sm_103a only", dev, major, minor);
+            return ANVIL_ERR_DEVICE;
+        }
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+                return cuda_fail(e == cudaSuccess ? cudaErrorSymbolNotFound : e,
+                                 "cuTensorMapEncodeTiled lookup");
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        if ((e = gemm_prepare())) return cuda_fail(e, "cudaFuncSetAttribute");
+        st.err = device_error_word();
+        if (!st.err) return cuda_fail(cudaGetLastError(), "cudaGetSymbolAddress(error word)");
+        st.ready = true;
+    }
+    *out = &st;
+    return ANVIL_OK;
+}
+
+// ---------------------------------------------------------------- launch profiling
+struct Profiler {
+    std::mutex mu;
+    bool active = false;
+    int cap = 0, used = 0;
+    cudaEvent_t* ev = nullptr;  // 2 * cap events
+    int* kind = nullptr;
+};
+Profiler g_prof;
+
+// Runs `launch`, bracketed by two events on `stream` when profiling is on.
+template <class F>
+cudaError_t profiled(int kind, cudaStream_t stream, F&& launch) {
+    int slot = -1;
+    {
+        std::lock_guard<std::mutex> lock(g_prof.mu);
+        if (g_prof.active && g_prof.used < g_prof.cap) slot = g_prof.used++;
+    }
+    cudaError_t e;
+    if (slot >= 0) {
+        g_prof.kind[slot] = kind;
+        if ((e = cudaEventRecord(g_prof.ev[2 * slot], stream))) return e;
+    }
+    if ((e = launch())) return e;
+    if (slot >= 0 && (e = cudaEventRecord(g_prof.ev[2 * slot + 1], stream))) return e;
+    return cudaSuccess;
+}
+
+// ---------------------------------------------------------------- geometry and layout
+struct Geom {
+    int g, m, n, tall, s, L, s_pad, L_pad, nlb, mat_begin;
+    size_t part_off, y_off, a_off;  // element offsets into the call-wide arrays
+};
+
+struct Layout {
+    Geom bank[ANVIL_MAX_BANKS];
+    int nbanks, total_mats;
+    size_t d_bytes, part_elems, y_elems, a_elems;
+    size_t off_d, off_part, off_y0, off_y1, off_a, off_b, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+anvil_status make_layout(const anvil_bank_desc* banks, int nbanks, Layout* L) {
+    if (!banks || nbanks < 1 || nbanks > ANVIL_MAX_BANKS) return ANVIL_ERR_INVALID_ARG;
+    L->nbanks = nbanks;
+    L->total_mats = 0;
+    L->part_elems = L->y_elems = L->a_elems = 0;
+    for (int i = 0; i < nbanks; ++i) {
+        const anvil_bank_desc& b = banks[i];
+        if (b.g < 1 || b.m < 1 || b.n < 1) return ANVIL_ERR_INVALID_ARG;
+        if (b.m > ANVIL_MAX_DIM || b.n > ANVIL_MAX_DIM || b.g > ANVIL_MAX_BATCH)
+            return ANVIL_ERR_UNSUPPORTED_SHAPE;
+        Geom& G = L->bank[i];
+        G.g = b.g;
+        G.m = b.m;
+        G.n = b.n;
+        G.tall = b.m > b.n;
+        G.s = G.tall ? b.n : b.m;
+        G.L = G.tall ? b.m : b.n;
+        G.s_pad = round_up(G.s, TILE);
+        G.L_pad = round_up(G.L, TILE);
+        G.nlb = G.L_pad / LBLK;
+        G.mat_begin = L->total_mats;
+        L->total_mats += b.g;
+        G.part_off = L->part_elems;
+        G.y_off = L->y_elems;
+        G.a_off = L->a_elems;
+        L->part_elems += static_cast<size_t>(b.g) * G.nlb * G.s_pad;
+        L->y_elems += static_cast<size_t>(b.g) * G.s_pad * G.L_pad;
+        L->a_elems += static_cast<size_t>(b.g) * G.s_pad * G.s_pad;
+    }
+    L->off_d = 0;
+    L->off_part = align256(L->off_d + sizeof(float) * L->total_mats);
+    L->off_y0 = align256(L->off_part + sizeof(float) * L->part_elems);
+    L->off_y1 = align256(L->off_y0 + 2 * L->y_elems);
+    L->off_a = align256(L->off_y1 + 2 * L->y_elems);
+    L->off_b = align256(L->off_a + 2 * L->a_elems);
+    L->total = align256(L->off_b + 2 * L->a_elems);
+    return ANVIL_OK;
+}
+
+struct Range {
+    uintptr_t lo, hi;
+};
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+anvil_status check_banks(const anvil_bank_desc* banks, int nbanks, const Layout& L) {
+    Range rg[ANVIL_MAX_BANKS][3];
+    for (int i = 0; i < nbanks; ++i) {
+        const anvil_bank_desc& b = banks[i];
+        if (!b.grad || !b.velocity || !b.out) return ANVIL_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(b.grad) & 3) || (reinterpret_cast<uintptr_t>(b.velocity) & 3) ||
+            (reinterpret_cast<uintptr_t>(b.out) & 1))
+            return ANVIL_ERR_ALIGNMENT;
+        const size_t cnt = static_cast<size_t>(b.g) * b.m * b.n;
+        rg[i][0] = {reinterpret_cast<uintptr_t>(b.grad), reinterpret_cast<uintptr_t>(b.grad + cnt)};
+        rg[i][1] = {reinterpret_cast<uintptr_t>(b.velocity), reinterpret_cast<uintptr_t>(b.velocity + 2 * cnt)};
+        rg[i][2] = {reinterpret_cast<uintptr_t>(b.out), reinterpret_cast<uintptr_t>(b.out + cnt)};
+    }
+    (void)L;
+    // written buffers (velocity, out) must overlap nothing else of the call
+    for (int i = 0; i < nbanks; ++i)
+        for (int w = 1; w <= 2; ++w)
+            for (int j = 0; j < nbanks; ++j)
+                for (int k = 0; k < 3; ++k) {
+                    if (i == j && k == w) continue;
+                    if (overlap(rg[i][w], rg[j][k])) return ANVIL_ERR_ALIAS;
+                }
+    return ANVIL_OK;
+}
+
+anvil_status check_maps(const anvil_map* maps, int nmaps) {
+    if (!maps || nmaps < 1 || nmaps > ANVIL_MAX_MAPS) return ANVIL_ERR_INVALID_ARG;
+    return ANVIL_OK;
+}
+
+// 3-D bf16 tensor map over [g][rows][cols], 128-byte swizzle, box {box0, box1, 1}.
+anvil_status encode_map(CUtensorMap* map, void* base, int g, int rows, int cols, int box0, int box1) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(g)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
+                                   static_cast<cuuint64_t>(rows) * cols * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(box0), static_cast<cuuint32_t>(box1), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed (%d)",
+                 static_cast<int>(r));
+        return ANVIL_ERR_CUDA;
+    }
+    return ANVIL_OK;
+}
+
+// Device pointers of one bank's slices of the workspace.
+struct BankPtrs {
+    uint16_t* y[2];
+    uint16_t* a;
+    uint16_t* b;
+    float* part;
+    float* d;
+    CUtensorMap tm_yk[2], tm_yn[2], tm_a, tm_b;
+};
+
+anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scalars* d_scalars,
+                      const anvil_map* maps, int nmaps, float margin, float eps, void* workspace,
+                      size_t ws_bytes, cudaStream_t stream, const anvil_trace* trace) {
+    // Every argument check comes before any CUDA call.
+    anvil_status st;
+    Layout L;
+    if ((st = make_layout(banks, nbanks, &L)) != ANVIL_OK) return st;
+    if ((st = check_banks(banks, nbanks, L)) != ANVIL_OK) return st;
+    if ((st = check_maps(maps, nmaps)) != ANVIL_OK) return st;
+    if (!workspace || ws_bytes < L.total) return ANVIL_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return ANVIL_ERR_ALIGNMENT;
+    {
+        const Range wr = {reinterpret_cast<uintptr_t>(workspace),
+                          reinterpret_cast<uintptr_t>(workspace) + L.total};
+        for (int i = 0; i < nbanks; ++i) {
+            const size_t cnt = static_cast<size_t>(banks[i].g) * banks[i].m * banks[i].n;
+            const Range r[3] = {{reinterpret_cast<uintptr_t>(banks[i].grad), reinterpret_cast<uintptr_t>(banks[i].grad + cnt)},
+                                {reinterpret_cast<uintptr_t>(banks[i].velocity), reinterpret_cast<uintptr_t>(banks[i].velocity + 2 * cnt)},
+                                {reinterpret_cast<uintptr_t>(banks[i].out), reinterpret_cast<uintptr_t>(banks[i].out + cnt)}};
+            for (int k = 0; k < 3; ++k)
+                if (overlap(wr, r[k])) return ANVIL_ERR_ALIAS;
+        }
+    }
+    if (d_scalars && (reinterpret_cast<uintptr_t>(d_scalars) & 3)) return ANVIL_ERR_ALIGNMENT;
+    DeviceState* dev = nullptr;
+    if ((st = device_setup(&dev)) != ANVIL_OK) return st;
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* d_all = reinterpret_cast<float*>(ws + L.off_d);
+    BankPtrs P[ANVIL_MAX_BANKS];
+    for (int i = 0; i < nbanks; ++i) {
+        const Geom& G = L.bank[i];
+        BankPtrs& B = P[i];
+        B.y[0] = reinterpret_cast<uint16_t*>(ws + L.off_y0) + G.y_off;
+        B.y[1] = reinterpret_cast<uint16_t*>(ws + L.off_y1) + G.y_off;
+        B.a = reinterpret_cast<uint16_t*>(ws + L.off_a) + G.a_off;
+        B.b = reinterpret_cast<uint16_t*>(ws + L.off_b) + G.a_off;
+        B.part = reinterpret_cast<float*>(ws + L.off_part) + G.part_off;
+        B.d = d_all + G.mat_begin;
+        for (int k = 0; k < 2; ++k) {
+            if ((st = encode_map(&B.tm_yk[k], B.y[k], G.g, G.s_pad, G.L_pad, BK, TILE))) return st;
+            if ((st = encode_map(&B.tm_yn[k], B.y[k], G.g, G.s_pad, G.L_pad, BK, BK))) return st;
+        }
+        if ((st = encode_map(&B.tm_a, B.a, G.g, G.s_pad, G.s_pad, BK, TILE))) return st;
+        if ((st = encode_map(&B.tm_b, B.b, G.g, G.s_pad, G.s_pad, BK, TILE))) return st;
+    }
+
+    cudaError_t e;
+    // ---- momentum + cast + diagonal partials
+    {
+        MomentumParams mp;
+        memset(&mp, 0, sizeof(mp));
+        mp.nbanks = nbanks;
+        mp.dev_scalars = reinterpret_cast<const float*>(d_scalars);
+        mp.err = dev->err;
+        int tiles = 0;
+        for (int i = 0; i < nbanks; ++i) {
+            const Geom& G = L.bank[i];
+            const anvil_bank_desc& b = banks[i];
+            MomentumBank& M = mp.bank[i];
+            M.grad = b.grad;
+            M.velocity = b.velocity;
+            M.y = P[i].y[0];
+            M.part = P[i].part;
+            M.g = G.g;
+            M.m = G.m;
+            M.n = G.n;
+            M.tall = G.tall;
+            M.s_pad = G.s_pad;
+            M.L_pad = G.L_pad;
+            M.nlb = G.nlb;
+            M.tiles_r = (G.tall ? G.L_pad : G.s_pad) / LBLK;
+            M.tiles_c = (G.tall ? G.s_pad : G.L_pad) / LBLK;
+            M.tile_begin = tiles;
+            M.vec4 = (G.n % 4 == 0) && !(reinterpret_cast<uintptr_t>(b.grad) & 15) &&
+                     !(reinterpret_cast<uintptr_t>(b.velocity) & 15);
+            M.momentum = b.scalars.momentum;
+            M.fast_beta = b.scalars.fast_beta;
+            M.fast_weight = b.scalars.fast_weight;
+            M.slow_beta = b.scalars.slow_beta;
+            tiles += G.g * M.tiles_r * M.tiles_c;
+        }
+        mp.total_tiles = tiles;
+        if ((e = profiled(ANVIL_KERNEL_MOMENTUM, stream, [&] { return launch_momentum(mp, stream); })))
+            return cuda_fail(e, "momentum launch");
+    }
+    // ---- d
+    NormParams np;
+    memset(&np, 0, sizeof(np));
+    np.nbanks = nbanks;
+    np.total_mats = L.total_mats;
+    np.margin = margin;
+    np.eps = eps;
+    np.d = d_all;
+    np.err = dev->err;
+    {
+        long long vecs = 0;
+        for (int i = 0; i < nbanks; ++i) {
+            const Geom& G = L.bank[i];
+            NormBank& N = np.bank[i];
+            N.y = P[i].y[0];
+            N.part = P[i].part;
+            N.g = G.g;
+            N.s_pad = G.s_pad;
+            N.L_pad = G.L_pad;
+            N.nlb = G.nlb;
+            N.mat_begin = G.mat_begin;
+            N.vec_begin = vecs;
+            vecs += static_cast<long long>(G.g) * G.s_pad * G.L_pad / 8;
+        }
+        np.total_vecs = vecs;
+    }
+    if ((e = profiled(ANVIL_KERNEL_NORM_D, stream, [&] { return launch_norm_d(np, stream); })))
+        return cuda_fail(e, "norm_d launch");
+    if (trace) {
+        const Geom& G = L.bank[0];
+        if (trace->X_raw && (e = launch_extract_x(P[0].y[0], trace->X_raw, G.g, G.m, G.n, G.tall,
+                                                  G.s_pad, G.L_pad, stream)))
+            return cuda_fail(e, "trace");
+        if (trace->d && (e = cudaMemcpyAsync(trace->d, P[0].d, sizeof(float) * G.g,
+                                             cudaMemcpyDeviceToDevice, stream)))
+            return cuda_fail(e, "trace");
+    }
+
+    // GEMM banks, heaviest tiles first within each launch group.
+    int order[ANVIL_MAX_BANKS];
+    for (int i = 0; i < nbanks; ++i) order[i] = i;
+    std::stable_sort(order, order + nbanks, [&](int x, int y) {
+        const long long wx = static_cast<long long>(L.bank[x].s_pad) * L.bank[x].L_pad;
+        const long long wy = static_cast<long long>(L.bank[y].s_pad) * L.bank[y].L_pad;
+        return wx > wy;
+    });
+
+    auto gemm_phase = [&](GemmOp op, int k, const anvil_map& mp) -> anvil_status {
+        for (int first = 0; first < nbanks; first += MAX_LAUNCH_BANKS) {
+            GemmParams gp;
+            memset(&gp, 0, sizeof(gp));
+            gp.a = mp.a;
+            gp.b = mp.b;
+            gp.c = mp.c;
+            gp.err = dev->err;
+            int tiles = 0, nb = 0;
+            for (int q = first; q < nbanks && q < first + MAX_LAUNCH_BANKS; ++q, ++nb) {
+                const int i = order[q];
+                const Geom& G = L.bank[i];
+                const BankPtrs& B = P[i];
+                GemmBank& gb = gp.bank[nb];
+                const int cur = k & 1;
+                gb.g = G.g;
+                gb.s_pad = G.s_pad;
+                gb.L_pad = G.L_pad;
+                gb.m = G.m;
+                gb.n = G.n;
+                gb.tall = G.tall;
+                gb.T = G.s_pad / TILE;
+                gb.d = B.d;
+                switch (op) {
+                    case OP_GRAM:
+                    case OP_GRAM_NORM:
+                        gb.tm_a = B.tm_yk[cur];
+                        gb.tm_b = B.tm_yk[cur];
+                        gb.dst = B.a;
+                        gb.nt_n = gb.T;
+                        gb.tiles_per_mat = gb.T * (gb.T + 1) / 2;
+                        gb.num_kb = G.L_pad / BK;
+                        break;
+                    case OP_SQPOLY:
+                        gb.tm_a = B.tm_a;
+                        gb.tm_b = B.tm_a;
+                        gb.src = B.a;
+                        gb.dst = B.b;
+                        gb.nt_n = gb.T;
+                        gb.tiles_per_mat = gb.T * (gb.T + 1) / 2;
+                        gb.num_kb = G.s_pad / BK;
+                        break;
+                    case OP_XUPDATE:
+                    case OP_XUPDATE_OUT:
+                        gb.tm_a = B.tm_b;
+                        gb.tm_b = B.tm_yn[cur];
+                        gb.src = B.y[cur];
+                        gb.dst = op == OP_XUPDATE ? B.y[cur ^ 1] : banks[i].out;
+                        gb.nt_n = G.L_pad / TILE;
+                        gb.tiles_per_mat = gb.T * gb.nt_n;
+                        gb.num_kb = G.s_pad / BK;
+                        break;
+                }
+                gb.tile_begin = tiles;
+                tiles += G.g * gb.tiles_per_mat;
+            }
+            gp.nbanks = nb;
+            gp.total_tiles = tiles;
+            static const int kinds[5] = {ANVIL_KERNEL_GRAM, ANVIL_KERNEL_GRAM_NORM, ANVIL_KERNEL_SQPOLY,
+                                         ANVIL_KERNEL_XUPDATE, ANVIL_KERNEL_XUPDATE_OUT};
+            cudaError_t ee = profiled(kinds[op], stream, [&] { return launch_gemm(op, gp, stream); });
+            if (ee) return cuda_fail(ee, "gemm launch");
+        }
+        return ANVIL_OK;
+    };
+
+    const anvil_map none = {0.f, 0.f, 0.f};
+    if ((st = gemm_phase(OP_GRAM_NORM, 0, none))) return st;
+    if ((e = profiled(ANVIL_KERNEL_NORMALIZE, stream, [&] { return launch_normalize(np, stream); })))
+        return cuda_fail(e, "normalize launch");
+    const Geom& G0 = L.bank[0];
+    const size_t nx1 = static_cast<size_t>(G0.g) * G0.m * G0.n;
+    const size_t na1 = static_cast<size_t>(G0.g) * G0.s * G0.s;
+    if (trace && trace->X &&
+        (e = launch_extract_x(P[0].y[0], trace->X, G0.g, G0.m, G0.n, G0.tall, G0.s_pad, G0.L_pad, stream)))
+        return cuda_fail(e, "trace");
+    for (int k = 0; k < nmaps; ++k) {
+        if (k > 0 && (st = gemm_phase(OP_GRAM, k, maps[k]))) return st;
+        if (trace && trace->A &&
+            (e = launch_extract_sq(P[0].a, trace->A + k * na1, G0.g, G0.s, G0.s_pad, stream)))
+            return cuda_fail(e, "trace");
+        if ((st = gemm_phase(OP_SQPOLY, k, maps[k]))) return st;
+        if (trace && trace->B &&
+            (e = launch_extract_sq(P[0].b, trace->B + k * na1, G0.g, G0.s, G0.s_pad, stream)))
+            return cuda_fail(e, "trace");
+        const bool last = k == nmaps - 1;
+        if ((st = gemm_phase(last ? OP_XUPDATE_OUT : OP_XUPDATE, k, maps[k]))) return st;
+        if (trace && trace->X) {
+            if (last) {
+                if ((e = cudaMemcpyAsync(trace->X + (k + 1) * nx1, banks[0].out, 2 * nx1,
+                                         cudaMemcpyDeviceToDevice, stream)))
+                    return cuda_fail(e, "trace");
+            } else if ((e = launch_extract_x(P[0].y[(k + 1) & 1], trace->X + (k + 1) * nx1, G0.g,
+                                             G0.m, G0.n, G0.tall, G0.s_pad, G0.L_pad, stream))) {
+                return cuda_fail(e, "trace");
+            }
+        }
+    }
+    return ANVIL_OK;
+}
+
+// ---------------------------------------------------------------- library-owned workspace
+struct OwnedWorkspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mutex;
+OwnedWorkspace g_ws[64];
+
+}  // namespace
+
+extern "C" {
+
+int anvil_default_maps(anvil_map* maps, int cap) {
+    if (maps && cap >= 6) memcpy(maps, kAnvilMaps, sizeof(kAnvilMaps));
+    return 6;
+}
+
+size_t anvil_workspace_bytes(const anvil_bank_desc* banks, int nbanks) {
+    Layout L;
+    if (make_layout(banks, nbanks, &L) != ANVIL_OK) return 0;
+    return L.total;
+}
+
+anvil_status anvil_multi_bank_step(const anvil_bank_desc* banks, int nbanks,
+                                   const anvil_scalars* d_scalars, const anvil_map* maps,
+                                   int nmaps, float margin, float eps, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+    return run_step(banks, nbanks, d_scalars, maps, nmaps, margin, eps, workspace,
+                    workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+anvil_status anvil_bank_step_traced(const anvil_bank_desc* bank, const anvil_scalars* d_scalars,
+                                    const anvil_map* maps, int nmaps, float margin, float eps,
+                                    void* workspace, size_t workspace_bytes,
+                                    const anvil_trace* trace, void* stream) {
+    if (!trace) return ANVIL_ERR_INVALID_ARG;
+    return run_step(bank, 1, d_scalars, maps, nmaps, margin, eps, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream), trace);
+}
+
+anvil_status anvil_bank_step(const float* grad, float* velocity, int g, int m, int n,
+                             float momentum, float fast_beta, float fast_weight, float slow_beta,
+                             const anvil_map* maps, int nmaps, float margin, float eps,
+                             uint16_t* out, void* stream) {
+    anvil_bank_desc b;
+    b.grad = grad;
+    b.velocity = velocity;
+    b.out = out;
+    b.g = g;
+    b.m = m;
+    b.n = n;
+    b.scalars.momentum = momentum;
+    b.scalars.fast_beta = fast_beta;
+    b.scalars.fast_weight = fast_weight;
+    b.scalars.slow_beta = slow_beta;
+    if (!maps) {
+        maps = kAnvilMaps;
+        nmaps = 6;
+    }
+    const size_t need = anvil_workspace_bytes(&b, 1);
+    if (need == 0) return ANVIL_ERR_INVALID_ARG;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return ANVIL_ERR_DEVICE;
+    void* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_ws_mutex);
+        OwnedWorkspace& w = g_ws[dev];
+        if (w.bytes < need) {
+            cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+            if ((e = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs)))
+                return cuda_fail(e, "cudaStreamIsCapturing");
+            if (cs != cudaStreamCaptureStatusNone) return ANVIL_ERR_WORKSPACE;
+            if (w.ptr) {
+                if ((e = cudaFree(w.ptr))) return cuda_fail(e, "cudaFree");
+                w.ptr = nullptr;
+                w.bytes = 0;
+            }
+            if ((e = cudaMalloc(&w.ptr, need))) {
+                w.ptr = nullptr;
+                return cuda_fail(e, "cudaMalloc(workspace)");
+            }
+            w.bytes = need;
+        }
+        ws = w.ptr;
+    }
+    return run_step(&b, 1, nullptr, maps, nmaps, margin, eps, ws, need,
+                    static_cast<cudaStream_t>(stream), nullptr);
+}
+
+anvil_status anvil_device_error(int clear) {
+    DeviceState* dev = nullptr;
+    anvil_status st = device_setup(&dev);
+    if (st != ANVIL_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e) return cuda_fail(e, "cudaDeviceSynchronize");
+    unsigned word = 0;
+    if ((e = cudaMemcpy(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost)))
+        return cuda_fail(e, "read error word");
+    if (clear && (e = cudaMemset(dev->err, 0, sizeof(unsigned))))
+        return cuda_fail(e, "clear error word");
+    if (clear && (e = cudaDeviceSynchronize())) return cuda_fail(e, "cudaDeviceSynchronize");
+    return (word & DEVERR_TIMEOUT) ? ANVIL_ERR_TIMEOUT : ANVIL_OK;
+}
+
+anvil_status anvil_selftest_wait_timeout(unsigned timeout_us, void* stream) {
+    DeviceState* dev = nullptr;
+    anvil_status st = device_setup(&dev);
+    if (st != ANVIL_OK) return st;
+    if (timeout_us == 0 || timeout_us > 10000000u) return ANVIL_ERR_INVALID_ARG;
+    cudaError_t e = launch_wait_selftest(timeout_us, dev->err, static_cast<cudaStream_t>(stream));
+    return e ? cuda_fail(e, "selftest launch") : ANVIL_OK;
+}
+
+anvil_status anvil_profile_begin(int max_records) {
+    if (max_records < 1 || max_records > (1 << 20)) return ANVIL_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    if (g_prof.active) return ANVIL_ERR_INVALID_ARG;
+    g_prof.ev = new cudaEvent_t[2 * static_cast<size_t>(max_records)];
+    g_prof.kind = new int[max_records];
+    for (int i = 0; i < 2 * max_records; ++i) {
+        cudaError_t e = cudaEventCreate(&g_prof.ev[i]);
+        if (e) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(g_prof.ev[j]);
+            delete[] g_prof.ev;
+            delete[] g_prof.kind;
+            g_prof.ev = nullptr;
+            g_prof.kind = nullptr;
+            return cuda_fail(e, "cudaEventCreate");
+        }
+    }
+    g_prof.cap = max_records;
+    g_prof.used = 0;
+    g_prof.active = true;
+    return ANVIL_OK;
+}
+
+int anvil_profile_end(anvil_profile_record* records, int cap) {
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    if (!g_prof.active) return 0;
+    int n = g_prof.used, rc = n;
+    for (int i = 0; i < n; ++i) {
+        cudaError_t e = cudaEventSynchronize(g_prof.ev[2 * i + 1]);
+        float ms = 0.f;
+        if (!e) e = cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]);
+        if (e) {
+            cuda_fail(e, "profile events");
+            rc = -1;
+            break;
+        }
+        if (records && i < cap) {
+            records[i].kind = g_prof.kind[i];
+            records[i].ms = ms;
+        }
+    }
+    for (int i = 0; i < 2 * g_prof.cap; ++i) cudaEventDestroy(g_prof.ev[i]);
+    delete[] g_prof.ev;
+    delete[] g_prof.kind;
+    g_prof.ev = nullptr;
+    g_prof.kind = nullptr;
+    g_prof.active = false;
+    g_prof.cap = g_prof.used = 0;
+    return rc;
+}
+
+const char* anvil_status_string(anvil_status s) {
+    switch (s) {
+        case ANVIL_OK: return "ANVIL_OK";
+        case ANVIL_ERR_INVALID_ARG: return "ANVIL_ERR_INVALID_ARG";
+        case ANVIL_ERR_UNSUPPORTED_SHAPE: return "ANVIL_ERR_UNSUPPORTED_SHAPE";
+        case ANVIL_ERR_ALIGNMENT: return "ANVIL_ERR_ALIGNMENT";
+        case ANVIL_ERR_ALIAS: return "ANVIL_ERR_ALIAS";
+        case ANVIL_ERR_WORKSPACE: return "ANVIL_ERR_WORKSPACE";
+        case ANVIL_ERR_CUDA: return "ANVIL_ERR_CUDA";
+        case ANVIL_ERR_TIMEOUT: return "ANVIL_ERR_TIMEOUT";
+        case ANVIL_ERR_DEVICE: return "ANVIL_ERR_DEVICE";
+    }
+    return "ANVIL_ERR_UNKNOWN";
+}
+
+const char* anvil_last_cuda_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,300 @@
+// anvil_elementwise.cu -- the HBM-bound kernels of the ANVIL bank step:
+//   * momentum_kernel: twin-rail Nesterov momentum + bf16 cast (page "modded-nanogpt
+//     track_1_short/optim/anvil.py", anvil_cascade, first block), writing X in the
+//     small-side-major working layout and the per-64-block sums of squares of the bf16
+//     values, from which the first Gram's diagonal (hence the trace) is read;
+//   * norm_d_kernel: d = sqrt(tr) * FROBENIUS_MARGIN + FROBENIUS_EPS per matrix;
+//   * normalize_kernel: X <- bf16(X / d) in place;
+//   * extraction kernels for the traced (parity-test) path and the wait self-test.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "anvil_device.cuh"
+#include "anvil_internal.h"
+
+namespace anvil {
+
+__device__ unsigned g_error_word;
+
+// One 64x64 tile of the padded natural extent of one matrix per block, 256 threads.
+// Thread (tx, ty) = (tid % 16, tid / 16) handles columns c0 + 4 tx .. +3 of rows
+// r0 + ty + 16 k, k = 0..3.  Every rounding matches the page's fp32 tensor ops one
+// operation at a time (no fused multiply-add): lerp(s, e, w) = s + w (e - s).
+__global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ MomentumParams p) {
+    __shared__ __align__(16) uint16_t tileT[64][64 + 8];  // tall: [s-index][L-index]
+
+    const int t = blockIdx.x;
+    int bi = 0;
+#pragma unroll 1
+    for (int i = 1; i < p.nbanks; ++i)
+        if (t >= p.bank[i].tile_begin) bi = i;
+    const MomentumBank& B = p.bank[bi];
+    const int local = t - B.tile_begin;
+    const int per_mat = B.tiles_r * B.tiles_c;
+    const int mat = local / per_mat;
+    const int rem = local - mat * per_mat;
+    const int tr = rem / B.tiles_c, tc = rem - (rem / B.tiles_c) * B.tiles_c;
+    const int r0 = tr * 64, c0 = tc * 64;
+
+    float mom = B.momentum, fbeta = B.fast_beta, fw = B.fast_weight, sbeta = B.slow_beta;
+    if (p.dev_scalars) {
+        const float* s = p.dev_scalars + 4 * bi;
+        mom = s[0];
+        fbeta = s[1];
+        fw = s[2];
+        sbeta = s[3];
+    }
+    const float wf = __fsub_rn(1.0f, fbeta);
+    const float ws = __fsub_rn(1.0f, sbeta);
+    const float omw = __fsub_rn(1.0f, fw);
+
+    const int m = B.m, n = B.n;
+    const size_t mn = static_cast<size_t>(m) * n;
+    const float* G = B.grad + static_cast<size_t>(mat) * mn;
+    float* V0 = B.velocity + static_cast<size_t>(mat) * mn;
+    float* V1 = V0 + static_cast<size_t>(B.g) * mn;
+    uint16_t* Y = B.y + static_cast<size_t>(mat) * B.s_pad * B.L_pad;
+    float* part = B.part + static_cast<size_t>(mat) * B.nlb * B.s_pad;
+
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int c = c0 + 4 * tx;
+
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = r0 + ty + 16 * k;
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (r < m) {
+            const size_t base = static_cast<size_t>(r) * n + c;
+            float g[4] = {0.f, 0.f, 0.f, 0.f}, v0[4] = {0.f, 0.f, 0.f, 0.f}, v1[4] = {0.f, 0.f, 0.f, 0.f};
+            bool in[4];
+            if (B.vec4) {
+                const bool row_in = c < n;  // n % 4 == 0: all four or none
+                if (row_in) {
+                    const float4 g4 = __ldcs(reinterpret_cast<const float4*>(G + base));
+                    const float4 a4 = __ldcs(reinterpret_cast<const float4*>(V0 + base));
+                    const float4 b4 = __ldcs(reinterpret_cast<const float4*>(V1 + base));
+                    g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
+                    v0[0] = a4.x; v0[1] = a4.y; v0[2] = a4.z; v0[3] = a4.w;
+                    v1[0] = b4.x; v1[1] = b4.y; v1[2] = b4.z; v1[3] = b4.w;
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) in[q] = row_in;
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    in[q] = c + q < n;
+                    g[q] = in[q] ? G[base + q] : 0.f;
+                    v0[q] = in[q] ? V0[base + q] : 0.f;
+                    v1[q] = in[q] ? V1[base + q] : 0.f;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float a = __fadd_rn(v0[q], __fmul_rn(wf, __fsub_rn(g[q], v0[q])));
+                const float b = __fadd_rn(v1[q], __fmul_rn(ws, __fsub_rn(g[q], v1[q])));
+                v0[q] = a;
+                v1[q] = b;
+                const float blend = __fadd_rn(__fmul_rn(fw, a), __fmul_rn(omw, b));
+                const float y = __fadd_rn(g[q], __fmul_rn(mom, __fsub_rn(blend, g[q])));
+                x[q] = in[q] ? round_bf(y) : 0.f;
+            }
+            if (B.vec4) {
+                if (in[0]) {
+                    __stcs(reinterpret_cast<float4*>(V0 + base), make_float4(v0[0], v0[1], v0[2], v0[3]));
+                    __stcs(reinterpret_cast<float4*>(V1 + base), make_float4(v1[0], v1[1], v1[2], v1[3]));
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (in[q]) {
+                        V0[base + q] = v0[q];
+                        V1[base + q] = v1[q];
+                    }
+            }
+        }
+        if (!B.tall) {
+            // wide: Y = X, row r, columns c..c+3 (inside the padded extent by construction)
+            uint2 pk;
+            pk.x = static_cast<uint32_t>(f2bf(x[0])) | (static_cast<uint32_t>(f2bf(x[1])) << 16);
+            pk.y = static_cast<uint32_t>(f2bf(x[2])) | (static_cast<uint32_t>(f2bf(x[3])) << 16);
+            *reinterpret_cast<uint2*>(Y + static_cast<size_t>(r) * B.L_pad + c) = pk;
+            // sum of squares of this row over the tile's 64 columns (16 lanes share a row)
+            float sq = __fadd_rn(__fadd_rn(__fmul_rn(x[0], x[0]), __fmul_rn(x[1], x[1])),
+                                 __fadd_rn(__fmul_rn(x[2], x[2]), __fmul_rn(x[3], x[3])));
+#pragma unroll
+            for (int off = 8; off >= 1; off >>= 1) sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, off));
+            if (tx == 0) part[static_cast<size_t>(tc) * B.s_pad + r] = sq;
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tileT[4 * tx + q][ty + 16 * k] = f2bf(x[q]);
+        }
+    }
+    if (B.tall) {
+        __syncthreads();
+        // tall: Y = X^T; Y row (c0 + cl) gets the 64 L-indices r0 .. r0+63 of this tile
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int cl = ty + 16 * k;
+            const uint2 pk = *reinterpret_cast<const uint2*>(&tileT[cl][4 * tx]);
+            *reinterpret_cast<uint2*>(Y + static_cast<size_t>(c0 + cl) * B.L_pad + r0 + 4 * tx) = pk;
+        }
+        // sum of squares of each s-index over the tile's 64 L-indices: 4 threads per index
+        const int cl = threadIdx.x >> 2, qq = threadIdx.x & 3;
+        float sq = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float v = bf2f(tileT[cl][16 * qq + j]);
+            sq = __fadd_rn(sq, __fmul_rn(v, v));
+        }
+        sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, 1));
+        sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, 2));
+        if (qq == 0) part[static_cast<size_t>(tr) * B.s_pad + c0 + cl] = sq;
+    }
+}
+
+cudaError_t launch_momentum(const MomentumParams& p, cudaStream_t stream) {
+    momentum_kernel<<<p.total_tiles, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// One block per matrix.  Diagonal entry i of the first Gram is the fp32 sum of the
+// squares of row i of Y, rounded to bf16 as the page stores the Gram; the trace sums
+// those in fp32.
+__global__ void __launch_bounds__(256) norm_d_kernel(const __grid_constant__ NormParams p) {
+    __shared__ float red[256];
+    const int gm = blockIdx.x;
+    int bi = 0;
+#pragma unroll 1
+    for (int i = 1; i < p.nbanks; ++i)
+        if (gm >= p.bank[i].mat_begin) bi = i;
+    const NormBank& B = p.bank[bi];
+    const int lm = gm - B.mat_begin;
+    const float* part = B.part + static_cast<size_t>(lm) * B.nlb * B.s_pad;
+    float acc = 0.f;
+    for (int i = threadIdx.x; i < B.s_pad; i += blockDim.x) {
+        float s = 0.f;
+        for (int lb = 0; lb < B.nlb; ++lb) s = __fadd_rn(s, part[static_cast<size_t>(lb) * B.s_pad + i]);
+        acc = __fadd_rn(acc, round_bf(s));
+    }
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] = __fadd_rn(red[threadIdx.x], red[threadIdx.x + w]);
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const float tr = red[0];
+        p.d[gm] = __fadd_rn(__fmul_rn(__fsqrt_rn(tr), p.margin), p.eps);
+    }
+}
+
+cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream) {
+    norm_d_kernel<<<p.total_mats, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// Y <- bf16(float(Y) / d) over 8-element (16-byte) vectors, grid-stride over all banks.
+__global__ void __launch_bounds__(256) normalize_kernel(const __grid_constant__ NormParams p) {
+    for (long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+         v < p.total_vecs; v += static_cast<long long>(gridDim.x) * blockDim.x) {
+        int bi = 0;
+#pragma unroll 1
+        for (int i = 1; i < p.nbanks; ++i)
+            if (v >= p.bank[i].vec_begin) bi = i;
+        const NormBank& B = p.bank[bi];
+        const long long lv = v - B.vec_begin;
+        const long long per_mat = static_cast<long long>(B.s_pad) * B.L_pad / 8;
+        const int lm = static_cast<int>(lv / per_mat);
+        const float d = p.d[B.mat_begin + lm];
+        uint4* ptr = reinterpret_cast<uint4*>(B.y) + lv;
+        uint4 u = *ptr;
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float lo = __fdiv_rn(bf2f(static_cast<uint16_t>(w[q] & 0xffffu)), d);
+            const float hi = __fdiv_rn(bf2f(static_cast<uint16_t>(w[q] >> 16)), d);
+            w[q] = static_cast<uint32_t>(f2bf(lo)) | (static_cast<uint32_t>(f2bf(hi)) << 16);
+        }
+        *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+cudaError_t launch_normalize(const NormParams& p, cudaStream_t stream) {
+    long long blocks = (p.total_vecs + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    normalize_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- tracing
+__global__ void extract_x_kernel(const uint16_t* __restrict__ y, uint16_t* __restrict__ dst, int g,
+                                 int m, int n, int tall, int s_pad, int L_pad) {
+    const long long total = static_cast<long long>(g) * m * n;
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int c = static_cast<int>(e % n);
+        const int r = static_cast<int>((e / n) % m);
+        const int mat = static_cast<int>(e / (static_cast<long long>(m) * n));
+        const int i = tall ? c : r, l = tall ? r : c;
+        dst[e] = y[(static_cast<size_t>(mat) * s_pad + i) * L_pad + l];
+    }
+}
+
+cudaError_t launch_extract_x(const uint16_t* y, uint16_t* dst, int g, int m, int n, int tall,
+                             int s_pad, int L_pad, cudaStream_t stream) {
+    extract_x_kernel<<<1024, 256, 0, stream>>>(y, dst, g, m, n, tall, s_pad, L_pad);
+    return cudaGetLastError();
+}
+
+__global__ void extract_sq_kernel(const uint16_t* __restrict__ src, uint16_t* __restrict__ dst,
+                                  int g, int s, int s_pad) {
+    const long long total = static_cast<long long>(g) * s * s;
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int j = static_cast<int>(e % s);
+        const int i = static_cast<int>((e / s) % s);
+        const int mat = static_cast<int>(e / (static_cast<long long>(s) * s));
+        dst[e] = src[(static_cast<size_t>(mat) * s_pad + i) * s_pad + j];
+    }
+}
+
+cudaError_t launch_extract_sq(const uint16_t* src, uint16_t* dst, int g, int s, int s_pad,
+                              cudaStream_t stream) {
+    extract_sq_kernel<<<1024, 256, 0, stream>>>(src, dst, g, s, s_pad);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- bounded-wait self-test
+// Waits on an mbarrier that nothing ever completes; the bounded wait gives up after
+// limit_ns, records DEVERR_TIMEOUT and the kernel returns normally.
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, unsigned* err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, err, limit_ns);
+    __syncthreads();
+}
+
+cudaError_t launch_wait_selftest(unsigned timeout_us, unsigned* err, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(timeout_us) * 1000ull,
+                                               err);
+    return cudaGetLastError();
+}
+
+unsigned* device_error_word() {
+    static unsigned* cache[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cache[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<unsigned*>(ptr);
+    }
+    return cache[dev];
+}
+
+}  // namespace anvil

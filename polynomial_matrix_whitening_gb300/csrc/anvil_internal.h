@@ -1,0 +1,117 @@
+// anvil_internal.h -- kernel parameter blocks and launchers shared by libanvil's
+// translation units (not part of the public ABI).
+//
+// Working layout.  Every matrix is carried in small-side-major form Y [s_pad, L_pad]
+// (s = min(m, n) rows, L = max(m, n) columns, row-major, bf16): Y = X for a wide
+// matrix (m <= n) and Y = X^T for a tall one.  Both branches of the page's cascade
+// are then the same three products,
+//     A = Y Y^T,   B = b A + c A A,   Y <- a Y + B Y,
+// because for a tall X, X^T X = Y Y^T and (a X + X B)^T = a Y + B Y (B is symmetric).
+// s_pad and L_pad round s and L up to the 128-wide tile; the padding is zero and
+// stays zero through every step (zero rows and columns of Y give zero rows and
+// columns of A and B), so it changes no result.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace anvil {
+
+constexpr int TILE = 128;            // GEMM tile (M = N = 128) and the padding unit
+constexpr int BK = 64;               // GEMM k-block: one 128-byte swizzle row of bf16
+constexpr int LBLK = 64;             // momentum-kernel tile edge; one diagonal partial each
+constexpr int MAX_BANKS = 8;         // banks per call
+constexpr int MAX_LAUNCH_BANKS = 4;  // banks grouped into one GEMM launch
+
+inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+// Bits of the device error word (set with atomicOr, read by anvil_device_error).
+enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_BOUNDS = 2u };
+
+// ---------------------------------------------------------------- momentum + cast
+struct MomentumBank {
+    const float* grad;   // [g, m, n]
+    float* velocity;     // [2, g, m, n]
+    uint16_t* y;         // Y_raw [g, s_pad, L_pad]
+    float* part;         // [g, nlb, s_pad]: sums of squares of the bf16 values per 64-block
+    int g, m, n, tall, s_pad, L_pad, nlb;
+    int tiles_r, tiles_c;  // 64x64 tiles over the padded natural extent [rows, cols]
+    int tile_begin;        // first tile of this bank in the grouped grid
+    int vec4;              // n % 4 == 0 and 16-byte aligned grad/velocity: float4 path
+    float momentum, fast_beta, fast_weight, slow_beta;
+};
+struct MomentumParams {
+    MomentumBank bank[MAX_BANKS];
+    int nbanks, total_tiles;
+    const float* dev_scalars;  // [nbanks][4] on the device, or null
+    unsigned* err;
+};
+cudaError_t launch_momentum(const MomentumParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------- d and normalisation
+struct NormBank {
+    uint16_t* y;        // [g, s_pad, L_pad]
+    const float* part;  // [g, nlb, s_pad]
+    int g, s_pad, L_pad, nlb;
+    int mat_begin;      // first matrix of this bank among all matrices of the call
+    long long vec_begin;  // first 8-element vector of this bank in the grouped grid
+};
+struct NormParams {
+    NormBank bank[MAX_BANKS];
+    int nbanks, total_mats;
+    long long total_vecs;
+    float margin, eps;
+    float* d;  // [total_mats]
+    unsigned* err;
+};
+// d[mat] = sqrt(sum_i float(bf16(sum of the partials of i))) * margin + eps.
+cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream);
+// Y <- bf16(float(Y) / d[mat]) in place over every bank.
+cudaError_t launch_normalize(const NormParams& p, cudaStream_t stream);
+
+// ---------------------------------------------------------------- tcgen05 GEMMs
+enum GemmOp : int {
+    OP_GRAM = 0,        // A = bf16(Y Y^T)                    (upper tiles, mirrored)
+    OP_GRAM_NORM = 1,   // A = bf16(bf16(Y Y^T) / d^2)        (the first Gram)
+    OP_SQPOLY = 2,      // B = bf16(b A + c A A)              (upper tiles, mirrored)
+    OP_XUPDATE = 3,     // Y' = bf16(a Y + B Y)
+    OP_XUPDATE_OUT = 4  // the same, written to out in the natural [m, n] layout
+};
+
+struct GemmBank {
+    CUtensorMap tm_a;     // A operand, K-major, box {64, 128, 1}
+    CUtensorMap tm_b;     // B operand: K-major box {64, 128, 1}, or (xupdate) MN-major {64, 64, 1}
+    const uint16_t* src;  // epilogue input: A (sqpoly) or Y (xupdate)
+    uint16_t* dst;        // output
+    const float* d;       // [g] normaliser of this bank's matrices (gram_norm)
+    int g, s_pad, L_pad, m, n, tall;
+    int T;                // s_pad / TILE
+    int nt_n;             // output tiles along N (T for sym ops, L_pad / TILE for xupdate)
+    int tiles_per_mat;
+    int tile_begin;
+    int num_kb;           // k-blocks of BK
+};
+struct GemmParams {
+    GemmBank bank[MAX_LAUNCH_BANKS];
+    int nbanks, total_tiles;
+    float a, b, c;
+    unsigned* err;
+};
+cudaError_t launch_gemm(GemmOp op, const GemmParams& p, cudaStream_t stream);
+cudaError_t gemm_prepare();  // sets the GEMM kernels' shared-memory limit on this device
+
+// ---------------------------------------------------------------- tracing / self-test
+// dst [g, m, n] (natural layout) <- Y [g, s_pad, L_pad] (small-side-major), bf16.
+cudaError_t launch_extract_x(const uint16_t* y, uint16_t* dst, int g, int m, int n, int tall,
+                             int s_pad, int L_pad, cudaStream_t stream);
+// dst [g, s, s] <- src [g, s_pad, s_pad], bf16.
+cudaError_t launch_extract_sq(const uint16_t* src, uint16_t* dst, int g, int s, int s_pad,
+                              cudaStream_t stream);
+cudaError_t launch_wait_selftest(unsigned timeout_us, unsigned* err, cudaStream_t stream);
+
+// Device address of the current device's error word (null if it cannot be had).
+unsigned* device_error_word();
+
+}  // namespace anvil

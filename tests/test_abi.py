@@ -1,0 +1,97 @@
+"""Host-side checks of libanvil's C ABI that need no GPU: the library loads, exports
+every function include/anvil.h declares, holds the page's ANVIL_MAPS, and rejects bad
+arguments with the documented status before it makes any CUDA call."""
+import ctypes
+
+import numpy as np
+import pytest
+
+anvil = pytest.importorskip("polynomial_matrix_whitening_gb300.anvil",
+                            reason="libanvil.so not built")
+L = anvil.library()
+
+
+def test_exports_every_declared_symbol():
+    names = anvil.header_functions()
+    assert len(names) >= 11
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_default_maps_are_the_page_maps(constants):
+    maps, _ = constants
+    got = np.array(anvil.default_maps(), np.float32)
+    np.testing.assert_array_equal(got, np.array(maps, np.float32))
+
+
+def test_status_strings():
+    for code, name in anvil.STATUS.items():
+        assert L.anvil_status_string(code).decode() == name
+
+
+def _call(descs, maps=None, nmaps=6, ws=1 << 40, ws_bytes=1 << 40, margin=1.05, eps=1e-6):
+    arr = (anvil.BankDesc * len(descs))(*descs)
+    if maps is None:
+        marr, nm = anvil._maps_arg(None)
+    else:
+        marr, nm = maps, nmaps
+    return L.anvil_multi_bank_step(arr, len(descs), None, marr, nm if maps is None else nmaps,
+                                   margin, eps, ws, ws_bytes, None)
+
+
+G = 1 << 32  # fake, aligned device addresses far apart
+
+
+def d(g=2, m=40, n=24, grad=G, vel=2 * G, out=3 * G):
+    return anvil._raw_desc(g, m, n, grad, vel, out)
+
+
+def test_workspace_bytes():
+    assert anvil.workspace_bytes([(2, 40, 24)]) > 0
+    assert anvil.workspace_bytes([(0, 40, 24)]) == 0
+    one = anvil.workspace_bytes([(22, 256, 768)])
+    two = anvil.workspace_bytes([(22, 256, 768), (22, 2816, 768)])
+    assert two > one
+    # tall and wide of the same shape need the same scratch (small-side-major layout)
+    assert anvil.workspace_bytes([(3, 300, 130)]) == anvil.workspace_bytes([(3, 130, 300)])
+
+
+@pytest.mark.parametrize("desc,code", [
+    (dict(grad=0), anvil.ERR_INVALID_ARG),
+    (dict(vel=0), anvil.ERR_INVALID_ARG),
+    (dict(out=0), anvil.ERR_INVALID_ARG),
+    (dict(g=0), anvil.ERR_INVALID_ARG),
+    (dict(m=0), anvil.ERR_INVALID_ARG),
+    (dict(n=-1), anvil.ERR_INVALID_ARG),
+    (dict(m=20000), anvil.ERR_UNSUPPORTED_SHAPE),
+    (dict(grad=G + 2), anvil.ERR_ALIGNMENT),
+    (dict(out=3 * G + 1), anvil.ERR_ALIGNMENT),
+    (dict(out=G), anvil.ERR_ALIAS),            # out == grad
+    (dict(out=2 * G + 4), anvil.ERR_ALIAS),    # out inside velocity
+    (dict(vel=G + 64), anvil.ERR_ALIAS),       # velocity overlaps grad
+])
+def test_argument_errors(desc, code):
+    assert _call([d(**desc)]) == code
+
+
+def test_alias_across_banks_and_workspace():
+    a = d()
+    b = d(grad=4 * G, vel=5 * G, out=2 * G + 128)  # bank 2 writes into bank 1's velocity
+    assert _call([a, b]) == anvil.ERR_ALIAS
+    assert _call([d()], ws=2 * G) == anvil.ERR_ALIAS  # workspace over the velocity
+
+
+def test_map_and_bank_count_errors():
+    marr, _ = anvil._maps_arg(None)
+    assert _call([d()], maps=marr, nmaps=0) == anvil.ERR_INVALID_ARG
+    big = (anvil.Map * 17)()
+    assert _call([d()], maps=big, nmaps=17) == anvil.ERR_INVALID_ARG
+    descs = [d(grad=(10 + 3 * i) * G, vel=(11 + 3 * i) * G, out=(12 + 3 * i) * G) for i in range(9)]
+    assert _call(descs) == anvil.ERR_INVALID_ARG
+
+
+def test_workspace_errors():
+    need = anvil.workspace_bytes([(2, 40, 24)])
+    assert _call([d()], ws=0) == anvil.ERR_WORKSPACE
+    assert _call([d()], ws=7 * G, ws_bytes=need - 1) == anvil.ERR_WORKSPACE
+    assert _call([d()], ws=7 * G + 128, ws_bytes=need) == anvil.ERR_ALIGNMENT
