@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark of the ANVIL optimizer step on GB300: one full step over the three
+projection banks (qk 22x256x768, vo 22x768x768, mlp 22x2816x768; 66 matrices), mixed
+synthetic inputs (half Gaussian, half rank-32 plus 1e-3 noise), post-engage scalars,
+each step one CUDA-graph replay of the grouped launch sequence.
+
+Prints one JSON line (rank 0).  ``value`` is whole-job matrices/s with the inputs
+resident in HBM; ``e2e`` is the same metric through the same C-ABI call with the
+gradients copied in from pinned host memory and the outputs copied back every step;
+``roofline`` is the dominant kernel's achieved rate (algorithmic work / its CUDA-event
+duration inside timed steps) against the measured peak; ``cpu_baseline`` is the CPU
+oracle on a bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl anvil|reference]
+
+``--impl reference`` times the CPU oracle (the reference arm of this build) on the same
+workload and metric.  With N > 1 (launched by torch.distributed.run) every rank runs an
+independent replica of the step on its own GPU: the path shards by whole matrices and
+has no exchange step, so there is no collective on the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from polynomial_matrix_whitening_gb300 import workloads as W  # noqa: E402
+
+METRIC = "ANVIL bank-step matrices/s and TFLOP/s; % of GB300 bf16 tensor peak"
+UNIT = "matrices/s"
+WORKLOAD = "full_step"
+
+# ncu DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
+# kernel kind on this workload, from the capture summarised under profiles/; valid only
+# while the kernel source hashes to the recorded value.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash(kind):
+    name = "anvil_elementwise.cu" if kind in ("momentum", "norm_d", "normalize") else "anvil_gemm.cu"
+    with open(os.path.join(ROOT, "polynomial_matrix_whitening_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ------------------------------------------------------------------ work accounting
+
+def bank_dims(banks):
+    out = []
+    for b in banks:
+        s, L = min(b.m, b.n), max(b.m, b.n)
+        out.append((b.g, b.m, b.n, s, L))
+    return out
+
+
+def algorithmic_work(banks, nmaps=6):
+    """Per launch of each kernel kind over all banks: flops (GEMMs, symmetric products
+    counted on one triangle) or bytes (elementwise kernels)."""
+    w = {"gram": 0.0, "gram_norm": 0.0, "sqpoly": 0.0, "xupdate": 0.0, "xupdate_out": 0.0,
+         "momentum": 0.0, "normalize": 0.0, "norm_d": 0.0}
+    for g, m, n, s, L in bank_dims(banks):
+        w["gram"] += g * s * (s + 1) * L
+        w["gram_norm"] += g * s * (s + 1) * L
+        w["sqpoly"] += g * s * (s + 1) * s
+        w["xupdate"] += g * 2.0 * s * s * L
+        w["xupdate_out"] += g * 2.0 * s * s * L
+        w["momentum"] += g * m * n * 22.0        # 4 B grad + 2x(4+4) B rails + 2 B X
+        w["normalize"] += g * m * n * 4.0        # read + write bf16
+        w["norm_d"] += g * m * 4.0
+    return w
+
+
+def step_flops(banks, nmaps=6):
+    alg = dense = 0.0
+    for g, m, n, s, L in bank_dims(banks):
+        alg += g * nmaps * (s * (s + 1) * L + s * (s + 1) * s + 2.0 * s * s * L)
+        dense += g * nmaps * (4.0 * s * s * L + 2.0 * s ** 3)
+    return alg, dense
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons every 200 ms while running."""
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() in ("active", "1", "0x1"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ the CPU oracle arm
+
+def oracle_sample(wl, per_bank):
+    """Times the oracle on `per_bank` matrices of each bank of the workload (step 0 of the
+    grad pool, zero rails) and extrapolates to matrices/s of the full step."""
+    import oracle
+    oracle.build()
+    secs = 0.0
+    est = 0.0
+    picks = []
+    for j, b in enumerate(wl.banks):
+        grad = wl.grad(j, 0)
+        idx = [0, b.g // 2][:per_bank] if per_bank <= 2 else list(range(per_bank))
+        t_sum = 0.0
+        for i in idx:
+            g1 = np.ascontiguousarray(grad[i:i + 1])
+            v1 = np.zeros((2,) + g1.shape, np.float32)
+            sc = wl.scalars(0)
+            t0 = time.perf_counter()
+            oracle.bank_step(g1, v1, sc.momentum, sc.fast_beta, sc.fast_weight, sc.slow_beta)
+            t_sum += time.perf_counter() - t0
+        secs += t_sum
+        est += b.g * t_sum / len(idx)
+        picks.append(f"{b.name}{list(idx)}")
+    total = sum(b.g for b in wl.banks)
+    return total / est, secs, oracle.num_threads(), ", ".join(picks)
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    wl = W.workloads()[WORKLOAD]
+    for _ in range(args.warmup):
+        oracle_sample(wl, 1)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        v, secs, cores, picks = oracle_sample(wl, 1)
+        vals.append(v)
+    wall = time.perf_counter() - t0
+    value = statistics.median(vals)
+    ms = 1000.0 * sum(b.g for b in wl.banks) / value
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "banks": "qk 22x256x768 + vo 22x768x768 + mlp 22x2816x768"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"one matrix of each bank per step ({picks}), extrapolated "
+                                   f"to the 66-matrix step; {wall:.1f} s for {args.steps} steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ the GPU arm
+
+def run_anvil(args, world, rank, local):
+    import torch
+    from polynomial_matrix_whitening_gb300 import anvil
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = W.workloads()[WORKLOAD]
+    sc = wl.scalars(0)
+    scal = dict(momentum=sc.momentum, fast_beta=sc.fast_beta, fast_weight=sc.fast_weight,
+                slow_beta=sc.slow_beta)
+    pool_h = [[wl.grad(j, p) for j in range(len(wl.banks))] for p in range(wl.pool)]
+    pool_d = [[torch.from_numpy(x).to(dev) for x in p] for p in pool_h]
+    banks = [anvil.Bank(pool_d[0][j], torch.from_numpy(wl.velocity(j)).to(dev),
+                        torch.empty((b.g, b.m, b.n), dtype=torch.bfloat16, device=dev), **scal)
+             for j, b in enumerate(wl.banks)]
+    shapes = [b.shape for b in banks]
+    ws = anvil.alloc_workspace(shapes, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+
+    def capture(grads):
+        for b, gt in zip(banks, grads):
+            b.grad = gt
+        anvil.multi_bank_step(banks, ws, stream=stream)  # outside capture: device set-up
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            anvil.multi_bank_step(banks, ws, stream=stream)
+        return gr
+
+    with torch.cuda.stream(stream):
+        graphs = [capture(p) for p in pool_d]
+    launches_per_step = 3 * 6 + 3
+    nsteps, nwarm = args.steps, args.warmup
+
+    # ---- timed region: K graph replays, inputs resident in HBM
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for s in range(nwarm):
+            graphs[s % wl.pool].replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    with sampler, torch.cuda.stream(stream):
+        time.sleep(0.25)
+        e0.record(stream)
+        for s in range(nsteps):
+            graphs[s % wl.pool].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1) / nsteps
+    ms_max = max_over_ranks(ms, world)
+    mats = sum(b.shape[0] for b in banks)
+    value = mats * world / (ms_max / 1000.0)
+    alg, dense = step_flops(wl.banks)
+
+    # ---- per-kernel CUDA-event durations over timed steps (same launches, not in a graph)
+    prof_steps = max(3, min(nsteps, 10))
+    with torch.cuda.stream(stream):
+        for s in range(2):
+            for b, gt in zip(banks, pool_d[s % wl.pool]):
+                b.grad = gt
+            anvil.multi_bank_step(banks, ws, stream=stream)
+        torch.cuda.synchronize()
+        with anvil.profile(max_records=prof_steps * launches_per_step + 8) as prof:
+            p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            p0.record(stream)
+            for s in range(prof_steps):
+                for b, gt in zip(banks, pool_d[s % wl.pool]):
+                    b.grad = gt
+                anvil.multi_bank_step(banks, ws, stream=stream)
+            p1.record(stream)
+    torch.cuda.synchronize()
+    prof_ms_step = p0.elapsed_time(p1) / prof_steps
+    work = algorithmic_work(wl.banks)
+    peaks = measured_peaks()
+    per_kind = {}
+    for kind, t in prof.records:
+        d = per_kind.setdefault(kind, [0, 0.0])
+        d[0] += 1
+        d[1] += t
+    kernels = {}
+    for kind, (cnt, tot) in per_kind.items():
+        avg = tot / cnt
+        gemm = kind in ("gram", "gram_norm", "sqpoly", "xupdate", "xupdate_out")
+        rate = work[kind] / (avg / 1000.0)
+        kernels[kind] = {
+            "launches_per_step": cnt / prof_steps, "avg_ms": round(avg, 5),
+            "share": round(tot / sum(v[1] for v in per_kind.values()), 4),
+            "achieved": round(rate / (1e12 if gemm else 1e9), 2),
+            "unit": "TFLOP/s" if gemm else "GB/s",
+            "frac": round(rate / (1e12 if gemm else 1e9) /
+                          (peaks["bf16_tflops_sustained"] if gemm else peaks["hbm_gbs"]), 4)}
+    # dominant kernel: largest total time per step
+    dom = max(per_kind, key=lambda k: per_kind[k][1])
+    dk = kernels[dom]
+    gemm = dk["unit"] == "TFLOP/s"
+    traffic = None
+    rec = NCU_TRAFFIC.get(dom)
+    if rec and rec.get("source_hash") == kernel_source_hash(dom):
+        traffic = rec["bytes_per_launch"]
+    roofline = {"kernel": dom, "bound": "tensor" if gemm else "hbm", "achieved": dk["achieved"],
+                "peak": peaks["bf16_tflops_sustained"] if gemm else peaks["hbm_gbs"],
+                "unit": dk["unit"], "frac": dk["frac"], "traffic": traffic,
+                "peak_source": f"{peaks['source']} ({'bf16 sustained' if gemm else 'HBM copy'})"}
+    gemm_ms = sum(per_kind[k][1] for k in per_kind
+                  if k in ("gram", "gram_norm", "sqpoly", "xupdate", "xupdate_out")) / prof_steps
+    mom_ms = per_kind.get("momentum", [1, 0.0])[1] / prof_steps
+
+    # ---- end to end: pinned host gradients in, outputs out, every step
+    host_pool = [[torch.from_numpy(x).pin_memory() for x in p] for p in pool_h]
+    gbuf = [torch.empty_like(x) for x in pool_d[0]]
+    out_h = [torch.empty(b.out.shape, dtype=torch.bfloat16).pin_memory() for b in banks]
+    with torch.cuda.stream(stream):
+        g_e2e = capture(gbuf)
+        for s in range(nwarm):
+            for dst, src in zip(gbuf, host_pool[s % wl.pool]):
+                dst.copy_(src, non_blocking=True)
+            g_e2e.replay()
+            for dst, b in zip(out_h, banks):
+                dst.copy_(b.out, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        q0.record(stream)
+        for s in range(nsteps):
+            for dst, src in zip(gbuf, host_pool[s % wl.pool]):
+                dst.copy_(src, non_blocking=True)
+            g_e2e.replay()
+            for dst, b in zip(out_h, banks):
+                dst.copy_(b.out, non_blocking=True)
+        q1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(q0.elapsed_time(q1) / nsteps, world)
+    h2d = sum(x.numel() * 4 for x in gbuf)
+    d2h = sum(b.out.numel() * 2 for b in banks)
+    if not all(torch.isfinite(b.out.float()).all() for b in banks):
+        raise RuntimeError("non-finite output")
+    if anvil.device_error() != anvil.OK:
+        raise RuntimeError("device error word set during the bench")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, secs, cores, picks = oracle_sample(wl, 2)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"two matrices of each bank ({picks}) timed once each ({secs:.1f} s), "
+                         f"extrapolated to the 66-matrix step"}
+
+    if rank == 0:
+        clocks = sampler.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": nsteps,
+            "warmup": nwarm, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD,
+                       "banks": "qk 22x256x768 + vo 22x768x768 + mlp 22x2816x768",
+                       "inputs": "matrices 0-10 N(0,0.02^2), 11-21 rank-32 + 1e-3 noise; pool of 4",
+                       "scalars": "post-engage: momentum 0.95, fast_beta 0.85, fast_weight 0.4385, "
+                                  "slow_beta 0.98",
+                       "maps": "6 ANVIL_MAPS", "graph": "one CUDA graph per step",
+                       "l2": "inputs larger than L2 (grads 260 MB + rails 520 MB per step)",
+                       "parallelism": f"replicas x{world}"},
+            "tflops_algorithmic": alg / (ms_max / 1000.0) / 1e12 * world,
+            "tflops_dense_equivalent": dense / (ms_max / 1000.0) / 1e12 * world,
+            "gemm_phase_frac_of_peak": (alg / (gemm_ms / 1000.0) / 1e12) / peaks["bf16_tflops_sustained"],
+            "momentum_frac_of_hbm": (work["momentum"] / (mom_ms / 1000.0) / 1e9) / peaks["hbm_gbs"],
+            "profiled_ms_per_step": prof_ms_step,
+            "roofline": roofline, "kernels": kernels,
+            "e2e": {"value": mats * world / (e2e_ms / 1000.0), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": launches_per_step * nsteps,
+            "clocks": clocks, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["anvil", "reference"], default="anvil")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_anvil(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
