@@ -113,6 +113,34 @@ anvil_status anvil_bank_step(const float* grad, float* velocity, int g, int m, i
                              const anvil_map* maps, int nmaps, float margin, float eps,
                              uint16_t* out, void* stream);
 
+/* anvil_bank_step for callers that must not allocate device memory.  The page has no
+ * counterpart: this is a deployment convenience.  Some hosts cannot call cudaMalloc
+ * from the code that runs the optimizer step: an application whose device memory is
+ * all handed out by its own pool or budget, code running while another thread
+ * captures a CUDA graph in global capture mode (a cudaMalloc there breaks the
+ * capture), or a latency-bound loop where cudaMalloc / cudaFree, which synchronise
+ * the device, are not allowed.  This variant takes the same arguments as
+ * anvil_bank_step but keeps its scratch in a fixed array of
+ * ANVIL_STATIC_SCRATCH_BYTES bytes of device memory that the library declares
+ * statically: each GPU that loads the library holds that array until the process
+ * exits.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Sizes whose scratch (anvil_workspace_bytes of the one bank) exceeds
+ *     ANVIL_STATIC_SCRATCH_BYTES are rejected with ANVIL_ERR_WORKSPACE, and
+ *     anvil_last_cuda_error() says how many bytes the call needed.  32 MiB holds,
+ *     e.g., 22 matrices of 256 x 768 or 3 of 2816 x 768.
+ *   - The first call on each GPU looks up the array's device address on that GPU
+ *     (cudaGetSymbolAddress, with that GPU current); make that first call before
+ *     any stream capture.
+ *   - All calls on a GPU share the one array, which keeps whatever the last call
+ *     left in it; the step writes every scratch byte before reading it, so nothing
+ *     needs clearing.  Two calls whose work overlaps on the GPU (different streams,
+ *     or threads) race on the array and corrupt each other's results: serialise them. */
+#define ANVIL_STATIC_SCRATCH_BYTES (32u << 20)
+anvil_status anvil_bank_step_noalloc(const float* grad, float* velocity, int g, int m, int n,
+                                     float momentum, float fast_beta, float fast_weight,
+                                     float slow_beta, const anvil_map* maps, int nmaps,
+                                     float margin, float eps, uint16_t* out, void* stream);
+
 /* Per-stage dumps of one bank step, for parity testing (not the hot path).
  * DEVICE pointers, each optional (NULL = skip), in the page's layout:
  *   X_raw [g, m, n] bf16            bf16 cast of the momentum lookahead

@@ -77,6 +77,8 @@ _lib.anvil_multi_bank_step.restype = _i
 _lib.anvil_bank_step.argtypes = [_vp, _vp, _i, _i, _i, _f, _f, _f, _f, ctypes.POINTER(Map), _i,
                                  _f, _f, _vp, _vp]
 _lib.anvil_bank_step.restype = _i
+_lib.anvil_bank_step_noalloc.argtypes = _lib.anvil_bank_step.argtypes
+_lib.anvil_bank_step_noalloc.restype = _i
 _lib.anvil_bank_step_traced.argtypes = [ctypes.POINTER(BankDesc), _vp, ctypes.POINTER(Map), _i,
                                         _f, _f, _vp, _sz, ctypes.POINTER(Trace), _vp]
 _lib.anvil_bank_step_traced.restype = _i
@@ -213,6 +215,22 @@ def bank_step(grad, velocity, out, momentum=0.95, fast_beta=0.85, fast_weight=0.
                               fast_weight, slow_beta, marr, nm, margin, eps, out.data_ptr(),
                               _stream_arg(stream))
     _check(st, "anvil_bank_step")
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def bank_step_noalloc(grad, velocity, out, momentum=0.95, fast_beta=0.85, fast_weight=0.4385,
+                      slow_beta=0.98, maps=None, margin=1.05, eps=1e-6, stream=None):
+    """bank_step with the library's fixed device scratch (no allocation by the call); for
+    callers that cannot allocate device memory.  Calls that overlap on the GPU race."""
+    _desc(grad, velocity, out)
+    g, m, n = grad.shape
+    marr, nm = (None, 0) if maps is None else _maps_arg(maps)
+    st = _lib.anvil_bank_step_noalloc(grad.data_ptr(), velocity.data_ptr(), g, m, n, momentum,
+                                      fast_beta, fast_weight, slow_beta, marr, nm, margin, eps,
+                                      out.data_ptr(), _stream_arg(stream))
+    _check(st, "anvil_bank_step_noalloc")
 
 
 def bank_step_traced(bank: Bank, workspace, maps=None, margin=1.05, eps=1e-6, stream=None):

@@ -487,6 +487,17 @@ OwnedWorkspace g_ws[64];
 
 }  // namespace
 
+// ---------------------------------------------------------------- fixed-scratch variant
+// Scratch of anvil_bank_step_noalloc: one array per GPU, created when this library's
+// device code is loaded onto that GPU and held until the process exits.  Host code may
+// only use its name with cudaGetSymbolAddress; the device address differs per GPU.
+static __device__ __align__(256) unsigned char g_static_scratch[ANVIL_STATIC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_static_mutex;
+void* g_static_addr[64] = {nullptr};
+}  // namespace
+
 extern "C" {
 
 int anvil_default_maps(anvil_map* maps, int cap) {
@@ -659,5 +670,59 @@ const char* anvil_status_string(anvil_status s) {
 }
 
 const char* anvil_last_cuda_error(void) { return g_last_error; }
+
+anvil_status anvil_bank_step_noalloc(const float* grad, float* velocity, int g, int m, int n,
+                                     float momentum, float fast_beta, float fast_weight,
+                                     float slow_beta, const anvil_map* maps, int nmaps,
+                                     float margin, float eps, uint16_t* out, void* stream) {
+    anvil_bank_desc b;
+    b.grad = grad;
+    b.velocity = velocity;
+    b.out = out;
+    b.g = g;
+    b.m = m;
+    b.n = n;
+    b.scalars.momentum = momentum;
+    b.scalars.fast_beta = fast_beta;
+    b.scalars.fast_weight = fast_weight;
+    b.scalars.slow_beta = slow_beta;
+    if (!maps) {
+        maps = kAnvilMaps;
+        nmaps = 6;
+    }
+    Layout L;
+    anvil_status st = make_layout(&b, 1, &L);
+    if (st != ANVIL_OK) return st;
+    if (L.total > ANVIL_STATIC_SCRATCH_BYTES) {
+        snprintf(g_last_error, sizeof(g_last_error),
+                 "anvil_bank_step_noalloc: %d x %d x %d needs %zu bytes of scratch; the fixed "
+                 "scratch holds %zu",
+                 g, m, n, L.total, static_cast<size_t>(ANVIL_STATIC_SCRATCH_BYTES));
+        return ANVIL_ERR_WORKSPACE;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return ANVIL_ERR_DEVICE;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mutex);
+        if (!g_static_addr[dev]) {
+            // once per GPU, with that GPU current: the array's device address
+            void* ptr = nullptr;
+            e = cudaGetSymbolAddress(&ptr, g_static_scratch);
+            if (e != cudaSuccess || !ptr)
+                return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
+                                 "cudaGetSymbolAddress(fixed scratch)");
+            g_static_addr[dev] = ptr;
+        }
+        scratch = g_static_addr[dev];
+    }
+    // Every byte of the scratch that the step reads is written earlier in the same step,
+    // so what a previous call left there does not matter.
+    return run_step(&b, 1, nullptr, maps, nmaps, margin, eps, scratch,
+                    static_cast<size_t>(ANVIL_STATIC_SCRATCH_BYTES),
+                    static_cast<cudaStream_t>(stream), nullptr);
+}
 
 }  // extern "C"
