@@ -12,6 +12,7 @@ duration inside timed steps) against the measured peak; ``cpu_baseline`` is the 
 oracle on a bounded sample of the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl anvil|reference]
+  python bench.py --ncu-case     # two eager steps of the same workload, for ncu captures
 
 ``--impl reference`` times the CPU oracle (the reference arm of this build) on the same
 workload and metric.  With N > 1 (launched by torch.distributed.run) every rank runs an
@@ -425,6 +426,28 @@ def run_anvil(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_ncu_case():
+    """Two eager (non-graph) steps of the bench workload, one grad draw: a short program for
+    ncu captures (18 GEMM launches per step; the third of the second step is an X-update)."""
+    import torch
+    from polynomial_matrix_whitening_gb300 import anvil
+    dev = torch.device("cuda", 0)
+    wl = W.workloads()[WORKLOAD]
+    sc = wl.scalars(0)
+    banks = [anvil.Bank(torch.from_numpy(wl.grad(j, 0)).to(dev),
+                        torch.from_numpy(wl.velocity(j)).to(dev),
+                        torch.empty((b.g, b.m, b.n), dtype=torch.bfloat16, device=dev),
+                        momentum=sc.momentum, fast_beta=sc.fast_beta, fast_weight=sc.fast_weight,
+                        slow_beta=sc.slow_beta) for j, b in enumerate(wl.banks)]
+    ws = anvil.alloc_workspace([b.shape for b in banks], device=dev)
+    for _ in range(2):
+        anvil.multi_bank_step(banks, ws)
+    torch.cuda.synchronize()
+    if anvil.device_error() != anvil.OK:
+        raise RuntimeError("device error word set")
+    print("ncu case done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -432,7 +455,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["anvil", "reference"], default="anvil")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ncu-case", action="store_true")
     args = ap.parse_args()
+    if args.ncu_case:
+        run_ncu_case()
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_setup()
