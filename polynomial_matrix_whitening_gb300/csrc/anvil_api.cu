@@ -49,6 +49,7 @@ struct DeviceState {
     bool ready = false;
     anvil_status status = ANVIL_OK;
     unsigned* err = nullptr;
+    int sm_count = 0;
 };
 std::mutex g_dev_mutex;
 DeviceState g_dev[64];
@@ -89,6 +90,8 @@ anvil_status device_setup(DeviceState** out) {
             g_encode = reinterpret_cast<EncodeTiledFn>(fn);
         }
         if ((e = gemm_prepare())) return cuda_fail(e, "cudaFuncSetAttribute");
+        if ((e = cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev)))
+            return cuda_fail(e, "cudaDeviceGetAttribute");
         st.err = device_error_word();
         if (!st.err) return cuda_fail(cudaGetLastError(), "cudaGetSymbolAddress(error word)");
         st.ready = true;
@@ -158,7 +161,7 @@ anvil_status make_layout(const anvil_bank_desc* banks, int nbanks, Layout* L) {
         G.s = G.tall ? b.n : b.m;
         G.L = G.tall ? b.m : b.n;
         G.s_pad = round_up(G.s, TILE);
-        G.L_pad = round_up(G.L, TILE);
+        G.L_pad = round_up(G.L, LPAD);
         G.nlb = G.L_pad / LBLK;
         G.mat_begin = L->total_mats;
         L->total_mats += b.g;
@@ -384,6 +387,7 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
             gp.b = mp.b;
             gp.c = mp.c;
             gp.err = dev->err;
+            gp.sm_count = dev->sm_count;
             int tiles = 0, nb = 0;
             for (int q = first; q < nbanks && q < first + MAX_LAUNCH_BANKS; ++q, ++nb) {
                 const int i = order[q];
@@ -424,7 +428,7 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
                         gb.tm_b = B.tm_yn[cur];
                         gb.src = B.y[cur];
                         gb.dst = op == OP_XUPDATE ? B.y[cur ^ 1] : banks[i].out;
-                        gb.nt_n = G.L_pad / TILE;
+                        gb.nt_n = G.L_pad / gemm_tile_cols(op);
                         gb.tiles_per_mat = gb.T * gb.nt_n;
                         gb.num_kb = G.s_pad / BK;
                         break;

@@ -12,14 +12,16 @@
 // rows (A A = A A^T), so every operand is K-major except Y in the X-update, which is
 // read MN-major (contiguous along the output columns).
 //
-// One CTA computes one 128x128 output tile of one matrix; the grid covers every tile
-// of every matrix of up to four banks (a grouped launch).  Warp roles: warp 0 lane 0
-// issues TMA loads into a STAGES-deep shared-memory ring, warp 1 lane 0 issues
-// tcgen05.mma (M = 128, N = 128, K = 16) into a 128-column fp32 TMEM accumulator,
-// warp 2 owns the TMEM allocation; then all four warps read the accumulator back with
-// tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = tile rows) and run the fused epilogue.
-// Every wait is bounded (anvil_device.cuh); a wait that gives up sets the device error
-// word, the tile's epilogue is skipped, and the CTA still frees its TMEM and exits.
+// Persistent and warp-specialised: one CTA per SM walks output tiles tile = blockIdx.x,
+// blockIdx.x + gridDim.x, ... over every matrix of up to four banks (heaviest bank
+// first).  Warp 0 (one lane) issues TMA loads into a STAGES-deep shared-memory ring;
+// warp 1 owns the TMEM allocation and (one lane) issues tcgen05.mma (M = 128, N = BN,
+// K = 16) into one of two BN-column fp32 TMEM accumulators; warps 2-5 read the other
+// accumulator back with tcgen05.ld (warp w owns TMEM lanes 32 (w % 4) ..) and run the
+// fused epilogue, so a tile's epilogue overlaps the next tile's MMAs.  Every wait is
+// bounded (anvil_device.cuh): a wait that gives up sets the device error word and an
+// abort flag; all roles stop, in-flight copies and MMAs are waited for (bounded), the
+// TMEM is freed and the CTA exits.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -28,25 +30,31 @@
 
 namespace anvil {
 
-constexpr int STAGES = 3;
-constexpr int A_STAGE = TILE * BK * 2;  // 16 KB
-constexpr int B_STAGE = TILE * BK * 2;  // 16 KB
-constexpr int STAGE_BYTES = A_STAGE + B_STAGE;
-constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024;  // + alignment slack
-constexpr uint32_t TMEM_COLS = 128;
+constexpr uint32_t SMEM_BUDGET = 192 * 1024;
 
 template <int OP>
 struct OpTraits {
     static constexpr bool sym = (OP == OP_GRAM || OP == OP_GRAM_NORM || OP == OP_SQPOLY);
     static constexpr bool xupdate = (OP == OP_XUPDATE || OP == OP_XUPDATE_OUT);
+    static constexpr int BN = xupdate ? 256 : 128;          // output tile columns
+    static constexpr int A_STAGE = TILE * BK * 2;            // 16 KB
+    static constexpr int B_STAGE = BN * BK * 2;              // 16 or 32 KB
+    static constexpr int STAGE = A_STAGE + B_STAGE;
+    static constexpr int STAGES = SMEM_BUDGET / STAGE;       // 6 or 4
+    static constexpr int SMEM = STAGES * STAGE + 1024;       // + alignment slack
+    static constexpr uint32_t TMEM_COLS = 2 * BN;            // two accumulators
 };
+
+constexpr int GEMM_THREADS = 192;  // 6 warps
 
 __device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&f)[32]) {
     const uint4* p = reinterpret_cast<const uint4*>(src);
+    uint4 u[4];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) u[v] = p[v];
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-        const uint4 u = p[v];
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+        const uint32_t w[4] = {u[v].x, u[v].y, u[v].z, u[v].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             f[8 * v + 2 * q] = bf2f(static_cast<uint16_t>(w[q] & 0xffffu));
@@ -68,41 +76,51 @@ __device__ __forceinline__ void store32_bf16(uint16_t* dst, const uint16_t (&o)[
     }
 }
 
+struct TileCoord {
+    int bi, mat, ti, tj;
+};
+
+// Tile t of the grouped launch -> (bank, matrix, row tile, column tile).
 template <int OP>
-__global__ void __launch_bounds__(128) gemm_kernel(const __grid_constant__ GemmParams p) {
+__device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
+    TileCoord c;
+    c.bi = 0;
+#pragma unroll 1
+    for (int i = 1; i < p.nbanks; ++i)
+        if (t >= p.bank[i].tile_begin) c.bi = i;
+    const GemmBank& bk = p.bank[c.bi];
+    const int local = t - bk.tile_begin;
+    c.mat = local / bk.tiles_per_mat;
+    int r = local - c.mat * bk.tiles_per_mat;
+    if (OpTraits<OP>::sym) {
+        c.ti = 0;
+        while (r >= bk.T - c.ti) {
+            r -= bk.T - c.ti;
+            ++c.ti;
+        }
+        c.tj = c.ti + r;
+    } else {
+        c.ti = r / bk.nt_n;
+        c.tj = r - c.ti * bk.nt_n;
+    }
+    return c;
+}
+
+template <int OP>
+__global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
     using TR = OpTraits<OP>;
+    constexpr int BN = TR::BN;
+    constexpr int STAGES = TR::STAGES;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];
     __shared__ __align__(8) uint64_t empty_bar[STAGES];
-    __shared__ __align__(8) uint64_t acc_bar;
+    __shared__ __align__(8) uint64_t tfull_bar[2];
+    __shared__ __align__(8) uint64_t tempty_bar[2];
+    __shared__ __align__(8) uint64_t mma_done_bar;
     __shared__ uint32_t tmem_slot;
-    __shared__ int aborted;
+    __shared__ volatile int aborted;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    // ---- which tile of which matrix of which bank
-    const int t = blockIdx.x;
-    int bi = 0;
-#pragma unroll 1
-    for (int i = 1; i < p.nbanks; ++i)
-        if (t >= p.bank[i].tile_begin) bi = i;
-    const GemmBank& bk = p.bank[bi];
-    const int local = t - bk.tile_begin;
-    const int mat = local / bk.tiles_per_mat;
-    int r = local - mat * bk.tiles_per_mat;
-    int ti, tj;
-    if (TR::sym) {
-        ti = 0;
-        while (r >= bk.T - ti) {
-            r -= bk.T - ti;
-            ++ti;
-        }
-        tj = ti + r;
-    } else {
-        ti = r / bk.nt_n;
-        tj = r - ti * bk.nt_n;
-    }
-
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
@@ -111,142 +129,195 @@ __global__ void __launch_bounds__(128) gemm_kernel(const __grid_constant__ GemmP
             mbar_init(&full_bar[s], 1);
             mbar_init(&empty_bar[s], 1);
         }
-        mbar_init(&acc_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull_bar[b], 1);
+            mbar_init(&tempty_bar[b], 4);  // one arrival per epilogue warp
+        }
+        mbar_init(&mma_done_bar, 1);
         fence_mbar_init();
         aborted = 0;
     }
     if (threadIdx.x == 32) {
-        tma_prefetch_desc(&bk.tm_a);
-        tma_prefetch_desc(&bk.tm_b);
+        for (int i = 0; i < p.nbanks; ++i) {
+            tma_prefetch_desc(&p.bank[i].tm_a);
+            tma_prefetch_desc(&p.bank[i].tm_b);
+        }
     }
-    if (warp == 2) tmem_alloc(&tmem_slot, TMEM_COLS);
+    if (warp == 1) tmem_alloc(&tmem_slot, TR::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    const int nkb = bk.num_kb;
-    int issued = 0;  // k-blocks whose loads the producer armed
+    int issued = 0;  // producer: k-blocks whose loads were armed (in the whole CTA life)
 
-    if (warp == 0 && lane == 0) {
-        // ---------------- TMA producer
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t round = kb / STAGES;
-            if (!mbar_wait(&empty_bar[s], (round & 1u) ^ 1u, p.err)) {
-                aborted = 1;
-                break;
-            }
-            issued = kb + 1;
-            uint8_t* sa = smem + s * STAGE_BYTES;
-            uint8_t* sb = sa + A_STAGE;
-            mbar_arrive_expect_tx(&full_bar[s], STAGE_BYTES);
-            tma_load_3d(sa, &bk.tm_a, &full_bar[s], kb * BK, ti * TILE, mat);
-            if (TR::xupdate) {
-                // Y rows kb*64 .. +63 (the contraction index), columns tj*128 .. +127 in
-                // two 64-column boxes: MN-major chunks 8 KB apart.
-                tma_load_3d(sb, &bk.tm_b, &full_bar[s], tj * TILE, kb * BK, mat);
-                tma_load_3d(sb + 8192, &bk.tm_b, &full_bar[s], tj * TILE + 64, kb * BK, mat);
-            } else {
-                tma_load_3d(sb, &bk.tm_b, &full_bar[s], kb * BK, tj * TILE, mat);
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            int it = 0;
+            for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+                const TileCoord c = decode_tile<OP>(p, t);
+                const GemmBank& bk = p.bank[c.bi];
+                for (int kb = 0; kb < bk.num_kb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t r = static_cast<uint32_t>(it / STAGES);
+                    if (!mbar_wait(&empty_bar[s], (r & 1u) ^ 1u, p.err)) {
+                        aborted = 1;
+                        break;
+                    }
+                    uint8_t* sa = smem + s * TR::STAGE;
+                    uint8_t* sb = sa + TR::A_STAGE;
+                    mbar_arrive_expect_tx(&full_bar[s], TR::STAGE);
+                    tma_load_3d(sa, &bk.tm_a, &full_bar[s], kb * BK, c.ti * TILE, c.mat);
+                    if (TR::xupdate) {
+                        // Y rows kb*64 .. +63 (the contraction index), columns tj*BN ..
+                        // +BN-1 in 64-column boxes: MN-major chunks 8 KB apart.
+#pragma unroll
+                        for (int q = 0; q < BN / 64; ++q)
+                            tma_load_3d(sb + q * 8192, &bk.tm_b, &full_bar[s], c.tj * BN + 64 * q,
+                                        kb * BK, c.mat);
+                    } else {
+                        tma_load_3d(sb, &bk.tm_b, &full_bar[s], kb * BK, c.tj * TILE, c.mat);
+                    }
+                    issued = it + 1;
+                }
             }
         }
-    } else if (warp == 1 && lane == 0) {
-        // ---------------- MMA issuer
-        constexpr uint32_t idesc = idesc_bf16_f32(TILE, TILE, false, TR::xupdate);
-        for (int kb = 0; kb < nkb; ++kb) {
-            const int s = kb % STAGES;
-            const uint32_t round = kb / STAGES;
-            if (!mbar_wait(&full_bar[s], round & 1u, p.err)) {
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(TILE, BN, false, TR::xupdate);
+            int it = 0, lt = 0;
+            for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x, ++lt) {
+                const TileCoord c = decode_tile<OP>(p, t);
+                const int nkb = p.bank[c.bi].num_kb;
+                const int ab = lt & 1;
+                const uint32_t u = static_cast<uint32_t>(lt >> 1);
+                if (!mbar_wait(&tempty_bar[ab], (u & 1u) ^ 1u, p.err)) {
+                    aborted = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dacc = tmem + static_cast<uint32_t>(ab * BN);
+                bool ok = true;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t r = static_cast<uint32_t>(it / STAGES);
+                    if (!mbar_wait(&full_bar[s], r & 1u, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(smem + s * TR::STAGE);
+                    const uint32_t b0 = a0 + TR::A_STAGE;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                        const uint64_t bd = TR::xupdate ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
+                                                        : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                        umma_bf16(dacc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
+                }
+                if (!ok) {
+                    aborted = 1;
+                    break;
+                }
+                umma_commit(&tfull_bar[ab]);  // accumulator ab complete
+            }
+            // every MMA this thread issued has completed once this barrier fires
+            umma_commit(&mma_done_bar);
+            mbar_wait(&mma_done_bar, 0, p.err);
+        }
+    } else {
+        // ---------------- epilogue: warps 2-5, TMEM lane quadrant = warp % 4
+        const int quad = warp & 3;
+        int lt = 0;
+        for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x, ++lt) {
+            const TileCoord c = decode_tile<OP>(p, t);
+            const GemmBank& bk = p.bank[c.bi];
+            const int ab = lt & 1;
+            const uint32_t u = static_cast<uint32_t>(lt >> 1);
+            if (!mbar_wait(&tfull_bar[ab], u & 1u, p.err)) {
                 aborted = 1;
                 break;
             }
             tc_fence_after();
-            const uint32_t a0 = smem_u32(smem + s * STAGE_BYTES);
-            const uint32_t b0 = a0 + A_STAGE;
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-                const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                const uint64_t bd = TR::xupdate ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
-                                                : smem_desc_sw128(b0 + kk * 32, 16, 1024);
-                umma_bf16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            const int row = c.ti * TILE + quad * 32 + lane;  // row in the padded small side
+            const size_t sq = static_cast<size_t>(bk.s_pad);
+            float dd = 0.f;
+            if (OP == OP_GRAM_NORM) {
+                const float d = bk.d[c.mat];
+                dd = __fmul_rn(d, d);
             }
-            umma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
-        }
-        umma_commit(&acc_bar);  // accumulator complete
-    }
-    __syncwarp();
-
-    // ---------------- epilogue: all four warps
-    const bool acc_ok = mbar_wait(&acc_bar, 0, p.err);
-    __syncthreads();  // makes the producer's / issuer's abort flag visible
-    tc_fence_after();
-    if (acc_ok && !aborted) {
-        const int row = ti * TILE + warp * 32 + lane;  // row in the padded small side
-        const size_t sq = static_cast<size_t>(bk.s_pad);
-        float dd = 0.f;
-        if (OP == OP_GRAM_NORM) {
-            const float d = bk.d[mat];
-            dd = __fmul_rn(d, d);
-        }
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) +
+                                   static_cast<uint32_t>(ab * BN);
 #pragma unroll 1
-        for (int cc = 0; cc < TILE / 32; ++cc) {
-            float v[32];
-            tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc * 32, v);
-            const int col0 = tj * TILE + cc * 32;
-            uint16_t o[32];
-            if (OP == OP_GRAM) {
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                const int col0 = c.tj * BN + cc * 32;
+                float in[32];
+                if (OP == OP_SQPOLY)
+                    load32_bf16(bk.src + (static_cast<size_t>(c.mat) * sq + row) * sq + col0, in);
+                else if (TR::xupdate)
+                    load32_bf16(bk.src + (static_cast<size_t>(c.mat) * sq + row) * bk.L_pad + col0, in);
+                float v[32];
+                tmem_ld_32x32b_x32(tbase + cc * 32, v);
+                uint16_t o[32];
+                if (OP == OP_GRAM) {
 #pragma unroll
-                for (int q = 0; q < 32; ++q) o[q] = f2bf(v[q]);
-            } else if (OP == OP_GRAM_NORM) {
+                    for (int q = 0; q < 32; ++q) o[q] = f2bf(v[q]);
+                } else if (OP == OP_GRAM_NORM) {
 #pragma unroll
-                for (int q = 0; q < 32; ++q) o[q] = f2bf(__fdiv_rn(round_bf(v[q]), dd));
-            } else if (OP == OP_SQPOLY) {
-                float av[32];
-                load32_bf16(bk.src + (static_cast<size_t>(mat) * sq + row) * sq + col0, av);
-#pragma unroll
-                for (int q = 0; q < 32; ++q)
-                    o[q] = f2bf(__fadd_rn(__fmul_rn(p.b, av[q]), __fmul_rn(p.c, v[q])));
-            } else {
-                float yv[32];
-                load32_bf16(bk.src + (static_cast<size_t>(mat) * sq + row) * bk.L_pad + col0, yv);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) o[q] = f2bf(__fadd_rn(__fmul_rn(p.a, yv[q]), v[q]));
-            }
-
-            if (TR::sym) {
-                uint16_t* base = bk.dst + static_cast<size_t>(mat) * sq * sq;
-                store32_bf16(base + row * sq + col0, o);
-                if (ti != tj) {
-                    // mirror: column `row` of rows col0..col0+31; a warp writes 64 contiguous
-                    // bytes per q
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) base[(col0 + q) * sq + row] = o[q];
-                }
-            } else if (OP == OP_XUPDATE) {
-                store32_bf16(bk.dst + (static_cast<size_t>(mat) * sq + row) * bk.L_pad + col0, o);
-            } else {  // OP_XUPDATE_OUT: natural [m, n] layout, clipped to the real extent
-                const int m = bk.m, n = bk.n;
-                uint16_t* out = bk.dst + static_cast<size_t>(mat) * m * n;
-                if (!bk.tall) {
-                    if (row < m) {
-                        uint16_t* dst = out + static_cast<size_t>(row) * n + col0;
-                        if (col0 + 32 <= n && (n & 7) == 0 &&
-                            (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
-                            store32_bf16(dst, o);
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 32; ++q)
-                                if (col0 + q < n) dst[q] = o[q];
-                        }
-                    }
-                } else if (row < n) {
+                    for (int q = 0; q < 32; ++q) o[q] = f2bf(__fdiv_rn(round_bf(v[q]), dd));
+                } else if (OP == OP_SQPOLY) {
 #pragma unroll
                     for (int q = 0; q < 32; ++q)
-                        if (col0 + q < m) out[static_cast<size_t>(col0 + q) * n + row] = o[q];
+                        o[q] = f2bf(__fadd_rn(__fmul_rn(p.b, in[q]), __fmul_rn(p.c, v[q])));
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) o[q] = f2bf(__fadd_rn(__fmul_rn(p.a, in[q]), v[q]));
+                }
+
+                if (TR::sym) {
+                    uint16_t* base = bk.dst + static_cast<size_t>(c.mat) * sq * sq;
+                    store32_bf16(base + row * sq + col0, o);
+                    if (c.ti != c.tj) {
+                        // mirror: column `row` of rows col0..col0+31 (a warp writes 64
+                        // contiguous bytes per q)
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) base[(col0 + q) * sq + row] = o[q];
+                    }
+                } else if (OP == OP_XUPDATE) {
+                    store32_bf16(bk.dst + (static_cast<size_t>(c.mat) * sq + row) * bk.L_pad + col0, o);
+                } else {  // OP_XUPDATE_OUT: natural [m, n] layout, clipped to the real extent
+                    const int m = bk.m, n = bk.n;
+                    uint16_t* out = bk.dst + static_cast<size_t>(c.mat) * m * n;
+                    if (!bk.tall) {
+                        if (row < m) {
+                            uint16_t* dst = out + static_cast<size_t>(row) * n + col0;
+                            if (col0 + 32 <= n && (n & 7) == 0 &&
+                                (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+                                store32_bf16(dst, o);
+                            } else {
+#pragma unroll
+                                for (int q = 0; q < 32; ++q)
+                                    if (col0 + q < n) dst[q] = o[q];
+                            }
+                        }
+                    } else if (row < n) {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q)
+                            if (col0 + q < m) out[static_cast<size_t>(col0 + q) * n + row] = o[q];
+                    }
                 }
             }
+            // accumulator ab may be overwritten once all four epilogue warps are done
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cta(&tempty_bar[ab]);
         }
     }
+
+    __syncthreads();
     if (aborted && warp == 0 && lane == 0) {
         // Let the copies still in flight land before the CTA's shared memory goes away:
         // the last load armed on each stage is that stage's latest phase.
@@ -255,12 +326,14 @@ __global__ void __launch_bounds__(128) gemm_kernel(const __grid_constant__ GemmP
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) tmem_dealloc(tmem, TMEM_COLS);
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, TR::TMEM_COLS);
 }
 
 template <int OP>
 static cudaError_t launch_op(const GemmParams& p, cudaStream_t stream) {
-    gemm_kernel<OP><<<p.total_tiles, 128, GEMM_SMEM, stream>>>(p);
+    int grid = p.total_tiles < p.sm_count ? p.total_tiles : p.sm_count;
+    gemm_kernel<OP><<<grid, GEMM_THREADS, OpTraits<OP>::SMEM, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -276,13 +349,23 @@ cudaError_t launch_gemm(GemmOp op, const GemmParams& p, cudaStream_t stream) {
     return cudaErrorInvalidValue;
 }
 
+int gemm_tile_cols(GemmOp op) {
+    return (op == OP_XUPDATE || op == OP_XUPDATE_OUT) ? OpTraits<OP_XUPDATE>::BN
+                                                      : OpTraits<OP_GRAM>::BN;
+}
+
 cudaError_t gemm_prepare() {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(gemm_kernel<OP_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM))) return e;
-    if ((e = cudaFuncSetAttribute(gemm_kernel<OP_GRAM_NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM))) return e;
-    if ((e = cudaFuncSetAttribute(gemm_kernel<OP_SQPOLY>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM))) return e;
-    if ((e = cudaFuncSetAttribute(gemm_kernel<OP_XUPDATE>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM))) return e;
-    if ((e = cudaFuncSetAttribute(gemm_kernel<OP_XUPDATE_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM))) return e;
+#define ANVIL_SET_SMEM(OPV)                                                                  \
+    if ((e = cudaFuncSetAttribute(gemm_kernel<OPV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                  OpTraits<OPV>::SMEM)))                                     \
+        return e;
+    ANVIL_SET_SMEM(OP_GRAM)
+    ANVIL_SET_SMEM(OP_GRAM_NORM)
+    ANVIL_SET_SMEM(OP_SQPOLY)
+    ANVIL_SET_SMEM(OP_XUPDATE)
+    ANVIL_SET_SMEM(OP_XUPDATE_OUT)
+#undef ANVIL_SET_SMEM
     return cudaSuccess;
 }
 

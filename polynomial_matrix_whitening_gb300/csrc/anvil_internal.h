@@ -7,7 +7,7 @@
 // are then the same three products,
 //     A = Y Y^T,   B = b A + c A A,   Y <- a Y + B Y,
 // because for a tall X, X^T X = Y Y^T and (a X + X B)^T = a Y + B Y (B is symmetric).
-// s_pad and L_pad round s and L up to the 128-wide tile; the padding is zero and
+// s_pad rounds s up to 128 and L_pad rounds L up to 256; the padding is zero and
 // stays zero through every step (zero rows and columns of Y give zero rows and
 // columns of A and B), so it changes no result.
 #pragma once
@@ -19,7 +19,8 @@
 
 namespace anvil {
 
-constexpr int TILE = 128;            // GEMM tile (M = N = 128) and the padding unit
+constexpr int TILE = 128;            // GEMM tile rows, and the padding unit of the small side
+constexpr int LPAD = 256;            // padding unit of the long side (X-update tile columns)
 constexpr int BK = 64;               // GEMM k-block: one 128-byte swizzle row of bf16
 constexpr int LBLK = 64;             // momentum-kernel tile edge; one diagonal partial each
 constexpr int MAX_BANKS = 8;         // banks per call
@@ -96,10 +97,12 @@ struct GemmBank {
 struct GemmParams {
     GemmBank bank[MAX_LAUNCH_BANKS];
     int nbanks, total_tiles;
+    int sm_count;  // persistent grid: min(total_tiles, sm_count) CTAs
     float a, b, c;
     unsigned* err;
 };
 cudaError_t launch_gemm(GemmOp op, const GemmParams& p, cudaStream_t stream);
+int gemm_tile_cols(GemmOp op);  // output tile columns of this op's kernel
 cudaError_t gemm_prepare();  // sets the GEMM kernels' shared-memory limit on this device
 
 // ---------------------------------------------------------------- tracing / self-test
