@@ -426,6 +426,8 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
                     case OP_XUPDATE_OUT:
                         gb.tm_a = B.tm_b;
                         gb.tm_b = B.tm_yn[cur];
+                        gb.tm_c = B.tm_yk[cur];
+                        gb.tm_d = B.tm_yk[cur ^ 1];
                         gb.src = B.y[cur];
                         gb.dst = op == OP_XUPDATE ? B.y[cur ^ 1] : banks[i].out;
                         gb.nt_n = G.L_pad / gemm_tile_cols(op);

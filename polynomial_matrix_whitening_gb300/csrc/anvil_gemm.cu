@@ -41,7 +41,9 @@ struct OpTraits {
     static constexpr int B_STAGE = BN * BK * 2;              // 16 or 32 KB
     static constexpr int STAGE = A_STAGE + B_STAGE;
     static constexpr int STAGES = SMEM_BUDGET / STAGE;       // 6 or 4
-    static constexpr int SMEM = STAGES * STAGE + 1024;       // + alignment slack
+    // X-update epilogue staging: two 128 x 64 bf16 boxes (one per in-flight quarter tile)
+    static constexpr int STAGING = (OP == OP_XUPDATE) ? 2 * TILE * 64 * 2 : 0;
+    static constexpr int SMEM = STAGES * STAGE + STAGING + 1024;  // + alignment slack
     static constexpr uint32_t TMEM_COLS = 2 * BN;            // two accumulators
 };
 
@@ -80,6 +82,13 @@ struct TileCoord {
     int bi, mat, ti, tj;
 };
 
+// The k-th tile of CTA c in a persistent grid of G CTAs: tiles are handed out in rounds
+// of G, alternating direction (a snake), so the heavy tiles at the front of the order
+// spread evenly.  Returns >= total when the CTA has no k-th tile.
+__device__ __forceinline__ int snake_tile(int k, int c, int G) {
+    return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
 // Tile t of the grouped launch -> (bank, matrix, row tile, column tile).
 template <int OP>
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
@@ -117,6 +126,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     __shared__ __align__(8) uint64_t tfull_bar[2];
     __shared__ __align__(8) uint64_t tempty_bar[2];
     __shared__ __align__(8) uint64_t mma_done_bar;
+    __shared__ __align__(8) uint64_t epi_bar[2];  // X-update staging loads
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int aborted;
 
@@ -134,6 +144,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             mbar_init(&tempty_bar[b], 4);  // one arrival per epilogue warp
         }
         mbar_init(&mma_done_bar, 1);
+        mbar_init(&epi_bar[0], 1);
+        mbar_init(&epi_bar[1], 1);
         fence_mbar_init();
         aborted = 0;
     }
@@ -141,6 +153,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         for (int i = 0; i < p.nbanks; ++i) {
             tma_prefetch_desc(&p.bank[i].tm_a);
             tma_prefetch_desc(&p.bank[i].tm_b);
+            if (OP == OP_XUPDATE) {
+                tma_prefetch_desc(&p.bank[i].tm_c);
+                tma_prefetch_desc(&p.bank[i].tm_d);
+            }
         }
     }
     if (warp == 1) tmem_alloc(&tmem_slot, TR::TMEM_COLS);
@@ -154,7 +170,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         if (lane == 0) {
             // ---------------- TMA producer
             int it = 0;
-            for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x) {
+            for (int k = 0;; ++k) {
+                const int t = snake_tile(k, blockIdx.x, gridDim.x);
+                if (t >= p.total_tiles || aborted) break;
                 const TileCoord c = decode_tile<OP>(p, t);
                 const GemmBank& bk = p.bank[c.bi];
                 for (int kb = 0; kb < bk.num_kb; ++kb, ++it) {
@@ -186,8 +204,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         if (lane == 0) {
             // ---------------- MMA issuer
             constexpr uint32_t idesc = idesc_bf16_f32(TILE, BN, false, TR::xupdate);
-            int it = 0, lt = 0;
-            for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x, ++lt) {
+            int it = 0;
+            for (int lt = 0;; ++lt) {
+                const int t = snake_tile(lt, blockIdx.x, gridDim.x);
+                if (t >= p.total_tiles || aborted) break;
                 const TileCoord c = decode_tile<OP>(p, t);
                 const int nkb = p.bank[c.bi].num_kb;
                 const int ab = lt & 1;
@@ -231,12 +251,89 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     } else {
         // ---------------- epilogue: warps 2-5, TMEM lane quadrant = warp % 4
         const int quad = warp & 3;
-        int lt = 0;
-        for (int t = blockIdx.x; t < p.total_tiles && !aborted; t += gridDim.x, ++lt) {
+        const bool leader = (warp == 2 && lane == 0);
+        uint8_t* stg = smem + STAGES * TR::STAGE;  // X-update staging (1024-aligned)
+        int gq = 0;                                // X-update: quarter tiles done so far
+        for (int lt = 0;; ++lt) {
+            const int t = snake_tile(lt, blockIdx.x, gridDim.x);
+            if (t >= p.total_tiles || aborted) break;
             const TileCoord c = decode_tile<OP>(p, t);
             const GemmBank& bk = p.bank[c.bi];
             const int ab = lt & 1;
             const uint32_t u = static_cast<uint32_t>(lt >> 1);
+            if (OP == OP_XUPDATE) {
+                // ---- staged epilogue: Y' = bf16(a Y + acc) through shared memory, by
+                // quarters of 64 columns, double-buffered: TMA load of the Y quarter,
+                // in-place update, TMA store of the result.
+                if (leader) {
+                    bulk_wait_read_all();
+                    mbar_arrive_expect_tx(&epi_bar[gq & 1], TILE * 64 * 2);
+                    tma_load_3d(stg + (gq & 1) * (TILE * 128), &bk.tm_c, &epi_bar[gq & 1],
+                                c.tj * BN, c.ti * TILE, c.mat);
+                }
+                if (!mbar_wait(&tfull_bar[ab], u & 1u, p.err)) {
+                    aborted = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) +
+                                       static_cast<uint32_t>(ab * BN);
+                const int r = quad * 32 + lane;  // row within the tile
+                bool ok = true;
+                for (int q = 0; q < BN / 64; ++q, ++gq) {
+                    const int buf = gq & 1;
+                    if (leader && q + 1 < BN / 64) {
+                        bulk_wait_read_all();
+                        mbar_arrive_expect_tx(&epi_bar[buf ^ 1], TILE * 64 * 2);
+                        tma_load_3d(stg + (buf ^ 1) * (TILE * 128), &bk.tm_c, &epi_bar[buf ^ 1],
+                                    c.tj * BN + 64 * (q + 1), c.ti * TILE, c.mat);
+                    }
+                    if (!mbar_wait(&epi_bar[buf], (static_cast<uint32_t>(gq) >> 1) & 1u, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* box = stg + buf * (TILE * 128) + r * 128;
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        float v[32];
+                        tmem_ld_32x32b_x32(tbase + q * 64 + cc * 32, v);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            // 16-byte chunk j of this 128-byte row sits at chunk j ^ (r % 8)
+                            const int j = cc * 4 + w;
+                            uint4* cp = reinterpret_cast<uint4*>(box + ((j ^ (r & 7)) << 4));
+                            const uint4 y = *cp;
+                            const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+                            uint32_t ow[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float lo = __fadd_rn(__fmul_rn(p.a, bf2f(static_cast<uint16_t>(yw[e] & 0xffffu))), v[8 * w + 2 * e]);
+                                const float hi = __fadd_rn(__fmul_rn(p.a, bf2f(static_cast<uint16_t>(yw[e] >> 16))), v[8 * w + 2 * e + 1]);
+                                ow[e] = static_cast<uint32_t>(f2bf(lo)) | (static_cast<uint32_t>(f2bf(hi)) << 16);
+                            }
+                            *cp = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                        }
+                    }
+                    if (q + 1 == BN / 64) {
+                        // accumulator ab is free once all four epilogue warps have read it
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cta(&tempty_bar[ab]);
+                    }
+                    fence_proxy_async_smem();
+                    named_barrier_sync(1, 128);
+                    if (leader) {
+                        tma_store_3d(&bk.tm_d, stg + buf * (TILE * 128), c.tj * BN + 64 * q,
+                                     c.ti * TILE, c.mat);
+                        bulk_commit_group();
+                    }
+                }
+                if (!ok) {
+                    aborted = 1;
+                    break;
+                }
+                continue;
+            }
             if (!mbar_wait(&tfull_bar[ab], u & 1u, p.err)) {
                 aborted = 1;
                 break;
@@ -317,6 +414,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         }
     }
 
+    if (OP == OP_XUPDATE && warp == 2 && lane == 0) bulk_wait_all();  // stores complete
     __syncthreads();
     if (aborted && warp == 0 && lane == 0) {
         // Let the copies still in flight land before the CTA's shared memory goes away:

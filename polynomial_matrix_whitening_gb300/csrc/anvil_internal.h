@@ -84,6 +84,8 @@ enum GemmOp : int {
 struct GemmBank {
     CUtensorMap tm_a;     // A operand, K-major, box {64, 128, 1}
     CUtensorMap tm_b;     // B operand: K-major box {64, 128, 1}, or (xupdate) MN-major {64, 64, 1}
+    CUtensorMap tm_c;     // xupdate epilogue input Y, box {64, 128, 1}
+    CUtensorMap tm_d;     // xupdate output Y', box {64, 128, 1}
     const uint16_t* src;  // epilogue input: A (sqpoly) or Y (xupdate)
     uint16_t* dst;        // output
     const float* d;       // [g] normaliser of this bank's matrices (gram_norm)
