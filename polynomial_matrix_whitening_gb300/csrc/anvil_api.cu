@@ -217,8 +217,9 @@ anvil_status check_maps(const anvil_map* maps, int nmaps) {
     return ANVIL_OK;
 }
 
-// 3-D bf16 tensor map over [g][rows][cols], 128-byte swizzle, box {box0, box1, 1}.
-anvil_status encode_map(CUtensorMap* map, void* base, int g, int rows, int cols, int box0, int box1) {
+// 3-D bf16 tensor map over [g][rows][cols], box {box0, box1, 1}, 128-byte swizzle or none.
+anvil_status encode_map(CUtensorMap* map, void* base, int g, int rows, int cols, int box0, int box1,
+                        bool swizzle = true) {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(g)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
@@ -226,7 +227,8 @@ anvil_status encode_map(CUtensorMap* map, void* base, int g, int rows, int cols,
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(box0), static_cast<cuuint32_t>(box1), 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed (%d)",
@@ -243,7 +245,8 @@ struct BankPtrs {
     uint16_t* b;
     float* part;
     float* d;
-    CUtensorMap tm_yk[2], tm_yn[2], tm_a, tm_b;
+    CUtensorMap tm_yk[2], tm_yn[2], tm_a, tm_b, tm_at, tm_bt, tm_out;
+    bool out_tma;
 };
 
 anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scalars* d_scalars,
@@ -291,6 +294,15 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         }
         if ((st = encode_map(&B.tm_a, B.a, G.g, G.s_pad, G.s_pad, BK, TILE))) return st;
         if ((st = encode_map(&B.tm_b, B.b, G.g, G.s_pad, G.s_pad, BK, TILE))) return st;
+        if ((st = encode_map(&B.tm_at, B.a, G.g, G.s_pad, G.s_pad, TILE, BK, false))) return st;
+        if ((st = encode_map(&B.tm_bt, B.b, G.g, G.s_pad, G.s_pad, TILE, BK, false))) return st;
+        // the last X-update stores `out` [g, m, n] by TMA when its rows are 16-byte aligned:
+        // wide banks as Y boxes {64, 128}, tall banks as transposed boxes {128, 64}
+        B.out_tma = (G.n % 8 == 0) && !(reinterpret_cast<uintptr_t>(banks[i].out) & 15);
+        if (B.out_tma &&
+            (st = encode_map(&B.tm_out, banks[i].out, G.g, G.m, G.n, G.tall ? TILE : BK,
+                             G.tall ? BK : TILE, !G.tall)))
+            return st;
     }
 
     cudaError_t e;
@@ -408,6 +420,8 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
                     case OP_GRAM_NORM:
                         gb.tm_a = B.tm_yk[cur];
                         gb.tm_b = B.tm_yk[cur];
+                        gb.tm_d = B.tm_a;
+                        gb.tm_e = B.tm_at;
                         gb.dst = B.a;
                         gb.nt_n = gb.T;
                         gb.tiles_per_mat = gb.T * (gb.T + 1) / 2;
@@ -416,6 +430,9 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
                     case OP_SQPOLY:
                         gb.tm_a = B.tm_a;
                         gb.tm_b = B.tm_a;
+                        gb.tm_c = B.tm_a;
+                        gb.tm_d = B.tm_b;
+                        gb.tm_e = B.tm_bt;
                         gb.src = B.a;
                         gb.dst = B.b;
                         gb.nt_n = gb.T;
@@ -427,7 +444,13 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
                         gb.tm_a = B.tm_b;
                         gb.tm_b = B.tm_yn[cur];
                         gb.tm_c = B.tm_yk[cur];
-                        gb.tm_d = B.tm_yk[cur ^ 1];
+                        if (op == OP_XUPDATE) {
+                            gb.tm_d = B.tm_yk[cur ^ 1];
+                        } else if (B.out_tma) {
+                            gb.out_tma = 1;
+                            if (G.tall) gb.tm_e = B.tm_out;
+                            else gb.tm_d = B.tm_out;
+                        }
                         gb.src = B.y[cur];
                         gb.dst = op == OP_XUPDATE ? B.y[cur ^ 1] : banks[i].out;
                         gb.nt_n = G.L_pad / gemm_tile_cols(op);

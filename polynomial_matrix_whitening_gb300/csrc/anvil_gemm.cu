@@ -12,16 +12,25 @@
 // rows (A A = A A^T), so every operand is K-major except Y in the X-update, which is
 // read MN-major (contiguous along the output columns).
 //
-// Persistent and warp-specialised: one CTA per SM walks output tiles tile = blockIdx.x,
-// blockIdx.x + gridDim.x, ... over every matrix of up to four banks (heaviest bank
-// first).  Warp 0 (one lane) issues TMA loads into a STAGES-deep shared-memory ring;
-// warp 1 owns the TMEM allocation and (one lane) issues tcgen05.mma (M = 128, N = BN,
-// K = 16) into one of two BN-column fp32 TMEM accumulators; warps 2-5 read the other
-// accumulator back with tcgen05.ld (warp w owns TMEM lanes 32 (w % 4) ..) and run the
-// fused epilogue, so a tile's epilogue overlaps the next tile's MMAs.  Every wait is
-// bounded (anvil_device.cuh): a wait that gives up sets the device error word and an
-// abort flag; all roles stop, in-flight copies and MMAs are waited for (bounded), the
-// TMEM is freed and the CTA exits.
+// Persistent and warp-specialised: one CTA per SM walks output tiles in a snake order
+// over every matrix of up to four banks (heaviest bank first).  Warp 0 (one lane)
+// issues TMA loads into a STAGES-deep shared-memory ring; warp 1 owns the TMEM
+// allocation and (one lane) issues tcgen05.mma (M = 128, N = BN, K = 16) into one of
+// two BN-column fp32 TMEM accumulators; warps 2-5 read the other accumulator back with
+// tcgen05.ld (warp w owns TMEM lanes 32 (w % 4) ..) and run the fused epilogue, so a
+// tile's epilogue overlaps the next tile's MMAs.
+//
+// The epilogue works by quarters of 64 output columns through two shared-memory
+// staging buffers: the epilogue input (A for sqpoly, Y for the X-update) arrives by
+// TMA into a 128x64 box (128-byte swizzle, conflict-free 16-byte reads), the result
+// is written back in place and leaves by TMA store; a transposed 64x128 box carries
+// the mirror tile of the symmetric products (and the last X-update of a tall bank,
+// whose output is X = Y^T).  The last X-update of a bank whose column count is not a
+// multiple of 8 writes `out` with plain bounds-checked stores instead.
+//
+// Every wait is bounded (anvil_device.cuh): a wait that gives up sets the device error
+// word and an abort flag; all roles stop, in-flight copies and MMAs are waited for
+// (bounded), the TMEM is freed and the CTA exits.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -30,21 +39,25 @@
 
 namespace anvil {
 
-constexpr uint32_t SMEM_BUDGET = 192 * 1024;
+constexpr int SMEM_MAX = 227 * 1024;  // opt-in dynamic shared memory per block
+constexpr int QBOX = TILE * 64 * 2;   // one 128 x 64 bf16 staging box (16 KB)
 
 template <int OP>
 struct OpTraits {
     static constexpr bool sym = (OP == OP_GRAM || OP == OP_GRAM_NORM || OP == OP_SQPOLY);
     static constexpr bool xupdate = (OP == OP_XUPDATE || OP == OP_XUPDATE_OUT);
-    static constexpr int BN = xupdate ? 256 : 128;          // output tile columns
-    static constexpr int A_STAGE = TILE * BK * 2;            // 16 KB
-    static constexpr int B_STAGE = BN * BK * 2;              // 16 or 32 KB
+    static constexpr bool has_in = (OP == OP_SQPOLY) || xupdate;   // epilogue reads a tile
+    static constexpr bool has_t = sym || OP == OP_XUPDATE_OUT;     // transposed staging box
+    static constexpr int BN = xupdate ? 256 : 128;                 // output tile columns
+    static constexpr int NQ = BN / 64;                             // quarters per tile
+    static constexpr int A_STAGE = TILE * BK * 2;                  // 16 KB
+    static constexpr int B_STAGE = BN * BK * 2;                    // 16 or 32 KB
     static constexpr int STAGE = A_STAGE + B_STAGE;
-    static constexpr int STAGES = SMEM_BUDGET / STAGE;       // 6 or 4
-    // X-update epilogue staging: two 128 x 64 bf16 boxes (one per in-flight quarter tile)
-    static constexpr int STAGING = (OP == OP_XUPDATE) ? 2 * TILE * 64 * 2 : 0;
-    static constexpr int SMEM = STAGES * STAGE + STAGING + 1024;  // + alignment slack
-    static constexpr uint32_t TMEM_COLS = 2 * BN;            // two accumulators
+    static constexpr int BUF = has_t ? 2 * QBOX : QBOX;            // one staging buffer
+    static constexpr int STAGING = 2 * BUF;                        // double-buffered
+    static constexpr int STAGES = (SMEM_MAX - 2048 - STAGING) / STAGE;
+    static constexpr int SMEM = STAGES * STAGE + STAGING + 1024;   // + alignment slack
+    static constexpr uint32_t TMEM_COLS = 2 * BN;                  // two accumulators
 };
 
 constexpr int GEMM_THREADS = 192;  // 6 warps
@@ -115,18 +128,29 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
     return c;
 }
 
+// The elementwise part of each op's epilogue, on fp32 accumulator value v and (where
+// the op has one) the bf16 input value x at the same position.
+template <int OP>
+__device__ __forceinline__ uint16_t epi_value(const GemmParams& p, float v, float x, float dd) {
+    if (OP == OP_GRAM) return f2bf(v);
+    if (OP == OP_GRAM_NORM) return f2bf(__fdiv_rn(round_bf(v), dd));  // bf16(bf16(acc) / d^2)
+    if (OP == OP_SQPOLY) return f2bf(__fadd_rn(__fmul_rn(p.b, x), __fmul_rn(p.c, v)));
+    return f2bf(__fadd_rn(__fmul_rn(p.a, x), v));                   // a Y + acc
+}
+
 template <int OP>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
     using TR = OpTraits<OP>;
     constexpr int BN = TR::BN;
     constexpr int STAGES = TR::STAGES;
+    constexpr int NQ = TR::NQ;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];
     __shared__ __align__(8) uint64_t empty_bar[STAGES];
     __shared__ __align__(8) uint64_t tfull_bar[2];
     __shared__ __align__(8) uint64_t tempty_bar[2];
     __shared__ __align__(8) uint64_t mma_done_bar;
-    __shared__ __align__(8) uint64_t epi_bar[2];  // X-update staging loads
+    __shared__ __align__(8) uint64_t epi_bar[2];  // epilogue input loads, one per buffer
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int aborted;
 
@@ -142,10 +166,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull_bar[b], 1);
             mbar_init(&tempty_bar[b], 4);  // one arrival per epilogue warp
+            mbar_init(&epi_bar[b], 1);
         }
         mbar_init(&mma_done_bar, 1);
-        mbar_init(&epi_bar[0], 1);
-        mbar_init(&epi_bar[1], 1);
         fence_mbar_init();
         aborted = 0;
     }
@@ -153,10 +176,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         for (int i = 0; i < p.nbanks; ++i) {
             tma_prefetch_desc(&p.bank[i].tm_a);
             tma_prefetch_desc(&p.bank[i].tm_b);
-            if (OP == OP_XUPDATE) {
-                tma_prefetch_desc(&p.bank[i].tm_c);
-                tma_prefetch_desc(&p.bank[i].tm_d);
-            }
+            if (TR::has_in) tma_prefetch_desc(&p.bank[i].tm_c);
+            tma_prefetch_desc(&p.bank[i].tm_d);
+            if (TR::has_t) tma_prefetch_desc(&p.bank[i].tm_e);
         }
     }
     if (warp == 1) tmem_alloc(&tmem_slot, TR::TMEM_COLS);
@@ -164,7 +186,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
-    int issued = 0;  // producer: k-blocks whose loads were armed (in the whole CTA life)
+    int issued = 0;        // producer: k-blocks whose loads were armed (in the whole CTA life)
+    int epi_issued = 0;    // epilogue leader: staging loads armed
 
     if (warp == 0) {
         if (lane == 0) {
@@ -251,9 +274,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     } else {
         // ---------------- epilogue: warps 2-5, TMEM lane quadrant = warp % 4
         const int quad = warp & 3;
+        const int r = quad * 32 + lane;  // row within the tile
         const bool leader = (warp == 2 && lane == 0);
-        uint8_t* stg = smem + STAGES * TR::STAGE;  // X-update staging (1024-aligned)
-        int gq = 0;                                // X-update: quarter tiles done so far
+        uint8_t* stg = smem + STAGES * TR::STAGE;  // staging buffers (1024-aligned)
+        int gq = 0;                                // quarter tiles done so far
         for (int lt = 0;; ++lt) {
             const int t = snake_tile(lt, blockIdx.x, gridDim.x);
             if (t >= p.total_tiles || aborted) break;
@@ -261,160 +285,150 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             const GemmBank& bk = p.bank[c.bi];
             const int ab = lt & 1;
             const uint32_t u = static_cast<uint32_t>(lt >> 1);
-            if (OP == OP_XUPDATE) {
-                // ---- staged epilogue: Y' = bf16(a Y + acc) through shared memory, by
-                // quarters of 64 columns, double-buffered: TMA load of the Y quarter,
-                // in-place update, TMA store of the result.
-                if (leader) {
-                    bulk_wait_read_all();
-                    mbar_arrive_expect_tx(&epi_bar[gq & 1], TILE * 64 * 2);
-                    tma_load_3d(stg + (gq & 1) * (TILE * 128), &bk.tm_c, &epi_bar[gq & 1],
-                                c.tj * BN, c.ti * TILE, c.mat);
-                }
-                if (!mbar_wait(&tfull_bar[ab], u & 1u, p.err)) {
-                    aborted = 1;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) +
-                                       static_cast<uint32_t>(ab * BN);
-                const int r = quad * 32 + lane;  // row within the tile
-                bool ok = true;
-                for (int q = 0; q < BN / 64; ++q, ++gq) {
-                    const int buf = gq & 1;
-                    if (leader && q + 1 < BN / 64) {
-                        bulk_wait_read_all();
-                        mbar_arrive_expect_tx(&epi_bar[buf ^ 1], TILE * 64 * 2);
-                        tma_load_3d(stg + (buf ^ 1) * (TILE * 128), &bk.tm_c, &epi_bar[buf ^ 1],
-                                    c.tj * BN + 64 * (q + 1), c.ti * TILE, c.mat);
-                    }
-                    if (!mbar_wait(&epi_bar[buf], (static_cast<uint32_t>(gq) >> 1) & 1u, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* box = stg + buf * (TILE * 128) + r * 128;
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        float v[32];
-                        tmem_ld_32x32b_x32(tbase + q * 64 + cc * 32, v);
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            // 16-byte chunk j of this 128-byte row sits at chunk j ^ (r % 8)
-                            const int j = cc * 4 + w;
-                            uint4* cp = reinterpret_cast<uint4*>(box + ((j ^ (r & 7)) << 4));
-                            const uint4 y = *cp;
-                            const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
-                            uint32_t ow[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float lo = __fadd_rn(__fmul_rn(p.a, bf2f(static_cast<uint16_t>(yw[e] & 0xffffu))), v[8 * w + 2 * e]);
-                                const float hi = __fadd_rn(__fmul_rn(p.a, bf2f(static_cast<uint16_t>(yw[e] >> 16))), v[8 * w + 2 * e + 1]);
-                                ow[e] = static_cast<uint32_t>(f2bf(lo)) | (static_cast<uint32_t>(f2bf(hi)) << 16);
-                            }
-                            *cp = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                        }
-                    }
-                    if (q + 1 == BN / 64) {
-                        // accumulator ab is free once all four epilogue warps have read it
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cta(&tempty_bar[ab]);
-                    }
-                    fence_proxy_async_smem();
-                    named_barrier_sync(1, 128);
-                    if (leader) {
-                        tma_store_3d(&bk.tm_d, stg + buf * (TILE * 128), c.tj * BN + 64 * q,
-                                     c.ti * TILE, c.mat);
-                        bulk_commit_group();
-                    }
-                }
-                if (!ok) {
-                    aborted = 1;
-                    break;
-                }
-                continue;
+            const int row0 = c.ti * TILE;  // first row of the tile (padded small side)
+            const int col0 = c.tj * BN;    // first column
+            // what this tile stores: the tile itself, and/or its transpose
+            const bool to_direct = TR::sym || OP == OP_XUPDATE || (OP == OP_XUPDATE_OUT && !bk.tall);
+            const bool to_mirror = (TR::sym && c.ti != c.tj) || (OP == OP_XUPDATE_OUT && bk.tall);
+            const bool staged = OP != OP_XUPDATE_OUT || bk.out_tma;
+            float dd = 0.f;
+            if (OP == OP_GRAM_NORM) {
+                const float d = bk.d[c.mat];
+                dd = __fmul_rn(d, d);
+            }
+
+            if (staged && TR::has_in && leader) {
+                // input of the first quarter; both buffers' last stores must be done reading
+                bulk_wait_read_all();
+                const int buf = gq & 1;
+                mbar_arrive_expect_tx(&epi_bar[buf], QBOX);
+                tma_load_3d(stg + buf * TR::BUF, &bk.tm_c, &epi_bar[buf], col0, row0, c.mat);
+                epi_issued = gq + 1;
             }
             if (!mbar_wait(&tfull_bar[ab], u & 1u, p.err)) {
                 aborted = 1;
                 break;
             }
             tc_fence_after();
-            const int row = c.ti * TILE + quad * 32 + lane;  // row in the padded small side
-            const size_t sq = static_cast<size_t>(bk.s_pad);
-            float dd = 0.f;
-            if (OP == OP_GRAM_NORM) {
-                const float d = bk.d[c.mat];
-                dd = __fmul_rn(d, d);
-            }
             const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) +
                                    static_cast<uint32_t>(ab * BN);
-#pragma unroll 1
-            for (int cc = 0; cc < BN / 32; ++cc) {
-                const int col0 = c.tj * BN + cc * 32;
-                float in[32];
-                if (OP == OP_SQPOLY)
-                    load32_bf16(bk.src + (static_cast<size_t>(c.mat) * sq + row) * sq + col0, in);
-                else if (TR::xupdate)
-                    load32_bf16(bk.src + (static_cast<size_t>(c.mat) * sq + row) * bk.L_pad + col0, in);
-                float v[32];
-                tmem_ld_32x32b_x32(tbase + cc * 32, v);
-                uint16_t o[32];
-                if (OP == OP_GRAM) {
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) o[q] = f2bf(v[q]);
-                } else if (OP == OP_GRAM_NORM) {
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) o[q] = f2bf(__fdiv_rn(round_bf(v[q]), dd));
-                } else if (OP == OP_SQPOLY) {
-#pragma unroll
-                    for (int q = 0; q < 32; ++q)
-                        o[q] = f2bf(__fadd_rn(__fmul_rn(p.b, in[q]), __fmul_rn(p.c, v[q])));
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) o[q] = f2bf(__fadd_rn(__fmul_rn(p.a, in[q]), v[q]));
-                }
 
-                if (TR::sym) {
-                    uint16_t* base = bk.dst + static_cast<size_t>(c.mat) * sq * sq;
-                    store32_bf16(base + row * sq + col0, o);
-                    if (c.ti != c.tj) {
-                        // mirror: column `row` of rows col0..col0+31 (a warp writes 64
-                        // contiguous bytes per q)
+            if (!staged) {
+                // OP_XUPDATE_OUT into an `out` whose rows are not 16-byte aligned: plain
+                // bounds-checked stores straight from the accumulator.
+                const int m = bk.m, n = bk.n;
+                uint16_t* out = bk.dst + static_cast<size_t>(c.mat) * m * n;
+                const int row = row0 + r;
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    const int cb = col0 + cc * 32;
+                    float x[32];
+                    load32_bf16(bk.src + (static_cast<size_t>(c.mat) * bk.s_pad + row) * bk.L_pad + cb, x);
+                    float v[32];
+                    tmem_ld_32x32b_x32(tbase + cc * 32, v);
+                    uint16_t o[32];
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) base[(col0 + q) * sq + row] = o[q];
-                    }
-                } else if (OP == OP_XUPDATE) {
-                    store32_bf16(bk.dst + (static_cast<size_t>(c.mat) * sq + row) * bk.L_pad + col0, o);
-                } else {  // OP_XUPDATE_OUT: natural [m, n] layout, clipped to the real extent
-                    const int m = bk.m, n = bk.n;
-                    uint16_t* out = bk.dst + static_cast<size_t>(c.mat) * m * n;
+                    for (int q = 0; q < 32; ++q) o[q] = epi_value<OP>(p, v[q], x[q], dd);
                     if (!bk.tall) {
-                        if (row < m) {
-                            uint16_t* dst = out + static_cast<size_t>(row) * n + col0;
-                            if (col0 + 32 <= n && (n & 7) == 0 &&
-                                (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
-                                store32_bf16(dst, o);
-                            } else {
-#pragma unroll
-                                for (int q = 0; q < 32; ++q)
-                                    if (col0 + q < n) dst[q] = o[q];
-                            }
-                        }
+                        if (row < m)
+                            for (int q = 0; q < 32; ++q)
+                                if (cb + q < n) out[static_cast<size_t>(row) * n + cb + q] = o[q];
                     } else if (row < n) {
-#pragma unroll
                         for (int q = 0; q < 32; ++q)
-                            if (col0 + q < m) out[static_cast<size_t>(col0 + q) * n + row] = o[q];
+                            if (cb + q < m) out[static_cast<size_t>(cb + q) * n + row] = o[q];
                     }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cta(&tempty_bar[ab]);
+                continue;
+            }
+
+            bool ok = true;
+            for (int q = 0; q < NQ; ++q, ++gq) {
+                const int buf = gq & 1;
+                uint8_t* dbox = stg + buf * TR::BUF;    // 128 rows x 64 cols, 128-byte swizzle
+                uint8_t* tbox = dbox + QBOX;            // 64 rows x 128 cols, plain
+                if (TR::has_in) {
+                    if (leader && q + 1 < NQ) {
+                        bulk_wait_read_all();
+                        mbar_arrive_expect_tx(&epi_bar[buf ^ 1], QBOX);
+                        tma_load_3d(stg + (buf ^ 1) * TR::BUF, &bk.tm_c, &epi_bar[buf ^ 1],
+                                    col0 + 64 * (q + 1), row0, c.mat);
+                        epi_issued = gq + 2;
+                    }
+                    if (!mbar_wait(&epi_bar[buf], (static_cast<uint32_t>(gq) >> 1) & 1u, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                } else {
+                    // no input: the buffer must be free of its last store before any write
+                    if (leader) bulk_wait_read_all();
+                    named_barrier_sync(1, 128);
+                }
+                uint8_t* drow = dbox + r * 128;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    float v[32];
+                    tmem_ld_32x32b_x32(tbase + q * 64 + cc * 32, v);
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        // 16-byte chunk j of this 128-byte row sits at chunk j ^ (r % 8)
+                        const int j = cc * 4 + w;
+                        uint4* cp = reinterpret_cast<uint4*>(drow + ((j ^ (r & 7)) << 4));
+                        uint32_t xw[4] = {0u, 0u, 0u, 0u};
+                        if (TR::has_in) {
+                            const uint4 x = *cp;
+                            xw[0] = x.x; xw[1] = x.y; xw[2] = x.z; xw[3] = x.w;
+                        }
+                        uint16_t o[8];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            o[2 * e] = epi_value<OP>(p, v[8 * w + 2 * e],
+                                                     bf2f(static_cast<uint16_t>(xw[e] & 0xffffu)), dd);
+                            o[2 * e + 1] = epi_value<OP>(p, v[8 * w + 2 * e + 1],
+                                                         bf2f(static_cast<uint16_t>(xw[e] >> 16)), dd);
+                        }
+                        if (to_direct)
+                            *cp = make_uint4(static_cast<uint32_t>(o[0]) | (static_cast<uint32_t>(o[1]) << 16),
+                                             static_cast<uint32_t>(o[2]) | (static_cast<uint32_t>(o[3]) << 16),
+                                             static_cast<uint32_t>(o[4]) | (static_cast<uint32_t>(o[5]) << 16),
+                                             static_cast<uint32_t>(o[6]) | (static_cast<uint32_t>(o[7]) << 16));
+                        if (TR::has_t && to_mirror) {
+                            // transposed box: element (row r, column 8j + e) at [8j + e][r]
+                            uint16_t* tcol = reinterpret_cast<uint16_t*>(tbox) + r;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) tcol[(8 * j + e) * TILE] = o[e];
+                        }
+                    }
+                }
+                if (q + 1 == NQ) {
+                    // accumulator ab is free once all four epilogue warps have read it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cta(&tempty_bar[ab]);
+                }
+                fence_proxy_async_smem();
+                named_barrier_sync(1, 128);
+                if (leader) {
+                    if (to_direct) tma_store_3d(&bk.tm_d, dbox, col0 + 64 * q, row0, c.mat);
+                    if (TR::has_t && to_mirror) tma_store_3d(&bk.tm_e, tbox, row0, col0 + 64 * q, c.mat);
+                    bulk_commit_group();
                 }
             }
-            // accumulator ab may be overwritten once all four epilogue warps are done
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cta(&tempty_bar[ab]);
+            if (!ok) {
+                aborted = 1;
+                break;
+            }
+        }
+        if (leader) {
+            bulk_wait_all();  // every store of this CTA has completed
+            if (aborted)      // and every staging load it armed has landed
+                for (int g = epi_issued - 2 < 0 ? 0 : epi_issued - 2; g < epi_issued; ++g)
+                    mbar_wait(&epi_bar[g & 1], (static_cast<uint32_t>(g) >> 1) & 1u, p.err);
         }
     }
 
-    if (OP == OP_XUPDATE && warp == 2 && lane == 0) bulk_wait_all();  // stores complete
     __syncthreads();
     if (aborted && warp == 0 && lane == 0) {
         // Let the copies still in flight land before the CTA's shared memory goes away:

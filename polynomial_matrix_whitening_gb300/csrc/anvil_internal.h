@@ -84,12 +84,14 @@ enum GemmOp : int {
 struct GemmBank {
     CUtensorMap tm_a;     // A operand, K-major, box {64, 128, 1}
     CUtensorMap tm_b;     // B operand: K-major box {64, 128, 1}, or (xupdate) MN-major {64, 64, 1}
-    CUtensorMap tm_c;     // xupdate epilogue input Y, box {64, 128, 1}
-    CUtensorMap tm_d;     // xupdate output Y', box {64, 128, 1}
+    CUtensorMap tm_c;     // epilogue input (A for sqpoly, Y for xupdate), box {64, 128, 1}
+    CUtensorMap tm_d;     // epilogue output, box {64, 128, 1}, 128-byte swizzle
+    CUtensorMap tm_e;     // transposed epilogue output (mirror tile / tall out), box {128, 64, 1}
     const uint16_t* src;  // epilogue input: A (sqpoly) or Y (xupdate)
     uint16_t* dst;        // output
     const float* d;       // [g] normaliser of this bank's matrices (gram_norm)
     int g, s_pad, L_pad, m, n, tall;
+    int out_tma;          // xupdate_out: `out` rows are 16-byte aligned (TMA stores)
     int T;                // s_pad / TILE
     int nt_n;             // output tiles along N (T for sym ops, L_pad / TILE for xupdate)
     int tiles_per_mat;

@@ -105,8 +105,11 @@ def test_bounded_wait_gives_up_and_reports(A):
 
 # ------------------------------------------------------------------ stage by stage
 
+# Ragged and tiny shapes on both sides of every path: n % 8 != 0 writes `out` with plain
+# stores, n % 8 == 0 with clipped TMA stores (wide: Y boxes; tall: transposed boxes).
 SMALL = [(2, 256, 768), (2, 300, 130), (2, 130, 300), (1, 200, 200), (2, 4, 3), (2, 3, 4),
-         (1, 1, 1), (1, 129, 1000), (1, 1000, 257), (3, 128, 128), (1, 64, 2048)]
+         (1, 1, 1), (1, 129, 1000), (1, 1000, 257), (3, 128, 128), (1, 64, 2048),
+         (2, 1000, 264), (2, 264, 1000), (2, 4, 8), (2, 24, 16), (1, 520, 520)]
 
 
 def _gemm_bound(exact, abs_terms, K):
