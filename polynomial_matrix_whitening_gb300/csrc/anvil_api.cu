@@ -160,7 +160,7 @@ anvil_status make_layout(const anvil_bank_desc* banks, int nbanks, Layout* L) {
         G.tall = b.m > b.n;
         G.s = G.tall ? b.n : b.m;
         G.L = G.tall ? b.m : b.n;
-        G.s_pad = round_up(G.s, TILE);
+        G.s_pad = round_up(G.s, PAIR);
         G.L_pad = round_up(G.L, LPAD);
         G.nlb = G.L_pad / LBLK;
         G.mat_begin = L->total_mats;
@@ -413,7 +413,7 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
                 gb.m = G.m;
                 gb.n = G.n;
                 gb.tall = G.tall;
-                gb.T = G.s_pad / TILE;
+                gb.T = G.s_pad / PAIR;
                 gb.d = B.d;
                 switch (op) {
                     case OP_GRAM:

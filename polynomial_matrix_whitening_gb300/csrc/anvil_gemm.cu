@@ -7,18 +7,24 @@
 //   OP_XUPDATE(_OUT)       : Y' = bf16(a Y + B Y)        [written to out for the last map]
 //
 // in the small-side-major layout of anvil_internal.h.  A and B are symmetric, so the
-// Gram and the A A product compute only the upper-triangle 128x128 tiles and store each
+// Gram and the A A product compute only the upper-triangle 256x256 tiles and store each
 // off-diagonal tile twice (itself and its mirror).  A A contracts A's rows with A's
 // rows (A A = A A^T), so every operand is K-major except Y in the X-update, which is
 // read MN-major (contiguous along the output columns).
 //
-// Persistent and warp-specialised: one CTA per SM walks output tiles in a snake order
-// over every matrix of up to four banks (heaviest bank first).  Warp 0 (one lane)
-// issues TMA loads into a STAGES-deep shared-memory ring; warp 1 owns the TMEM
-// allocation and (one lane) issues tcgen05.mma (M = 128, N = BN, K = 16) into one of
-// two BN-column fp32 TMEM accumulators; warps 2-5 read the other accumulator back with
-// tcgen05.ld (warp w owns TMEM lanes 32 (w % 4) ..) and run the fused epilogue, so a
-// tile's epilogue overlaps the next tile's MMAs.
+// CTA pairs: the kernel runs in clusters of two CTAs on two SMs; each pair computes one
+// 256x256 output tile with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16).  CTA
+// rank r of the pair loads rows 128r..128r+127 of the tile's A operand and columns
+// 128r..128r+127 of its B operand, and holds output rows 128r.. in its own TMEM, so
+// each SM streams 32 KB of operands per 64-deep k-block for 2 x 128 x 256 x 64 MACs.
+// Persistent and warp-specialised: each pair walks output tiles in a snake order over
+// every matrix of up to four banks (heaviest bank first).  Warp 0 (one lane) issues TMA
+// loads into a STAGES-deep shared-memory ring, counted on the leader CTA's barrier;
+// warp 1 owns the TMEM allocation (in both CTAs) and, in the leader CTA only, issues the
+// MMAs into one of two 256-column fp32 accumulators and commits to both CTAs' barriers;
+// warps 2-5 of each CTA read the other accumulator back with tcgen05.ld (warp w owns
+// TMEM lanes 32 (w % 4) ..) and run the fused epilogue, so a tile's epilogue overlaps
+// the next tile's MMAs.
 //
 // The epilogue works by quarters of 64 output columns through two shared-memory
 // staging buffers: the epilogue input (A for sqpoly, Y for the X-update) arrives by
@@ -48,10 +54,10 @@ struct OpTraits {
     static constexpr bool xupdate = (OP == OP_XUPDATE || OP == OP_XUPDATE_OUT);
     static constexpr bool has_in = (OP == OP_SQPOLY) || xupdate;   // epilogue reads a tile
     static constexpr bool has_t = sym || OP == OP_XUPDATE_OUT;     // transposed staging box
-    static constexpr int BN = xupdate ? 256 : 128;                 // output tile columns
+    static constexpr int BN = PAIR;                                // output columns per CTA
     static constexpr int NQ = BN / 64;                             // quarters per tile
-    static constexpr int A_STAGE = TILE * BK * 2;                  // 16 KB
-    static constexpr int B_STAGE = BN * BK * 2;                    // 16 or 32 KB
+    static constexpr int A_STAGE = TILE * BK * 2;                  // 16 KB: this CTA's A rows
+    static constexpr int B_STAGE = TILE * BK * 2;                  // 16 KB: this CTA's B half
     static constexpr int STAGE = A_STAGE + B_STAGE;
     static constexpr int BUF = has_t ? 2 * QBOX : QBOX;            // one staging buffer
     static constexpr int STAGING = 2 * BUF;                        // double-buffered
@@ -95,14 +101,14 @@ struct TileCoord {
     int bi, mat, ti, tj;
 };
 
-// The k-th tile of CTA c in a persistent grid of G CTAs: tiles are handed out in rounds
+// The k-th tile of pair c in a persistent grid of G pairs: tiles are handed out in rounds
 // of G, alternating direction (a snake), so the heavy tiles at the front of the order
-// spread evenly.  Returns >= total when the CTA has no k-th tile.
+// spread evenly.  Returns >= total when the pair has no k-th tile.
 __device__ __forceinline__ int snake_tile(int k, int c, int G) {
     return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
-// Tile t of the grouped launch -> (bank, matrix, row tile, column tile).
+// Tile t of the grouped launch -> (bank, matrix, row block, column block), in 256s.
 template <int OP>
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
     TileCoord c;
@@ -155,6 +161,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     __shared__ volatile int aborted;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the MMAs), 1 = peer
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
@@ -165,7 +173,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull_bar[b], 1);
-            mbar_init(&tempty_bar[b], 4);  // one arrival per epilogue warp
+            mbar_init(&tempty_bar[b], 8);  // one arrival per epilogue warp of both CTAs
             mbar_init(&epi_bar[b], 1);
         }
         mbar_init(&mma_done_bar, 1);
@@ -181,9 +189,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             if (TR::has_t) tma_prefetch_desc(&p.bank[i].tm_e);
         }
     }
-    if (warp == 1) tmem_alloc(&tmem_slot, TR::TMEM_COLS);
+    if (warp == 1) tmem_alloc_pair(&tmem_slot, TR::TMEM_COLS);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     int issued = 0;        // producer: k-blocks whose loads were armed (in the whole CTA life)
@@ -194,10 +202,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             // ---------------- TMA producer
             int it = 0;
             for (int k = 0;; ++k) {
-                const int t = snake_tile(k, blockIdx.x, gridDim.x);
+                const int t = snake_tile(k, pair, npairs);
                 if (t >= p.total_tiles || aborted) break;
                 const TileCoord c = decode_tile<OP>(p, t);
                 const GemmBank& bk = p.bank[c.bi];
+                const int arow = c.ti * PAIR + TILE * rank;  // this CTA's A rows
+                const int bofs = c.tj * PAIR + TILE * rank;  // this CTA's B rows (or Y columns)
                 for (int kb = 0; kb < bk.num_kb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t r = static_cast<uint32_t>(it / STAGES);
@@ -207,29 +217,29 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                     }
                     uint8_t* sa = smem + s * TR::STAGE;
                     uint8_t* sb = sa + TR::A_STAGE;
-                    mbar_arrive_expect_tx(&full_bar[s], TR::STAGE);
-                    tma_load_3d(sa, &bk.tm_a, &full_bar[s], kb * BK, c.ti * TILE, c.mat);
+                    // both CTAs' bytes complete on the leader's barrier of this stage
+                    const uint32_t fb = map_to_rank(&full_bar[s], 0);
+                    if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * TR::STAGE);
+                    tma_load_3d_pair(sa, &bk.tm_a, fb, kb * BK, arow, c.mat);
                     if (TR::xupdate) {
-                        // Y rows kb*64 .. +63 (the contraction index), columns tj*BN ..
-                        // +BN-1 in 64-column boxes: MN-major chunks 8 KB apart.
-#pragma unroll
-                        for (int q = 0; q < BN / 64; ++q)
-                            tma_load_3d(sb + q * 8192, &bk.tm_b, &full_bar[s], c.tj * BN + 64 * q,
-                                        kb * BK, c.mat);
+                        // Y rows kb*64 .. +63 (the contraction index), this CTA's 128 of the
+                        // tile's columns in two 64-column boxes: MN-major chunks 8 KB apart.
+                        tma_load_3d_pair(sb, &bk.tm_b, fb, bofs, kb * BK, c.mat);
+                        tma_load_3d_pair(sb + 8192, &bk.tm_b, fb, bofs + 64, kb * BK, c.mat);
                     } else {
-                        tma_load_3d(sb, &bk.tm_b, &full_bar[s], kb * BK, c.tj * TILE, c.mat);
+                        tma_load_3d_pair(sb, &bk.tm_b, fb, kb * BK, bofs, c.mat);
                     }
                     issued = it + 1;
                 }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
-            constexpr uint32_t idesc = idesc_bf16_f32(TILE, BN, false, TR::xupdate);
+        if (lane == 0 && rank == 0) {
+            // ---------------- MMA issuer (leader CTA)
+            constexpr uint32_t idesc = idesc_bf16_f32(PAIR, PAIR, false, TR::xupdate);
             int it = 0;
             for (int lt = 0;; ++lt) {
-                const int t = snake_tile(lt, blockIdx.x, gridDim.x);
+                const int t = snake_tile(lt, pair, npairs);
                 if (t >= p.total_tiles || aborted) break;
                 const TileCoord c = decode_tile<OP>(p, t);
                 const int nkb = p.bank[c.bi].num_kb;
@@ -257,18 +267,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                         const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
                         const uint64_t bd = TR::xupdate ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
                                                         : smem_desc_sw128(b0 + kk * 32, 16, 1024);
-                        umma_bf16(dacc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        umma_bf16_pair(dacc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
-                    umma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
+                    umma_commit_pair(&empty_bar[s], 3);  // frees stage s in both CTAs
                 }
                 if (!ok) {
                     aborted = 1;
                     break;
                 }
-                umma_commit(&tfull_bar[ab]);  // accumulator ab complete
+                umma_commit_pair(&tfull_bar[ab], 3);  // accumulator ab complete in both CTAs
             }
-            // every MMA this thread issued has completed once this barrier fires
-            umma_commit(&mma_done_bar);
+            // every MMA has completed (in both CTAs' TMEM) once this barrier fires
+            umma_commit_pair(&mma_done_bar, 3);
+            mbar_wait(&mma_done_bar, 0, p.err);
+        } else if (lane == 0) {
+            // peer CTA: its TMEM is written by the leader's MMAs; wait for the last one
             mbar_wait(&mma_done_bar, 0, p.err);
         }
     } else {
@@ -278,15 +291,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         const bool leader = (warp == 2 && lane == 0);
         uint8_t* stg = smem + STAGES * TR::STAGE;  // staging buffers (1024-aligned)
         int gq = 0;                                // quarter tiles done so far
+        const uint32_t tempty_leader0 = map_to_rank(&tempty_bar[0], 0);
+        const uint32_t tempty_leader1 = map_to_rank(&tempty_bar[1], 0);
         for (int lt = 0;; ++lt) {
-            const int t = snake_tile(lt, blockIdx.x, gridDim.x);
+            const int t = snake_tile(lt, pair, npairs);
             if (t >= p.total_tiles || aborted) break;
             const TileCoord c = decode_tile<OP>(p, t);
             const GemmBank& bk = p.bank[c.bi];
             const int ab = lt & 1;
             const uint32_t u = static_cast<uint32_t>(lt >> 1);
-            const int row0 = c.ti * TILE;  // first row of the tile (padded small side)
-            const int col0 = c.tj * BN;    // first column
+            const int row0 = c.ti * PAIR + TILE * rank;  // this CTA's first output row
+            const int col0 = c.tj * PAIR;                // first column
             // what this tile stores: the tile itself, and/or its transpose
             const bool to_direct = TR::sym || OP == OP_XUPDATE || (OP == OP_XUPDATE_OUT && !bk.tall);
             const bool to_mirror = (TR::sym && c.ti != c.tj) || (OP == OP_XUPDATE_OUT && bk.tall);
@@ -340,7 +355,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cta(&tempty_bar[ab]);
+                if (lane == 0) mbar_arrive_cluster(ab ? tempty_leader1 : tempty_leader0);
                 continue;
             }
 
@@ -403,10 +418,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                     }
                 }
                 if (q + 1 == NQ) {
-                    // accumulator ab is free once all four epilogue warps have read it
+                    // accumulator ab is free once the epilogue warps of both CTAs have read it
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive_cta(&tempty_bar[ab]);
+                    if (lane == 0) mbar_arrive_cluster(ab ? tempty_leader1 : tempty_leader0);
                 }
                 fence_proxy_async_smem();
                 named_barrier_sync(1, 128);
@@ -430,23 +445,48 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     }
 
     __syncthreads();
-    if (aborted && warp == 0 && lane == 0) {
-        // Let the copies still in flight land before the CTA's shared memory goes away:
-        // the last load armed on each stage is that stage's latest phase.
+    if (aborted && warp == 0 && lane == 0 && rank == 0) {
+        // Let the copies still in flight land before the pair's shared memory goes away:
+        // both CTAs' loads complete on the leader's barriers, and the last load armed on
+        // each stage is that stage's latest phase (the peer waits in the cluster barrier).
         for (int kb = issued - STAGES < 0 ? 0 : issued - STAGES; kb < issued; ++kb)
             mbar_wait(&full_bar[kb % STAGES], (static_cast<uint32_t>(kb) / STAGES) & 1u, p.err);
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // neither CTA leaves while the pair still uses its memory
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, TR::TMEM_COLS);
+    if (warp == 1) tmem_dealloc_pair(tmem, TR::TMEM_COLS);
 }
+
+static int g_max_pairs[5][64];  // co-resident CTA pairs per op and device (0 = unknown)
 
 template <int OP>
 static cudaError_t launch_op(const GemmParams& p, cudaStream_t stream) {
-    int grid = p.total_tiles < p.sm_count ? p.total_tiles : p.sm_count;
-    gemm_kernel<OP><<<grid, GEMM_THREADS, OpTraits<OP>::SMEM, stream>>>(p);
-    return cudaGetLastError();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e) return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = OpTraits<OP>::SMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int& maxp = g_max_pairs[OP][dev & 63];
+    if (maxp == 0) {
+        cfg.gridDim = dim3(2 * (p.sm_count / 2), 1, 1);
+        int clusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel<OP>, &cfg);
+        if (e) return e;
+        maxp = clusters > 0 ? clusters : 1;
+    }
+    const int pairs = p.total_tiles < maxp ? p.total_tiles : maxp;
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<OP>, p);
 }
 
 cudaError_t launch_gemm(GemmOp op, const GemmParams& p, cudaStream_t stream) {
@@ -461,10 +501,7 @@ cudaError_t launch_gemm(GemmOp op, const GemmParams& p, cudaStream_t stream) {
     return cudaErrorInvalidValue;
 }
 
-int gemm_tile_cols(GemmOp op) {
-    return (op == OP_XUPDATE || op == OP_XUPDATE_OUT) ? OpTraits<OP_XUPDATE>::BN
-                                                      : OpTraits<OP_GRAM>::BN;
-}
+int gemm_tile_cols(GemmOp) { return PAIR; }
 
 cudaError_t gemm_prepare() {
     cudaError_t e;

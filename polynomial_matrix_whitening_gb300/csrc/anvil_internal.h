@@ -7,7 +7,7 @@
 // are then the same three products,
 //     A = Y Y^T,   B = b A + c A A,   Y <- a Y + B Y,
 // because for a tall X, X^T X = Y Y^T and (a X + X B)^T = a Y + B Y (B is symmetric).
-// s_pad rounds s up to 128 and L_pad rounds L up to 256; the padding is zero and
+// s_pad and L_pad round s and L up to 256; the padding is zero and
 // stays zero through every step (zero rows and columns of Y give zero rows and
 // columns of A and B), so it changes no result.
 #pragma once
@@ -19,8 +19,9 @@
 
 namespace anvil {
 
-constexpr int TILE = 128;            // GEMM tile rows, and the padding unit of the small side
-constexpr int LPAD = 256;            // padding unit of the long side (X-update tile columns)
+constexpr int TILE = 128;            // GEMM rows per CTA
+constexpr int PAIR = 256;            // GEMM tile edge per CTA pair, and the padding unit
+constexpr int LPAD = 256;            // padding unit of the long side
 constexpr int BK = 64;               // GEMM k-block: one 128-byte swizzle row of bf16
 constexpr int LBLK = 64;             // momentum-kernel tile edge; one diagonal partial each
 constexpr int MAX_BANKS = 8;         // banks per call
@@ -92,8 +93,8 @@ struct GemmBank {
     const float* d;       // [g] normaliser of this bank's matrices (gram_norm)
     int g, s_pad, L_pad, m, n, tall;
     int out_tma;          // xupdate_out: `out` rows are 16-byte aligned (TMA stores)
-    int T;                // s_pad / TILE
-    int nt_n;             // output tiles along N (T for sym ops, L_pad / TILE for xupdate)
+    int T;                // s_pad / PAIR (row blocks)
+    int nt_n;             // column blocks (T for sym ops, L_pad / PAIR for xupdate)
     int tiles_per_mat;
     int tile_begin;
     int num_kb;           // k-blocks of BK
@@ -101,7 +102,7 @@ struct GemmBank {
 struct GemmParams {
     GemmBank bank[MAX_LAUNCH_BANKS];
     int nbanks, total_tiles;
-    int sm_count;  // persistent grid: min(total_tiles, sm_count) CTAs
+    int sm_count;  // persistent grid: CTA pairs up to the co-resident limit
     float a, b, c;
     unsigned* err;
 };
