@@ -59,8 +59,12 @@ struct OpTraits {
     static constexpr int A_STAGE = TILE * BK * 2;                  // 16 KB: this CTA's A rows
     static constexpr int B_STAGE = TILE * BK * 2;                  // 16 KB: this CTA's B half
     static constexpr int STAGE = A_STAGE + B_STAGE;
-    static constexpr int BUF = has_t ? 2 * QBOX : QBOX;            // one staging buffer
-    static constexpr int STAGING = 2 * BUF;                        // double-buffered
+    // staging boxes: ops with an input stage the whole tile's input (one box per quarter,
+    // loaded as soon as the epilogue starts the tile) and update it in place; the Gram
+    // double-buffers its output boxes; mirrored / transposed outputs use two more boxes.
+    static constexpr int NDIR = has_in ? NQ : 2;
+    static constexpr int NT = has_t ? 2 : 0;
+    static constexpr int STAGING = (NDIR + NT) * QBOX;
     static constexpr int STAGES = (SMEM_MAX - 2048 - STAGING) / STAGE;
     static constexpr int SMEM = STAGES * STAGE + STAGING + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 2 * BN;                  // two accumulators
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     __shared__ __align__(8) uint64_t tfull_bar[2];
     __shared__ __align__(8) uint64_t tempty_bar[2];
     __shared__ __align__(8) uint64_t mma_done_bar;
-    __shared__ __align__(8) uint64_t epi_bar[2];  // epilogue input loads, one per buffer
+    __shared__ __align__(8) uint64_t epi_bar[NQ];  // epilogue input loads, one per quarter
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int aborted;
 
@@ -174,8 +178,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull_bar[b], 1);
             mbar_init(&tempty_bar[b], 8);  // one arrival per epilogue warp of both CTAs
-            mbar_init(&epi_bar[b], 1);
         }
+        for (int q = 0; q < NQ; ++q) mbar_init(&epi_bar[q], 1);
         mbar_init(&mma_done_bar, 1);
         fence_mbar_init();
         aborted = 0;
@@ -195,7 +199,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     int issued = 0;        // producer: k-blocks whose loads were armed (in the whole CTA life)
-    int epi_issued = 0;    // epilogue leader: staging loads armed
+    int epi_tiles = 0;     // epilogue: tiles whose input staging loads were armed
 
     if (warp == 0) {
         if (lane == 0) {
@@ -312,13 +316,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                 dd = __fmul_rn(d, d);
             }
 
-            if (staged && TR::has_in && leader) {
-                // input of the first quarter; both buffers' last stores must be done reading
-                bulk_wait_read_all();
-                const int buf = gq & 1;
-                mbar_arrive_expect_tx(&epi_bar[buf], QBOX);
-                tma_load_3d(stg + buf * TR::BUF, &bk.tm_c, &epi_bar[buf], col0, row0, c.mat);
-                epi_issued = gq + 1;
+            const uint32_t in_phase = static_cast<uint32_t>(epi_tiles) & 1u;
+            if (staged && TR::has_in) {
+                // the whole tile's input, one box per quarter, once every earlier store
+                // has finished reading the boxes
+                if (leader) {
+                    bulk_wait_read_all();
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) {
+                        mbar_arrive_expect_tx(&epi_bar[q], QBOX);
+                        tma_load_3d(stg + q * QBOX, &bk.tm_c, &epi_bar[q], col0 + 64 * q, row0, c.mat);
+                    }
+                }
+                ++epi_tiles;
             }
             if (!mbar_wait(&tfull_bar[ab], u & 1u, p.err)) {
                 aborted = 1;
@@ -361,25 +371,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
 
             bool ok = true;
             for (int q = 0; q < NQ; ++q, ++gq) {
-                const int buf = gq & 1;
-                uint8_t* dbox = stg + buf * TR::BUF;    // 128 rows x 64 cols, 128-byte swizzle
-                uint8_t* tbox = dbox + QBOX;            // 64 rows x 128 cols, plain
-                if (TR::has_in) {
-                    if (leader && q + 1 < NQ) {
-                        bulk_wait_read_all();
-                        mbar_arrive_expect_tx(&epi_bar[buf ^ 1], QBOX);
-                        tma_load_3d(stg + (buf ^ 1) * TR::BUF, &bk.tm_c, &epi_bar[buf ^ 1],
-                                    col0 + 64 * (q + 1), row0, c.mat);
-                        epi_issued = gq + 2;
-                    }
-                    if (!mbar_wait(&epi_bar[buf], (static_cast<uint32_t>(gq) >> 1) & 1u, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                } else {
-                    // no input: the buffer must be free of its last store before any write
-                    if (leader) bulk_wait_read_all();
+                // direct box: the tile's q-th input box (updated in place), or the Gram's
+                // double-buffered output box; transposed boxes alternate
+                uint8_t* dbox = stg + (TR::has_in ? q : (gq & 1)) * QBOX;
+                uint8_t* tbox = stg + (TR::NDIR + (gq & 1)) * QBOX;  // 64 rows x 128 cols, plain
+                if (!TR::has_in || TR::has_t) {
+                    // boxes written below must be free of the store issued two quarters ago
+                    if (leader) bulk_wait_read_but_one();
                     named_barrier_sync(1, 128);
+                }
+                if (TR::has_in && !mbar_wait(&epi_bar[q], in_phase, p.err)) {
+                    ok = false;
+                    break;
                 }
                 uint8_t* drow = dbox + r * 128;
 #pragma unroll
@@ -438,9 +441,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         }
         if (leader) {
             bulk_wait_all();  // every store of this CTA has completed
-            if (aborted)      // and every staging load it armed has landed
-                for (int g = epi_issued - 2 < 0 ? 0 : epi_issued - 2; g < epi_issued; ++g)
-                    mbar_wait(&epi_bar[g & 1], (static_cast<uint32_t>(g) >> 1) & 1u, p.err);
+            if (aborted && epi_tiles > 0)  // and every staging load it armed has landed
+                for (int q = 0; q < NQ; ++q)
+                    mbar_wait(&epi_bar[q], static_cast<uint32_t>(epi_tiles - 1) & 1u, p.err);
         }
     }
 
