@@ -32,6 +32,36 @@ __device__ __forceinline__ float bf2f(uint16_t h) {
 }
 __device__ __forceinline__ float round_bf(float x) { return bf2f(f2bf(x)); }
 
+// ---- packed pairs: two fp32 in one 64-bit register (element 0 in the low half), and two
+// bf16 in one 32-bit word (element 0 in the low half).  The f32x2 operations are two
+// independent IEEE round-to-nearest operations.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// two bf16 (round to nearest even) of a packed fp32 pair
+__device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+        : "=r"(d)
+        : "f"(__uint_as_float(static_cast<uint32_t>(v >> 32))),
+          "f"(__uint_as_float(static_cast<uint32_t>(v))));
+    return d;
+}
+// packed fp32 pair of two bf16 (exact)
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
+    return (static_cast<uint64_t>(w & 0xffff0000u) << 32) | (w << 16);
+}
+
 // ---- mbarrier -----------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

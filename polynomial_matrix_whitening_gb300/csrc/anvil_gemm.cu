@@ -47,6 +47,7 @@ namespace anvil {
 
 constexpr int SMEM_MAX = 227 * 1024;  // opt-in dynamic shared memory per block
 constexpr int QBOX = TILE * 64 * 2;   // one 128 x 64 bf16 staging box (16 KB)
+constexpr int EPI_GROUPS = 2;         // epilogue warp groups, one per half of the columns
 
 template <int OP>
 struct OpTraits {
@@ -59,18 +60,21 @@ struct OpTraits {
     static constexpr int A_STAGE = TILE * BK * 2;                  // 16 KB: this CTA's A rows
     static constexpr int B_STAGE = TILE * BK * 2;                  // 16 KB: this CTA's B half
     static constexpr int STAGE = A_STAGE + B_STAGE;
-    // staging boxes: ops with an input stage the whole tile's input (one box per quarter,
-    // loaded as soon as the epilogue starts the tile) and update it in place; the Gram
-    // double-buffers its output boxes; mirrored / transposed outputs use two more boxes.
-    static constexpr int NDIR = has_in ? NQ : 2;
-    static constexpr int NT = has_t ? 2 : 0;
+    // staging boxes (16 KB each): ops with an input stage the whole tile's input (one box
+    // per quarter, loaded as soon as the epilogue starts the tile) and update it in place;
+    // the Gram has one output box per epilogue group; mirrored / transposed outputs add
+    // one transposed box per group.
+    static constexpr int NDIR = has_in ? NQ : EPI_GROUPS;
+    static constexpr int NT = has_t ? EPI_GROUPS : 0;
     static constexpr int STAGING = (NDIR + NT) * QBOX;
     static constexpr int STAGES = (SMEM_MAX - 2048 - STAGING) / STAGE;
     static constexpr int SMEM = STAGES * STAGE + STAGING + 1024;   // + alignment slack
     static constexpr uint32_t TMEM_COLS = 2 * BN;                  // two accumulators
 };
 
-constexpr int GEMM_THREADS = 192;  // 6 warps
+// warp 0: TMA producer; warp 1: TMEM owner and MMA issuer; warps 2-9: epilogue, in two
+// groups of four (one warp per TMEM lane quadrant), group h owning quarters 2h, 2h+1.
+constexpr int GEMM_THREADS = 64 + EPI_GROUPS * 128;
 
 __device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&f)[32]) {
     const uint4* p = reinterpret_cast<const uint4*>(src);
@@ -148,6 +152,22 @@ __device__ __forceinline__ uint16_t epi_value(const GemmParams& p, float v, floa
     return f2bf(__fadd_rn(__fmul_rn(p.a, x), v));                   // a Y + acc
 }
 
+// The same on a pair: accumulator values v (packed fp32 pair), input word xw (two bf16);
+// returns two bf16.  Rounding is identical to epi_value (each product and sum rounded).
+template <int OP>
+__device__ __forceinline__ uint32_t epi_pair(uint64_t v, uint32_t xw, uint64_t coef_x,
+                                             uint64_t coef_v, float dd) {
+    if (OP == OP_GRAM) return f2_to_bf2(v);
+    if (OP == OP_GRAM_NORM) {
+        const float lo = __fdiv_rn(round_bf(__uint_as_float(static_cast<uint32_t>(v))), dd);
+        const float hi = __fdiv_rn(round_bf(__uint_as_float(static_cast<uint32_t>(v >> 32))), dd);
+        return f2_to_bf2(f2_pack(lo, hi));
+    }
+    const uint64_t t = f2_mul(coef_x, bf2_to_f2(xw));  // b A  or  a Y
+    if (OP == OP_SQPOLY) return f2_to_bf2(f2_add(t, f2_mul(coef_v, v)));  // + c acc
+    return f2_to_bf2(f2_add(t, v));                                          // + acc
+}
+
 template <int OP>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
     using TR = OpTraits<OP>;
@@ -177,7 +197,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull_bar[b], 1);
-            mbar_init(&tempty_bar[b], 8);  // one arrival per epilogue warp of both CTAs
+            mbar_init(&tempty_bar[b], 2 * 4 * EPI_GROUPS);  // each epilogue warp, both CTAs
         }
         for (int q = 0; q < NQ; ++q) mbar_init(&epi_bar[q], 1);
         mbar_init(&mma_done_bar, 1);
@@ -289,14 +309,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             mbar_wait(&mma_done_bar, 0, p.err);
         }
     } else {
-        // ---------------- epilogue: warps 2-5, TMEM lane quadrant = warp % 4
+        // ---------------- epilogue: warps 2-9, TMEM lane quadrant = warp % 4
         const int quad = warp & 3;
-        const int r = quad * 32 + lane;  // row within the tile
-        const bool leader = (warp == 2 && lane == 0);
-        uint8_t* stg = smem + STAGES * TR::STAGE;  // staging buffers (1024-aligned)
-        int gq = 0;                                // quarter tiles done so far
+        const int grp = (warp - 2) >> 2;          // column half of this warp group
+        const int r = quad * 32 + lane;           // row within the tile
+        const bool leader = ((warp - 2) & 3) == 0 && lane == 0;
+        uint8_t* stg = smem + STAGES * TR::STAGE;  // staging boxes (1024-aligned)
         const uint32_t tempty_leader0 = map_to_rank(&tempty_bar[0], 0);
         const uint32_t tempty_leader1 = map_to_rank(&tempty_bar[1], 0);
+        const uint64_t coef_x = f2_pack(OP == OP_SQPOLY ? p.b : p.a, OP == OP_SQPOLY ? p.b : p.a);
+        const uint64_t coef_v = f2_pack(p.c, p.c);
         for (int lt = 0;; ++lt) {
             const int t = snake_tile(lt, pair, npairs);
             if (t >= p.total_tiles || aborted) break;
@@ -318,12 +340,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
 
             const uint32_t in_phase = static_cast<uint32_t>(epi_tiles) & 1u;
             if (staged && TR::has_in) {
-                // the whole tile's input, one box per quarter, once every earlier store
-                // has finished reading the boxes
+                // this group's quarters of the tile's input, once this group's earlier
+                // stores have finished reading the boxes
                 if (leader) {
                     bulk_wait_read_all();
-#pragma unroll
-                    for (int q = 0; q < NQ; ++q) {
+                    for (int q = 2 * grp; q < 2 * grp + 2; ++q) {
                         mbar_arrive_expect_tx(&epi_bar[q], QBOX);
                         tma_load_3d(stg + q * QBOX, &bk.tm_c, &epi_bar[q], col0 + 64 * q, row0, c.mat);
                     }
@@ -340,12 +361,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
 
             if (!staged) {
                 // OP_XUPDATE_OUT into an `out` whose rows are not 16-byte aligned: plain
-                // bounds-checked stores straight from the accumulator.
+                // bounds-checked stores straight from the accumulator (this group's half).
                 const int m = bk.m, n = bk.n;
                 uint16_t* out = bk.dst + static_cast<size_t>(c.mat) * m * n;
                 const int row = row0 + r;
 #pragma unroll 1
-                for (int cc = 0; cc < BN / 32; ++cc) {
+                for (int cc = 4 * grp; cc < 4 * grp + 4; ++cc) {
                     const int cb = col0 + cc * 32;
                     float x[32];
                     load32_bf16(bk.src + (static_cast<size_t>(c.mat) * bk.s_pad + row) * bk.L_pad + cb, x);
@@ -370,15 +391,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             }
 
             bool ok = true;
-            for (int q = 0; q < NQ; ++q, ++gq) {
-                // direct box: the tile's q-th input box (updated in place), or the Gram's
-                // double-buffered output box; transposed boxes alternate
-                uint8_t* dbox = stg + (TR::has_in ? q : (gq & 1)) * QBOX;
-                uint8_t* tbox = stg + (TR::NDIR + (gq & 1)) * QBOX;  // 64 rows x 128 cols, plain
+            for (int q = 2 * grp; q < 2 * grp + 2; ++q) {
+                // direct box: the tile's q-th input box (updated in place), or the group's
+                // output box; transposed box: the group's
+                uint8_t* dbox = stg + (TR::has_in ? q : grp) * QBOX;
+                uint8_t* tbox = stg + (TR::NDIR + grp) * QBOX;  // 64 rows x 128 cols, plain
                 if (!TR::has_in || TR::has_t) {
-                    // boxes written below must be free of the store issued two quarters ago
-                    if (leader) bulk_wait_read_but_one();
-                    named_barrier_sync(1, 128);
+                    // the boxes written below must be free of this group's last store
+                    if (leader) bulk_wait_read_all();
+                    named_barrier_sync(1 + grp, 128);
                 }
                 if (TR::has_in && !mbar_wait(&epi_bar[q], in_phase, p.err)) {
                     ok = false;
@@ -399,35 +420,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                             const uint4 x = *cp;
                             xw[0] = x.x; xw[1] = x.y; xw[2] = x.z; xw[3] = x.w;
                         }
-                        uint16_t o[8];
+                        uint32_t o[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            o[2 * e] = epi_value<OP>(p, v[8 * w + 2 * e],
-                                                     bf2f(static_cast<uint16_t>(xw[e] & 0xffffu)), dd);
-                            o[2 * e + 1] = epi_value<OP>(p, v[8 * w + 2 * e + 1],
-                                                         bf2f(static_cast<uint16_t>(xw[e] >> 16)), dd);
-                        }
-                        if (to_direct)
-                            *cp = make_uint4(static_cast<uint32_t>(o[0]) | (static_cast<uint32_t>(o[1]) << 16),
-                                             static_cast<uint32_t>(o[2]) | (static_cast<uint32_t>(o[3]) << 16),
-                                             static_cast<uint32_t>(o[4]) | (static_cast<uint32_t>(o[5]) << 16),
-                                             static_cast<uint32_t>(o[6]) | (static_cast<uint32_t>(o[7]) << 16));
+                        for (int e = 0; e < 4; ++e)
+                            o[e] = epi_pair<OP>(f2_pack(v[8 * w + 2 * e], v[8 * w + 2 * e + 1]), xw[e],
+                                                coef_x, coef_v, dd);
+                        if (to_direct) *cp = make_uint4(o[0], o[1], o[2], o[3]);
                         if (TR::has_t && to_mirror) {
                             // transposed box: element (row r, column 8j + e) at [8j + e][r]
                             uint16_t* tcol = reinterpret_cast<uint16_t*>(tbox) + r;
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) tcol[(8 * j + e) * TILE] = o[e];
+                            for (int e = 0; e < 4; ++e) {
+                                tcol[(8 * j + 2 * e) * TILE] = static_cast<uint16_t>(o[e] & 0xffffu);
+                                tcol[(8 * j + 2 * e + 1) * TILE] = static_cast<uint16_t>(o[e] >> 16);
+                            }
                         }
                     }
                 }
-                if (q + 1 == NQ) {
-                    // accumulator ab is free once the epilogue warps of both CTAs have read it
+                if (q == 2 * grp + 1) {
+                    // accumulator ab is free once every epilogue warp of both CTAs has read it
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive_cluster(ab ? tempty_leader1 : tempty_leader0);
                 }
                 fence_proxy_async_smem();
-                named_barrier_sync(1, 128);
+                named_barrier_sync(1 + grp, 128);
                 if (leader) {
                     if (to_direct) tma_store_3d(&bk.tm_d, dbox, col0 + 64 * q, row0, c.mat);
                     if (TR::has_t && to_mirror) tma_store_3d(&bk.tm_e, tbox, row0, col0 + 64 * q, c.mat);
@@ -440,9 +457,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             }
         }
         if (leader) {
-            bulk_wait_all();  // every store of this CTA has completed
+            bulk_wait_all();  // every store of this group has completed
             if (aborted && epi_tiles > 0)  // and every staging load it armed has landed
-                for (int q = 0; q < NQ; ++q)
+                for (int q = 2 * grp; q < 2 * grp + 2; ++q)
                     mbar_wait(&epi_bar[q], static_cast<uint32_t>(epi_tiles - 1) & 1u, p.err);
         }
     }
