@@ -305,7 +305,7 @@ def run_anvil(args, world, rank, local):
     alg, dense = step_flops(wl.banks)
 
     # ---- per-kernel CUDA-event durations over timed steps (same launches, not in a graph)
-    prof_steps = max(3, min(nsteps, 10))
+    prof_steps = max(3, min(nsteps, 20))
     with torch.cuda.stream(stream):
         for s in range(2):
             for b, gt in zip(banks, pool_d[s % wl.pool]):
@@ -357,33 +357,60 @@ def run_anvil(args, world, rank, local):
                   if k in ("gram", "gram_norm", "sqpoly", "xupdate", "xupdate_out")) / prof_steps
     mom_ms = per_kind.get("momentum", [1, 0.0])[1] / prof_steps
 
-    # ---- end to end: pinned host gradients in, outputs out, every step
+    # ---- end to end: every step copies its gradients in from pinned host memory and
+    # its outputs back; the copies of neighbouring steps overlap the current step's
+    # compute (two device buffer sets, one upload and one download stream), all inside
+    # the timed region.
     host_pool = [[torch.from_numpy(x).pin_memory() for x in p] for p in pool_h]
-    gbuf = [torch.empty_like(x) for x in pool_d[0]]
+    gbufs = [[torch.empty_like(x) for x in pool_d[0]] for _ in range(2)]
+    outs = [[torch.empty_like(b.out) for b in banks] for _ in range(2)]
     out_h = [torch.empty(b.out.shape, dtype=torch.bfloat16).pin_memory() for b in banks]
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev = {k: [torch.cuda.Event() for _ in range(2)] for k in ("h2d", "comp", "d2h")}
+    main_outs = [b.out for b in banks]
+    g_e2e = []
     with torch.cuda.stream(stream):
-        g_e2e = capture(gbuf)
-        for s in range(nwarm):
-            for dst, src in zip(gbuf, host_pool[s % wl.pool]):
-                dst.copy_(src, non_blocking=True)
-            g_e2e.replay()
-            for dst, b in zip(out_h, banks):
-                dst.copy_(b.out, non_blocking=True)
+        for bset in range(2):
+            for b, o in zip(banks, outs[bset]):
+                b.out = o
+            g_e2e.append(capture(gbufs[bset]))
+    for b, o in zip(banks, main_outs):
+        b.out = o
+    torch.cuda.synchronize()
+
+    def e2e_steps(first, count):
+        for s in range(first, first + count):
+            bset = s & 1
+            with torch.cuda.stream(h2d_s):
+                if s >= 2:
+                    h2d_s.wait_event(ev["comp"][bset])      # step s-2 done reading gbufs[bset]
+                for dst, src in zip(gbufs[bset], host_pool[s % wl.pool]):
+                    dst.copy_(src, non_blocking=True)
+                ev["h2d"][bset].record(h2d_s)
+            stream.wait_event(ev["h2d"][bset])
+            if s >= 2:
+                stream.wait_event(ev["d2h"][bset])          # outs[bset] of step s-2 copied out
+            with torch.cuda.stream(stream):
+                g_e2e[bset].replay()
+            ev["comp"][bset].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(ev["comp"][bset])
+                for dst, o in zip(out_h, outs[bset]):
+                    dst.copy_(o, non_blocking=True)
+                ev["d2h"][bset].record(d2h_s)
+
+    e2e_steps(0, nwarm)
     torch.cuda.synchronize()
     barrier(world)
     q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        q0.record(stream)
-        for s in range(nsteps):
-            for dst, src in zip(gbuf, host_pool[s % wl.pool]):
-                dst.copy_(src, non_blocking=True)
-            g_e2e.replay()
-            for dst, b in zip(out_h, banks):
-                dst.copy_(b.out, non_blocking=True)
-        q1.record(stream)
+    q0.record(h2d_s)
+    e2e_steps(nwarm, nsteps)
+    d2h_s.wait_event(ev["comp"][(nwarm + nsteps - 1) & 1])
+    q1.record(d2h_s)
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(q0.elapsed_time(q1) / nsteps, world)
+    gbuf = gbufs[0]
     h2d = sum(x.numel() * 4 for x in gbuf)
     d2h = sum(b.out.numel() * 2 for b in banks)
     if not all(torch.isfinite(b.out.float()).all() for b in banks):
@@ -451,7 +478,7 @@ def run_ncu_case():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["anvil", "reference"], default="anvil")
     ap.add_argument("--no-cpu-baseline", action="store_true")

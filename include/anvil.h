@@ -21,7 +21,10 @@
  * Every number is computed on the GPU by this library's own kernels; there is
  * no CPU path.  All calls are asynchronous on the given stream (a
  * cudaStream_t / CUstream handle passed as void*; NULL = legacy default
- * stream).  No call below allocates, frees or synchronises, except
+ * stream).  One kernel of each step (the normalisation) runs on a second stream of the
+ * library's, forked from and joined back to the caller's stream by events (a captured
+ * graph holds it as a parallel branch).  No call below allocates, frees or
+ * synchronises, except
  * anvil_bank_step on its first use of a size (documented there) and the
  * diagnostic anvil_device_error.  Errors are returned as status codes; no
  * exception crosses the ABI.
@@ -185,7 +188,7 @@ anvil_status anvil_selftest_wait_timeout(unsigned timeout_us, void* stream);
 typedef enum {
     ANVIL_KERNEL_MOMENTUM = 0,     /* momentum + cast + diagonal partials */
     ANVIL_KERNEL_NORM_D = 1,       /* d per matrix */
-    ANVIL_KERNEL_NORMALIZE = 2,    /* X <- bf16(X / d) */
+    ANVIL_KERNEL_NORMALIZE = 2,    /* X <- bf16(X / d), on the second stream */
     ANVIL_KERNEL_GRAM_NORM = 3,    /* first Gram, A = bf16(bf16(X X^T) / d^2) */
     ANVIL_KERNEL_GRAM = 4,         /* A = bf16(X X^T) */
     ANVIL_KERNEL_SQPOLY = 5,       /* B = bf16(b A + c A A) */

@@ -4,13 +4,14 @@
 //
 //   momentum + cast (+ diagonal partials)   -> Y0 = X_raw
 //   d = sqrt(tr) * margin + eps             (tr from the bf16 diagonal of the first Gram)
-//   A = bf16(bf16(Y0 Y0^T) / d^2)           first Gram, on the unnormalised X
-//   Y0 <- bf16(Y0 / d)
-//   map k = 0..nmaps-1, reading Y[k%2], writing Y[(k+1)%2] (out for the last map):
+//   A = bf16(bf16(Y0 Y0^T) / d^2), then map 0's B     } on the caller's stream, while
+//   Y1 = bf16(Y0 / d)                                  } the second stream normalises
+//   map k = 0..nmaps-1, reading Y[(k+1)%2], writing Y[k%2] (out for the last map):
 //     [k > 0] A = bf16(Y Y^T);  B = bf16(b A + c A A);  Y' = bf16(a Y + B Y)
+//   (map 0's X-update waits for the normalisation)
 //
-// Every phase is one grouped launch over all banks of the call (two when more than
-// four banks), 4 + 3 * nmaps launches in all, on the caller's stream.
+// Every phase is one grouped launch over all banks of the call (GEMM phases: two when
+// more than four banks), 3 + 3 * nmaps launches in all.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -50,6 +51,8 @@ struct DeviceState {
     anvil_status status = ANVIL_OK;
     unsigned* err = nullptr;
     int sm_count = 0;
+    cudaStream_t side = nullptr;  // the normalisation's stream
+    cudaEvent_t fork = nullptr, join = nullptr;
 };
 std::mutex g_dev_mutex;
 DeviceState g_dev[64];
@@ -94,6 +97,10 @@ anvil_status device_setup(DeviceState** out) {
             return cuda_fail(e, "cudaDeviceGetAttribute");
         st.err = device_error_word();
         if (!st.err) return cuda_fail(cudaGetLastError(), "cudaGetSymbolAddress(error word)");
+        if ((e = cudaStreamCreateWithFlags(&st.side, cudaStreamNonBlocking)) ||
+            (e = cudaEventCreateWithFlags(&st.fork, cudaEventDisableTiming)) ||
+            (e = cudaEventCreateWithFlags(&st.join, cudaEventDisableTiming)))
+            return cuda_fail(e, "stream/event creation");
         st.ready = true;
     }
     *out = &st;
@@ -359,6 +366,7 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
             const Geom& G = L.bank[i];
             NormBank& N = np.bank[i];
             N.y = P[i].y[0];
+            N.y_out = P[i].y[1];
             N.part = P[i].part;
             N.g = G.g;
             N.s_pad = G.s_pad;
@@ -406,7 +414,8 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
                 const Geom& G = L.bank[i];
                 const BankPtrs& B = P[i];
                 GemmBank& gb = gp.bank[nb];
-                const int cur = k & 1;
+                // the first Gram reads X_raw (Y0); map k reads Y[(k+1)%2], writes Y[k%2]
+                const int cur = op == OP_GRAM_NORM ? 0 : ((k + 1) & 1);
                 gb.g = G.g;
                 gb.s_pad = G.s_pad;
                 gb.L_pad = G.L_pad;
@@ -472,15 +481,16 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
     };
 
     const anvil_map none = {0.f, 0.f, 0.f};
-    if ((st = gemm_phase(OP_GRAM_NORM, 0, none))) return st;
-    if ((e = profiled(ANVIL_KERNEL_NORMALIZE, stream, [&] { return launch_normalize(np, stream); })))
+    // normalisation (Y1 = bf16(Y0 / d)) on the second stream, beside the first Gram
+    if ((e = cudaEventRecord(dev->fork, stream)) || (e = cudaStreamWaitEvent(dev->side, dev->fork, 0)))
+        return cuda_fail(e, "fork");
+    if ((e = profiled(ANVIL_KERNEL_NORMALIZE, dev->side, [&] { return launch_normalize(np, dev->side); })))
         return cuda_fail(e, "normalize launch");
+    if ((e = cudaEventRecord(dev->join, dev->side))) return cuda_fail(e, "join");
+    if ((st = gemm_phase(OP_GRAM_NORM, 0, none))) return st;
     const Geom& G0 = L.bank[0];
     const size_t nx1 = static_cast<size_t>(G0.g) * G0.m * G0.n;
     const size_t na1 = static_cast<size_t>(G0.g) * G0.s * G0.s;
-    if (trace && trace->X &&
-        (e = launch_extract_x(P[0].y[0], trace->X, G0.g, G0.m, G0.n, G0.tall, G0.s_pad, G0.L_pad, stream)))
-        return cuda_fail(e, "trace");
     for (int k = 0; k < nmaps; ++k) {
         if (k > 0 && (st = gemm_phase(OP_GRAM, k, maps[k]))) return st;
         if (trace && trace->A &&
@@ -490,6 +500,14 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         if (trace && trace->B &&
             (e = launch_extract_sq(P[0].b, trace->B + k * na1, G0.g, G0.s, G0.s_pad, stream)))
             return cuda_fail(e, "trace");
+        if (k == 0) {
+            // map 0's X-update is the first reader of the normalised X
+            if ((e = cudaStreamWaitEvent(stream, dev->join, 0))) return cuda_fail(e, "join");
+            if (trace && trace->X &&
+                (e = launch_extract_x(P[0].y[1], trace->X, G0.g, G0.m, G0.n, G0.tall, G0.s_pad,
+                                      G0.L_pad, stream)))
+                return cuda_fail(e, "trace");
+        }
         const bool last = k == nmaps - 1;
         if ((st = gemm_phase(last ? OP_XUPDATE_OUT : OP_XUPDATE, k, maps[k]))) return st;
         if (trace && trace->X) {
@@ -497,7 +515,7 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
                 if ((e = cudaMemcpyAsync(trace->X + (k + 1) * nx1, banks[0].out, 2 * nx1,
                                          cudaMemcpyDeviceToDevice, stream)))
                     return cuda_fail(e, "trace");
-            } else if ((e = launch_extract_x(P[0].y[(k + 1) & 1], trace->X + (k + 1) * nx1, G0.g,
+            } else if ((e = launch_extract_x(P[0].y[k & 1], trace->X + (k + 1) * nx1, G0.g,
                                              G0.m, G0.n, G0.tall, G0.s_pad, G0.L_pad, stream))) {
                 return cuda_fail(e, "trace");
             }

@@ -159,6 +159,7 @@ __device__ __forceinline__ uint32_t epi_pair(uint64_t v, uint32_t xw, uint64_t c
                                              uint64_t coef_v, float dd) {
     if (OP == OP_GRAM) return f2_to_bf2(v);
     if (OP == OP_GRAM_NORM) {
+        // bf16(bf16(acc) / d^2), the quotient correctly rounded in fp32
         const float lo = __fdiv_rn(round_bf(__uint_as_float(static_cast<uint32_t>(v))), dd);
         const float hi = __fdiv_rn(round_bf(__uint_as_float(static_cast<uint32_t>(v >> 32))), dd);
         return f2_to_bf2(f2_pack(lo, hi));

@@ -54,7 +54,8 @@ cudaError_t launch_momentum(const MomentumParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- d and normalisation
 struct NormBank {
-    uint16_t* y;        // [g, s_pad, L_pad]
+    const uint16_t* y;  // X_raw [g, s_pad, L_pad]
+    uint16_t* y_out;    // normalised X [g, s_pad, L_pad]
     const float* part;  // [g, nlb, s_pad]
     int g, s_pad, L_pad, nlb;
     int mat_begin;      // first matrix of this bank among all matrices of the call
@@ -70,7 +71,7 @@ struct NormParams {
 };
 // d[mat] = sqrt(sum_i float(bf16(sum of the partials of i))) * margin + eps.
 cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream);
-// Y <- bf16(float(Y) / d[mat]) in place over every bank.
+// Y_out <- bf16(float(Y) / d[mat]) over every bank.
 cudaError_t launch_normalize(const NormParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- tcgen05 GEMMs
@@ -118,6 +119,7 @@ cudaError_t launch_extract_x(const uint16_t* y, uint16_t* dst, int g, int m, int
 cudaError_t launch_extract_sq(const uint16_t* src, uint16_t* dst, int g, int s, int s_pad,
                               cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned timeout_us, unsigned* err, cudaStream_t stream);
+
 
 // Device address of the current device's error word (null if it cannot be had).
 unsigned* device_error_word();
