@@ -45,7 +45,10 @@ WORKLOAD = "full_step"
 # ncu DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
 # kernel kind on this workload, from the capture summarised under profiles/; valid only
 # while the kernel source hashes to the recorded value.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/gemm_full_step.md: X-update of map 1 over all three banks
+    "xupdate": {"bytes_per_launch": 281.1e6, "source_hash": "aa89ca42115ad2e7"},
+}
 
 
 def kernel_source_hash(kind):
@@ -192,30 +195,34 @@ def barrier(world):
 
 # ------------------------------------------------------------------ the CPU oracle arm
 
-def oracle_sample(wl, per_bank):
+def oracle_sample(wl, per_bank, min_seconds=0.0):
     """Times the oracle on `per_bank` matrices of each bank of the workload (step 0 of the
-    grad pool, zero rails) and extrapolates to matrices/s of the full step."""
+    grad pool, zero rails; the first of each bank Gaussian, the second rank-32 + noise),
+    repeated until at least `min_seconds` of CPU work, and extrapolates the mean time per
+    matrix of each bank to matrices/s of the full step."""
     import oracle
     oracle.build()
-    secs = 0.0
-    est = 0.0
-    picks = []
+    picks, samples = [], []
     for j, b in enumerate(wl.banks):
         grad = wl.grad(j, 0)
         idx = [0, b.g // 2][:per_bank] if per_bank <= 2 else list(range(per_bank))
-        t_sum = 0.0
-        for i in idx:
-            g1 = np.ascontiguousarray(grad[i:i + 1])
+        picks.append(f"{b.name}{list(idx)}")
+        samples += [(j, np.ascontiguousarray(grad[i:i + 1])) for i in idx]
+    sc = wl.scalars(0)
+    times = [[] for _ in wl.banks]
+    secs, rounds = 0.0, 0
+    while rounds == 0 or secs < min_seconds:
+        for j, g1 in samples:
             v1 = np.zeros((2,) + g1.shape, np.float32)
-            sc = wl.scalars(0)
             t0 = time.perf_counter()
             oracle.bank_step(g1, v1, sc.momentum, sc.fast_beta, sc.fast_weight, sc.slow_beta)
-            t_sum += time.perf_counter() - t0
-        secs += t_sum
-        est += b.g * t_sum / len(idx)
-        picks.append(f"{b.name}{list(idx)}")
+            dt = time.perf_counter() - t0
+            times[j].append(dt)
+            secs += dt
+        rounds += 1
+    est = sum(b.g * statistics.mean(times[j]) for j, b in enumerate(wl.banks))
     total = sum(b.g for b in wl.banks)
-    return total / est, secs, oracle.num_threads(), ", ".join(picks)
+    return total / est, secs, oracle.num_threads(), ", ".join(picks) + f" x {rounds} rounds"
 
 
 def run_reference(args, world, rank):
@@ -420,10 +427,10 @@ def run_anvil(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, secs, cores, picks = oracle_sample(wl, 2)
+        v, secs, cores, picks = oracle_sample(wl, 2, min_seconds=10.0)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"two matrices of each bank ({picks}) timed once each ({secs:.1f} s), "
-                         f"extrapolated to the 66-matrix step"}
+               "sample": f"two matrices of each bank ({picks}; {secs:.1f} s of CPU work), "
+                         f"mean time per matrix extrapolated to the 66-matrix step"}
 
     if rank == 0:
         clocks = sampler.summary()
