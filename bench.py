@@ -166,14 +166,19 @@ class ClockSampler:
 # ------------------------------------------------------------------ distributed plumbing
 
 def dist_setup():
+    """Replicas: one process per GPU (NCCL), or gloo when no GPU is present (host tests).
+    The collectives are only the barrier and the max-over-ranks of the step time."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     return world, rank, local
 
 
@@ -182,9 +187,17 @@ def max_over_ranks(x, world):
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(ms_local, mats_per_rank, world):
+    """Whole-job matrices/s of independent replicas: every rank's matrices over the
+    slowest rank's step time."""
+    ms = max_over_ranks(ms_local, world)
+    return ms, mats_per_rank * world / (ms / 1000.0)
 
 
 def barrier(world):
@@ -306,9 +319,8 @@ def run_anvil(args, world, rank, local):
         torch.cuda.synchronize()
     barrier(world)
     ms = e0.elapsed_time(e1) / nsteps
-    ms_max = max_over_ranks(ms, world)
     mats = sum(b.shape[0] for b in banks)
-    value = mats * world / (ms_max / 1000.0)
+    ms_max, value = job_value(ms, mats, world)
     alg, dense = step_flops(wl.banks)
 
     # ---- per-kernel CUDA-event durations over timed steps (same launches, not in a graph)

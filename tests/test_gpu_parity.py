@@ -186,6 +186,36 @@ def test_stages_match_oracle(A, shape):
             assert np.all(np.abs(Xn - C) <= _gemm_bound(C, aC, s_dim + 2)), ("xupdate", k)
 
 
+# Other coefficient sets through the same kernels: the ABI takes any maps[] / nmaps.
+NS_CUBIC = (1.5, -0.5, 0.0)  # the textbook cubic Newton-Schulz step x -> 1.5 x - 0.5 x^3
+OTHER_MAPS = {
+    "ns_cubic_x5": [NS_CUBIC] * 5,
+    "single_map": [(3.923798038567, -6.095026865488, 3.905234618423)],
+    "sixteen_maps": [NS_CUBIC] * 10 + [(2.0, -1.5, 0.5)] * 6,
+    "mixed": [(2.0, -1.5, 0.5), (1.875, -1.25, 0.375), NS_CUBIC],
+}
+
+
+@pytest.mark.parametrize("name", sorted(OTHER_MAPS))
+@pytest.mark.parametrize("shape", [(3, 256, 768), (2, 520, 264)], ids=lambda s: "x".join(map(str, s)))
+def test_other_coefficient_sets(A, name, shape):
+    maps = OTHER_MAPS[name]
+    g, m, n = shape
+    grad, vel = W.random_case(77 + len(maps), g, m, n)
+    sc = dict(momentum=0.95, fast_beta=0.85, fast_weight=0.4385, slow_beta=0.98)
+    bank = gpu_bank(A, grad, vel, sc)
+    A.multi_bank_step([bank], A.alloc_workspace([shape]), maps=maps, margin=1.05, eps=1e-6)
+    torch.cuda.synchronize()
+    out, vel_or = oracle.bank_step(grad, vel, sc["momentum"], sc["fast_beta"], sc["fast_weight"],
+                                   sc["slow_beta"], maps=maps)
+    vg = bank.velocity.cpu().numpy()
+    assert np.max(np.abs(vg - vel_or)) <= VEL_RTOL * np.max(np.abs(vel_or))
+    got = bits(bank.out)
+    for i in range(g):
+        assert np.isfinite(f64(got[i])).all()
+        assert rel(f64(got[i]), f64(out[i])) <= OUT_RTOL, (name, i)
+
+
 def test_zero_grad_gives_zero_output(A):
     shape = (2, 300, 130)
     grad = np.zeros(shape, np.float32)
