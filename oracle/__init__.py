@@ -78,6 +78,8 @@ def lib():
         L.oracle_cascade_f64.restype = i
         L.oracle_bank_step.argtypes = [vp, vp, i, i, i, f, f, f, f, vp, i, f, f, i, vp]
         L.oracle_bank_step.restype = i
+        L.oracle_rail_equalizer.argtypes = [vp, i, i, i, vp, f, vp]
+        L.oracle_sign_aligned_decay.argtypes = [vp, vp, vp, vp, i, l, f, vp]
         L.oracle_num_threads.restype = i
         L.oracle_set_num_threads.argtypes = [i]
         _lib = L
@@ -188,3 +190,36 @@ def bank_step(grad, velocity, momentum, fast_beta, fast_weight, slow_beta, maps=
     if rc != 0:
         raise MemoryError("oracle_bank_step")
     return out, vel
+
+
+def rail_equalizer(v_bits, lane_energy, beta2):
+    """The equaliser on a bank of bf16 updates v [g, rows, cols]: returns (v_eq bits,
+    new lane_energy).  lane_energy: fp32 [g, rows] if rows >= cols else [g, cols]."""
+    v_bits = np.ascontiguousarray(v_bits, np.uint16)
+    g, rows, cols = v_bits.shape
+    le = np.array(lane_energy, np.float32, copy=True, order="C")
+    assert le.shape == (g, rows if rows >= cols else cols)
+    out = np.empty_like(v_bits)
+    lib().oracle_rail_equalizer(_ptr(v_bits), g, rows, cols, _ptr(le), beta2, _ptr(out))
+    return out, le
+
+
+def sign_aligned_decay(p_bits, mantissa, update_bits, gate, wd, lr):
+    """Decay + update of the fp32 master weight (bf16 bits p, uint16 mantissa), per matrix
+    learning rates lr [g]; gate fp32 (the slow rail).  Returns (new p bits, new mantissa)."""
+    p = np.array(p_bits, np.uint16, copy=True, order="C")
+    mt = np.array(mantissa, np.uint16, copy=True, order="C")
+    u = np.ascontiguousarray(update_bits, np.uint16)
+    gt = np.ascontiguousarray(gate, np.float32)
+    lr = np.ascontiguousarray(lr, np.float32)
+    g = p.shape[0]
+    assert lr.shape == (g,) and p.shape == mt.shape == u.shape == gt.shape
+    lib().oracle_sign_aligned_decay(_ptr(p), _ptr(mt), _ptr(u), _ptr(gt), g, p[0].size, wd, _ptr(lr))
+    return p, mt
+
+
+def update_tail(v_bits, lane_energy, beta2, p_bits, mantissa, gate, wd, lr):
+    """The page's tail of anvil_bank_update: equaliser, then sign-aligned decay update."""
+    v_eq, le = rail_equalizer(v_bits, lane_energy, beta2)
+    p, mt = sign_aligned_decay(p_bits, mantissa, v_eq, gate, wd, lr)
+    return p, mt, le, v_eq

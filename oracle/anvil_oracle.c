@@ -302,6 +302,94 @@ EXPORT int oracle_bank_step(const float* grad, float* velocity, int g, int rows,
     return rc;
 }
 
+/* ---- the update tail: anvil.py, `_rail_equalizer` and `_sign_aligned_decay_update` ----
+ *
+ * Equaliser, per matrix of a bank [g, rows, cols] of bf16 updates v (the cascade output):
+ * lanes run along the longer dimension (rows when rows >= cols, else columns) and each
+ * lane is reduced over the other one, of length lane_len:
+ *   lane_power[l] = mean over the lane of float(v)^2
+ *   pre_norm      = sqrt(sum_l lane_power[l] * lane_len)          (= ||v||_F)
+ *   lane_energy   <- lerp(lane_energy, lane_power, 1 - beta2)      (fp32 state)
+ *   gain[l]       = rsqrt(max(lane_energy[l], 1e-10))
+ *   post_power[l] = (lane_power[l] * lane_len) * gain[l]^2
+ *   post_norm     = sqrt(sum_l post_power[l])
+ *   scale[l]      = gain[l] * (pre_norm / max(post_norm, 1e-10))
+ *   v_eq          = bf16(float(v) * float(bf16(scale[lane])))      (scale cast to v's dtype)
+ * Sums run sequentially in fp32; mean = sum / lane_len; rsqrt is the correctly rounded
+ * 1/sqrt; one rounding per operation as elsewhere. */
+static inline float rsqrt_rn(float x) { return (float)(1.0 / sqrt((double)x)); }
+
+EXPORT void oracle_rail_equalizer(const uint16_t* v, int g, int rows, int cols, float* lane_energy,
+                                  float beta2, uint16_t* v_eq) {
+    const int lanes_are_rows = rows >= cols;
+    const int nl = lanes_are_rows ? rows : cols;
+    const int lane_len = lanes_are_rows ? cols : rows;
+    const float w = 1.0f - beta2;
+    float* power = malloc((size_t)nl * sizeof(float));
+    float* scale = malloc((size_t)nl * sizeof(float));
+    for (int mtx = 0; mtx < g; ++mtx) {
+        const uint16_t* V = v + (size_t)mtx * rows * cols;
+        uint16_t* E = v_eq + (size_t)mtx * rows * cols;
+        float* le = lane_energy + (size_t)mtx * nl;
+        for (int l = 0; l < nl; ++l) {
+            float s = 0.0f;
+            for (int k = 0; k < lane_len; ++k) {
+                const float x = bf16_to_f32(lanes_are_rows ? V[(size_t)l * cols + k] : V[(size_t)k * cols + l]);
+                s += x * x;
+            }
+            power[l] = s / (float)lane_len;
+        }
+        float psum = 0.0f;
+        for (int l = 0; l < nl; ++l) psum += power[l];
+        const float pre_norm = sqrtf(psum * (float)lane_len);
+        float qsum = 0.0f;
+        for (int l = 0; l < nl; ++l) {
+            le[l] = lerp32(le[l], power[l], w);
+            const float gain = rsqrt_rn(le[l] > 1e-10f ? le[l] : 1e-10f);
+            const float post = (power[l] * (float)lane_len) * (gain * gain);
+            qsum += post;
+            scale[l] = gain;
+        }
+        float post_norm = sqrtf(qsum);
+        if (post_norm < 1e-10f) post_norm = 1e-10f;
+        const float ratio = pre_norm / post_norm;
+        for (int l = 0; l < nl; ++l) scale[l] = round_bf16(scale[l] * ratio);
+        for (int i = 0; i < rows; ++i)
+            for (int j = 0; j < cols; ++j) {
+                const size_t e = (size_t)i * cols + j;
+                E[e] = f32_to_bf16(bf16_to_f32(V[e]) * scale[lanes_are_rows ? i : j]);
+            }
+    }
+    free(power);
+    free(scale);
+}
+
+/* Sign-aligned decay + parameter update on the fp32 master weight held as bf16 bits p
+ * (high half) and mantissa (low half), elementwise over g matrices of `count` elements:
+ *   w       = float(p << 16 | mantissa)
+ *   aligned = float(gate) * w >= 0          (gate: the slow rail)
+ *   w       = (w - ((w * aligned) * wd) * lr[mtx]) - update * lr[mtx]
+ *   p, mantissa = high and low 16 bits of w (a bit split, no rounding) */
+EXPORT void oracle_sign_aligned_decay(uint16_t* p, uint16_t* mantissa, const uint16_t* update,
+                                      const float* gate, int g, long count, float wd,
+                                      const float* lr) {
+    for (int mtx = 0; mtx < g; ++mtx) {
+        const float lrm = lr[mtx];
+        for (long k = 0; k < count; ++k) {
+            const size_t e = (size_t)mtx * count + k;
+            uint32_t bits = ((uint32_t)p[e] << 16) | mantissa[e];
+            float w;
+            memcpy(&w, &bits, 4);
+            const float aligned = (gate[e] * w >= 0.0f) ? 1.0f : 0.0f;
+            const float u = bf16_to_f32(update[e]);
+            w = (w - ((w * aligned) * wd) * lrm) - u * lrm;
+            memcpy(&bits, &w, 4);
+            p[e] = (uint16_t)(bits >> 16);
+            mantissa[e] = (uint16_t)(bits & 0xFFFFu);
+        }
+    }
+}
+
 EXPORT int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

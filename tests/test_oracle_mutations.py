@@ -26,6 +26,12 @@ MUTATIONS = {
     "first_gram_recomputed": ("if (k > 0) gram_bf16(Xf, rows, cols, is_tall, T, Af, A);",
                               "gram_bf16(Xf, rows, cols, is_tall, T, Af, A);"),
     "no_bf16_round_of_B": ("to_bf16(Bf, B, nA);\n        to_f32(B, Bf, nA);", "to_bf16(Bf, B, nA);"),
+    "ema_weight_beta2": ("const float w = 1.0f - beta2;", "const float w = beta2;"),
+    "lanes_wrong_dim": ("const int lanes_are_rows = rows >= cols;", "const int lanes_are_rows = rows < cols;"),
+    "gate_sign_reversed": ("const float aligned = (gate[e] * w >= 0.0f) ? 1.0f : 0.0f;",
+                           "const float aligned = (gate[e] * w <= 0.0f) ? 1.0f : 0.0f;"),
+    "decay_without_lr": ("w = (w - ((w * aligned) * wd) * lrm) - u * lrm;", "w = (w - (w * aligned) * wd) - u * lrm;"),
+    "no_norm_restore": ("const float ratio = pre_norm / post_norm;", "const float ratio = 1.0f;"),
 }
 
 
@@ -39,6 +45,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     src.write_text(text.replace(old, new))
     env = dict(os.environ, ANVIL_ORACLE_SRC=str(src), ANVIL_ORACLE_BUILD=str(tmp_path / "b"))
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_tail.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutation {name} survived:\n{r.stdout[-2000:]}"

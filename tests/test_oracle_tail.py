@@ -1,0 +1,117 @@
+"""Pins of the oracle's update tail (the page's `_rail_equalizer` and
+`_sign_aligned_decay_update` in anvil.py) against closed forms and invariants."""
+import numpy as np
+import pytest
+
+import oracle
+
+U32 = 2.0 ** -24
+
+
+def f64(b):
+    return oracle.bf16_to_f32(b).astype(np.float64)
+
+
+def lanes(x, rows_ge_cols):
+    """Mean square per lane: lanes along the longer dimension (rows when rows >= cols)."""
+    return (x ** 2).mean(axis=2) if rows_ge_cols else (x ** 2).mean(axis=1)
+
+
+def graded(shape, seed):
+    """bf16 updates whose lanes have very different energies."""
+    g, m, n = shape
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(shape)
+    if m >= n:
+        x *= np.geomspace(0.01, 10, m)[None, :, None]
+    else:
+        x *= np.geomspace(0.01, 10, n)[None, None, :]
+    return oracle.f32_to_bf16(x.astype(np.float32))
+
+
+@pytest.mark.parametrize("shape", [(2, 48, 16), (2, 16, 48), (1, 32, 32), (3, 7, 5)])
+def test_equalizer_from_zero_state_equalises_lanes_and_keeps_the_norm(shape):
+    """From zero lane energy: gain_l = 1/sqrt((1-b2) P_l), every lane's post power is the
+    same, so each lane leaves with the mean lane power and ||v||_F is preserved."""
+    g, m, n = shape
+    v = graded(shape, sum(shape))
+    le0 = np.zeros((g, m if m >= n else n), np.float32)
+    veq, le = oracle.rail_equalizer(v, le0, 0.95)
+    P = lanes(f64(v), m >= n)
+    Q = lanes(f64(veq), m >= n)
+    for i in range(g):
+        assert np.allclose(Q[i], P[i].mean(), rtol=2e-2)
+        assert abs(np.linalg.norm(f64(veq[i])) / np.linalg.norm(f64(v[i])) - 1) < 1e-2
+    np.testing.assert_allclose(le, 0.05 * P, rtol=1e-5)
+
+
+def test_lane_energy_is_an_ema_over_steps():
+    """The same update k times from zero: lane_energy_k = (1 - b2^k) P."""
+    shape = (2, 24, 40)
+    v = graded(shape, 3)
+    le = np.zeros((2, 40), np.float32)
+    P = lanes(f64(v), False)
+    b2 = np.float32(0.9)
+    for k in range(1, 8):
+        _, le = oracle.rail_equalizer(v, le, 0.9)
+        np.testing.assert_allclose(le, (1 - np.float64(b2) ** k) * P, rtol=1e-5)
+
+
+def test_equalizer_zero_lane_stays_zero_and_finite():
+    v = graded((1, 16, 8), 4)
+    v[0, 3, :] = 0
+    veq, le = oracle.rail_equalizer(v, np.zeros((1, 16), np.float32), 0.95)
+    assert np.isfinite(f64(veq)).all() and not veq[0, 3].any()
+
+
+def test_equalizer_with_equal_lanes_and_steady_state_is_identity_scale():
+    """Lanes already equal, lane_energy at its fixed point: the scale is 1."""
+    v = oracle.f32_to_bf16(np.ones((1, 12, 6), np.float32) * 0.5)
+    le = np.full((1, 12), 0.25, np.float32)
+    veq, le2 = oracle.rail_equalizer(v, le, 0.95)
+    np.testing.assert_array_equal(veq, v)
+    np.testing.assert_array_equal(le2, le)
+
+
+def _master(p, mt):
+    return ((p.astype(np.uint32) << 16) | mt.astype(np.uint32)).view(np.float32).astype(np.float64)
+
+
+def test_decay_matches_fp64_and_gates_on_the_slow_rail_sign():
+    rng = np.random.default_rng(6)
+    shape = (3, 20, 30)
+    w = (rng.standard_normal(shape) * 0.05).astype(np.float32)
+    bits = w.view(np.uint32)
+    p, mt = (bits >> 16).astype(np.uint16), (bits & 0xFFFF).astype(np.uint16)
+    u = oracle.f32_to_bf16(rng.standard_normal(shape).astype(np.float32))
+    gate = rng.standard_normal(shape).astype(np.float32) * 0.01
+    lr = np.array([0.02, 0.0, 0.05], np.float32)
+    wd = np.float32(0.1)
+    p2, mt2 = oracle.sign_aligned_decay(p, mt, u, gate, float(wd), lr)
+    W = _master(p, mt)
+    aligned = (gate.astype(np.float64) * W) >= 0
+    want = W - W * aligned * float(wd) * lr.astype(np.float64)[:, None, None] \
+        - f64(u) * lr.astype(np.float64)[:, None, None]
+    got = _master(p2, mt2)
+    scale = np.abs(W) + np.abs(f64(u)) * np.abs(lr.astype(np.float64))[:, None, None]
+    assert np.all(np.abs(got - want) <= 4 * U32 * scale + 1e-45)
+    # lr = 0: the master weight is untouched, bit for bit
+    np.testing.assert_array_equal(p2[1], p[1])
+    np.testing.assert_array_equal(mt2[1], mt[1])
+    # decay applies only where gate and weight agree in sign: flip the gate, the decay
+    # term moves to the complementary elements
+    p3, mt3 = oracle.sign_aligned_decay(p, mt, np.zeros_like(u), -gate, float(wd), lr)
+    d3 = _master(p3, mt3) - W
+    hit = d3[0] != 0
+    assert np.array_equal(hit, ~aligned[0] & (W[0] != 0))
+
+
+def test_decay_bit_split_round_trips():
+    rng = np.random.default_rng(7)
+    w = rng.standard_normal((1, 64)).astype(np.float32)
+    bits = w.view(np.uint32)
+    p, mt = (bits >> 16).astype(np.uint16), (bits & 0xFFFF).astype(np.uint16)
+    p2, mt2 = oracle.sign_aligned_decay(p, mt, np.zeros((1, 64), np.uint16),
+                                        np.ones((1, 64), np.float32), 0.0, np.zeros(1, np.float32))
+    np.testing.assert_array_equal(p2, p)
+    np.testing.assert_array_equal(mt2, mt)
