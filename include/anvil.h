@@ -144,6 +144,45 @@ anvil_status anvil_bank_step_noalloc(const float* grad, float* velocity, int g, 
                                      float slow_beta, const anvil_map* maps, int nmaps,
                                      float margin, float eps, uint16_t* out, void* stream);
 
+/* ---- the update tail: anvil_bank_update's steps after the cascade on the page
+ * (`_rail_equalizer`, then `_sign_aligned_decay_update`).  For every matrix, with the
+ * bank step's output as the update v and lanes along the longer dimension (the rows
+ * when m >= n, else the columns), each lane reduced over the other dimension:
+ *   P[l] = mean over lane l of v^2;  lane_energy <- lerp(lane_energy, P, 1 - beta2)
+ *   gain = rsqrt(max(lane_energy, 1e-10));  scale[l] = gain[l] * (||v||_F / post_norm),
+ *   post_norm^2 = sum_l P[l] * lane_len * gain[l]^2   (post_norm clamped at 1e-10)
+ *   u = bf16(v * bf16(scale[lane]))
+ *   w = fp32 master weight (param bits << 16 | mantissa)
+ *   w <- (w - w * [slow rail * w >= 0] * eff_wd * eff_lr[mat]) - u * eff_lr[mat]
+ *   param, mantissa <- high and low 16 bits of w.
+ * DEVICE pointers, row-major, caller-owned:
+ *   update      [g, m, n] bf16 bits, read (the out of anvil_bank_step)
+ *   velocity    [2, g, m, n] fp32, read (rail 1, the slow rail, gates the decay)
+ *   lane_energy [g, m] fp32 if m >= n, else [g, n]; read and written
+ *   param       [g, m, n] bf16 bits of the parameter; read and written
+ *   mantissa    [g, m, n] uint16, the low half of the fp32 master weight; read and written
+ *   eff_lr      [g] fp32 per-matrix learning rate, read when the kernels run
+ * Written buffers must not overlap any other buffer of the call. */
+typedef struct {
+    const uint16_t* update;
+    const float* velocity;
+    float* lane_energy;
+    uint16_t* param;
+    uint16_t* mantissa;
+    const float* eff_lr;
+    int g, m, n;
+    float eff_wd, beta2;
+} anvil_tail_desc;
+
+/* Bytes of device workspace anvil_update_tail needs (0 if the descriptors are invalid). */
+size_t anvil_tail_workspace_bytes(const anvil_tail_desc* banks, int nbanks);
+
+/* The update tail over nbanks banks (1 <= nbanks <= ANVIL_MAX_BANKS), three grouped
+ * launches on the stream; workspace as for anvil_multi_bank_step (256-byte aligned,
+ * caller-owned, contents on entry irrelevant).  Allocates nothing, never synchronises. */
+anvil_status anvil_update_tail(const anvil_tail_desc* banks, int nbanks, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 /* Per-stage dumps of one bank step, for parity testing (not the hot path).
  * DEVICE pointers, each optional (NULL = skip), in the page's layout:
  *   X_raw [g, m, n] bf16            bf16 cast of the momentum lookahead
@@ -178,8 +217,8 @@ anvil_status anvil_device_error(int clear);
 anvil_status anvil_selftest_wait_timeout(unsigned timeout_us, void* stream);
 
 /* Per-launch timing for benchmarks.  Between anvil_profile_begin and
- * anvil_profile_end, every kernel launch of anvil_multi_bank_step /
- * anvil_bank_step on the calling process is bracketed by two CUDA events
+ * anvil_profile_end, every kernel launch of anvil_multi_bank_step,
+ * anvil_bank_step and anvil_update_tail in the process is bracketed by two CUDA events
  * recorded on the call's stream (at most max_records launches; later ones are
  * not timed).  begin creates the events (a host call: do not begin, or step
  * with profiling on, while a stream is capturing).  end synchronises, writes up
@@ -193,7 +232,10 @@ typedef enum {
     ANVIL_KERNEL_GRAM = 4,         /* A = bf16(X X^T) */
     ANVIL_KERNEL_SQPOLY = 5,       /* B = bf16(b A + c A A) */
     ANVIL_KERNEL_XUPDATE = 6,      /* X <- bf16(a X + B X) */
-    ANVIL_KERNEL_XUPDATE_OUT = 7   /* the last map's X-update, written to out */
+    ANVIL_KERNEL_XUPDATE_OUT = 7,  /* the last map's X-update, written to out */
+    ANVIL_KERNEL_TAIL_POWER = 8,   /* update tail: lane powers */
+    ANVIL_KERNEL_TAIL_SCALE = 9,   /* update tail: lane energies and scales */
+    ANVIL_KERNEL_TAIL_APPLY = 10   /* update tail: equalise + sign-aligned decay update */
 } anvil_kernel_kind;
 
 typedef struct { int kind; float ms; } anvil_profile_record;

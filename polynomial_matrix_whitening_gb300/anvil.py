@@ -31,7 +31,7 @@ STATUS = {0: "ANVIL_OK", 1: "ANVIL_ERR_INVALID_ARG", 2: "ANVIL_ERR_UNSUPPORTED_S
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_ALIGNMENT, ERR_ALIAS, ERR_WORKSPACE, \
     ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(9)
 KERNEL_KINDS = ("momentum", "norm_d", "normalize", "gram_norm", "gram", "sqpoly", "xupdate",
-                "xupdate_out")
+                "xupdate_out", "tail_power", "tail_scale", "tail_apply")
 MAX_MAPS, MAX_BANKS = 16, 8
 
 
@@ -62,6 +62,14 @@ class Trace(ctypes.Structure):
                 ("A", ctypes.c_void_p), ("B", ctypes.c_void_p)]
 
 
+class TailDesc(ctypes.Structure):
+    _fields_ = [("update", ctypes.c_void_p), ("velocity", ctypes.c_void_p),
+                ("lane_energy", ctypes.c_void_p), ("param", ctypes.c_void_p),
+                ("mantissa", ctypes.c_void_p), ("eff_lr", ctypes.c_void_p),
+                ("g", ctypes.c_int), ("m", ctypes.c_int), ("n", ctypes.c_int),
+                ("eff_wd", ctypes.c_float), ("beta2", ctypes.c_float)]
+
+
 class ProfileRecord(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("ms", ctypes.c_float)]
 
@@ -82,6 +90,10 @@ _lib.anvil_bank_step_noalloc.restype = _i
 _lib.anvil_bank_step_traced.argtypes = [ctypes.POINTER(BankDesc), _vp, ctypes.POINTER(Map), _i,
                                         _f, _f, _vp, _sz, ctypes.POINTER(Trace), _vp]
 _lib.anvil_bank_step_traced.restype = _i
+_lib.anvil_tail_workspace_bytes.argtypes = [ctypes.POINTER(TailDesc), _i]
+_lib.anvil_tail_workspace_bytes.restype = _sz
+_lib.anvil_update_tail.argtypes = [ctypes.POINTER(TailDesc), _i, _vp, _sz, _vp]
+_lib.anvil_update_tail.restype = _i
 _lib.anvil_device_error.argtypes = [_i]
 _lib.anvil_device_error.restype = _i
 _lib.anvil_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
@@ -254,6 +266,45 @@ def bank_step_traced(bank: Bank, workspace, maps=None, margin=1.05, eps=1e-6, st
                                      _stream_arg(stream))
     _check(st, "anvil_bank_step_traced")
     return t
+
+
+class Tail:
+    """One bank of the update tail: the step's out as update, its velocity (rail 1 gates the
+    decay), lane_energy [g, m] if m >= n else [g, n] fp32, param (bf16) and mantissa
+    (uint16 as torch.int16) [g, m, n], eff_lr [g] fp32, and host eff_wd, beta2."""
+
+    def __init__(self, update, velocity, lane_energy, param, mantissa, eff_lr, eff_wd, beta2):
+        self.update, self.velocity, self.lane_energy = update, velocity, lane_energy
+        self.param, self.mantissa, self.eff_lr = param, mantissa, eff_lr
+        self.eff_wd, self.beta2 = float(eff_wd), float(beta2)
+
+    def desc(self):
+        import torch
+        g, m, n = self.update.shape
+        assert self.update.dtype == torch.bfloat16 and self.param.dtype == torch.bfloat16
+        assert self.mantissa.dtype in (torch.int16, torch.uint16) and self.mantissa.shape == (g, m, n)
+        assert self.velocity.shape == (2, g, m, n) and self.velocity.dtype == torch.float32
+        assert self.lane_energy.shape == (g, m if m >= n else n) and self.lane_energy.dtype == torch.float32
+        assert self.eff_lr.shape == (g,) and self.eff_lr.dtype == torch.float32
+        for t in (self.update, self.velocity, self.lane_energy, self.param, self.mantissa, self.eff_lr):
+            assert t.is_cuda and t.is_contiguous()
+        return TailDesc(self.update.data_ptr(), self.velocity.data_ptr(), self.lane_energy.data_ptr(),
+                        self.param.data_ptr(), self.mantissa.data_ptr(), self.eff_lr.data_ptr(),
+                        g, m, n, self.eff_wd, self.beta2)
+
+
+def tail_workspace_bytes(shapes):
+    descs = (TailDesc * len(shapes))(*[TailDesc(0, 0, 0, 0, 0, 0, g, m, n, 0.0, 0.0)
+                                       for g, m, n in shapes])
+    return int(_lib.anvil_tail_workspace_bytes(descs, len(shapes)))
+
+
+def update_tail(tails, workspace, stream=None):
+    """The page's update tail (equaliser + sign-aligned decay) over several banks."""
+    descs = (TailDesc * len(tails))(*[t.desc() for t in tails])
+    st = _lib.anvil_update_tail(descs, len(tails), workspace.data_ptr(),
+                                workspace.numel() * workspace.element_size(), _stream_arg(stream))
+    _check(st, "anvil_update_tail")
 
 
 def device_error(clear=True):

@@ -23,6 +23,7 @@
 
 #include "../../include/anvil.h"
 #include "anvil_internal.h"
+#include "anvil_tail.h"
 
 using namespace anvil;
 
@@ -524,6 +525,63 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
     return ANVIL_OK;
 }
 
+// ---------------------------------------------------------------- update tail
+struct TailLayout {
+    int total_mats;
+    size_t lanes_total;  // sum over banks of g * nl
+    size_t off_power, off_scale, total;
+    size_t lane_off[ANVIL_MAX_BANKS];
+};
+
+anvil_status make_tail_layout(const anvil_tail_desc* banks, int nbanks, TailLayout* T) {
+    if (!banks || nbanks < 1 || nbanks > ANVIL_MAX_BANKS) return ANVIL_ERR_INVALID_ARG;
+    T->total_mats = 0;
+    T->lanes_total = 0;
+    for (int i = 0; i < nbanks; ++i) {
+        const anvil_tail_desc& b = banks[i];
+        if (b.g < 1 || b.m < 1 || b.n < 1) return ANVIL_ERR_INVALID_ARG;
+        if (b.m > ANVIL_MAX_DIM || b.n > ANVIL_MAX_DIM || b.g > ANVIL_MAX_BATCH)
+            return ANVIL_ERR_UNSUPPORTED_SHAPE;
+        T->lane_off[i] = T->lanes_total;
+        T->lanes_total += static_cast<size_t>(b.g) * (b.m >= b.n ? b.m : b.n);
+        T->total_mats += b.g;
+    }
+    T->off_power = 0;
+    T->off_scale = align256(sizeof(float) * T->lanes_total);
+    T->total = align256(T->off_scale + sizeof(float) * T->lanes_total);
+    return ANVIL_OK;
+}
+
+anvil_status check_tail(const anvil_tail_desc* banks, int nbanks) {
+    Range rg[ANVIL_MAX_BANKS][6];
+    for (int i = 0; i < nbanks; ++i) {
+        const anvil_tail_desc& b = banks[i];
+        if (!b.update || !b.velocity || !b.lane_energy || !b.param || !b.mantissa || !b.eff_lr)
+            return ANVIL_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(b.update) & 1) || (reinterpret_cast<uintptr_t>(b.param) & 1) ||
+            (reinterpret_cast<uintptr_t>(b.mantissa) & 1) || (reinterpret_cast<uintptr_t>(b.velocity) & 3) ||
+            (reinterpret_cast<uintptr_t>(b.lane_energy) & 3) || (reinterpret_cast<uintptr_t>(b.eff_lr) & 3))
+            return ANVIL_ERR_ALIGNMENT;
+        const size_t cnt = static_cast<size_t>(b.g) * b.m * b.n;
+        const size_t nl = static_cast<size_t>(b.g) * (b.m >= b.n ? b.m : b.n);
+        rg[i][0] = {reinterpret_cast<uintptr_t>(b.lane_energy), reinterpret_cast<uintptr_t>(b.lane_energy + nl)};
+        rg[i][1] = {reinterpret_cast<uintptr_t>(b.param), reinterpret_cast<uintptr_t>(b.param + cnt)};
+        rg[i][2] = {reinterpret_cast<uintptr_t>(b.mantissa), reinterpret_cast<uintptr_t>(b.mantissa + cnt)};
+        rg[i][3] = {reinterpret_cast<uintptr_t>(b.update), reinterpret_cast<uintptr_t>(b.update + cnt)};
+        rg[i][4] = {reinterpret_cast<uintptr_t>(b.velocity), reinterpret_cast<uintptr_t>(b.velocity + 2 * cnt)};
+        rg[i][5] = {reinterpret_cast<uintptr_t>(b.eff_lr), reinterpret_cast<uintptr_t>(b.eff_lr + b.g)};
+    }
+    // written buffers (lane_energy, param, mantissa) overlap nothing else of the call
+    for (int i = 0; i < nbanks; ++i)
+        for (int w = 0; w < 3; ++w)
+            for (int j = 0; j < nbanks; ++j)
+                for (int k = 0; k < 6; ++k) {
+                    if (i == j && k == w) continue;
+                    if (overlap(rg[i][w], rg[j][k])) return ANVIL_ERR_ALIAS;
+                }
+    return ANVIL_OK;
+}
+
 // ---------------------------------------------------------------- library-owned workspace
 struct OwnedWorkspace {
     void* ptr = nullptr;
@@ -564,6 +622,65 @@ anvil_status anvil_multi_bank_step(const anvil_bank_desc* banks, int nbanks,
                                    size_t workspace_bytes, void* stream) {
     return run_step(banks, nbanks, d_scalars, maps, nmaps, margin, eps, workspace,
                     workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+size_t anvil_tail_workspace_bytes(const anvil_tail_desc* banks, int nbanks) {
+    TailLayout T;
+    if (make_tail_layout(banks, nbanks, &T) != ANVIL_OK) return 0;
+    return T.total;
+}
+
+anvil_status anvil_update_tail(const anvil_tail_desc* banks, int nbanks, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+    anvil_status st;
+    TailLayout T;
+    if ((st = make_tail_layout(banks, nbanks, &T)) != ANVIL_OK) return st;
+    if ((st = check_tail(banks, nbanks)) != ANVIL_OK) return st;
+    if (!workspace || workspace_bytes < T.total) return ANVIL_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return ANVIL_ERR_ALIGNMENT;
+    DeviceState* dev = nullptr;
+    if ((st = device_setup(&dev)) != ANVIL_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    TailParams tp;
+    memset(&tp, 0, sizeof(tp));
+    tp.nbanks = nbanks;
+    tp.total_mats = T.total_mats;
+    long long chunks = 0;
+    int mats = 0;
+    for (int i = 0; i < nbanks; ++i) {
+        const anvil_tail_desc& b = banks[i];
+        TailBank& B = tp.bank[i];
+        B.update = b.update;
+        B.velocity = b.velocity;
+        B.lane_energy = b.lane_energy;
+        B.param = b.param;
+        B.mantissa = b.mantissa;
+        B.eff_lr = b.eff_lr;
+        B.eff_wd = b.eff_wd;
+        B.beta2 = b.beta2;
+        B.g = b.g;
+        B.m = b.m;
+        B.n = b.n;
+        B.mat_begin = mats;
+        B.chunk_begin = chunks;
+        B.vec8 = (b.n % 8 == 0) && !(reinterpret_cast<uintptr_t>(b.update) & 15) &&
+                 !(reinterpret_cast<uintptr_t>(b.param) & 15) && !(reinterpret_cast<uintptr_t>(b.mantissa) & 15) &&
+                 !(reinterpret_cast<uintptr_t>(b.velocity) & 15);
+        B.power = reinterpret_cast<float*>(ws + T.off_power) + T.lane_off[i];
+        B.scale = reinterpret_cast<float*>(ws + T.off_scale) + T.lane_off[i];
+        mats += b.g;
+        chunks += static_cast<long long>(b.g) * b.m * ((b.n + 7) / 8);
+    }
+    tp.total_chunks = chunks;
+    cudaError_t e;
+    if ((e = profiled(ANVIL_KERNEL_TAIL_POWER, s, [&] { return launch_tail_power(tp, s); })))
+        return cuda_fail(e, "tail lane-power launch");
+    if ((e = profiled(ANVIL_KERNEL_TAIL_SCALE, s, [&] { return launch_tail_scale(tp, s); })))
+        return cuda_fail(e, "tail lane-scale launch");
+    if ((e = profiled(ANVIL_KERNEL_TAIL_APPLY, s, [&] { return launch_tail_apply(tp, s); })))
+        return cuda_fail(e, "tail apply launch");
+    return ANVIL_OK;
 }
 
 anvil_status anvil_bank_step_traced(const anvil_bank_desc* bank, const anvil_scalars* d_scalars,

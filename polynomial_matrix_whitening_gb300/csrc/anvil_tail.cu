@@ -1,0 +1,211 @@
+// anvil_tail.cu -- the update tail after the cascade (page "modded-nanogpt
+// track_1_short/optim/anvil.py", `anvil_bank_update` steps 2 and 3: `_rail_equalizer` and
+// `_sign_aligned_decay_update`), three HBM-bound kernels grouped over banks:
+//
+//   lane_power_kernel : P[l] = mean over lane l of float(v)^2; lanes run along the longer
+//                       dimension (rows when m >= n, else columns)
+//   lane_scale_kernel : one block per matrix: lane_energy <- lerp(lane_energy, P, 1 - beta2),
+//                       gain = rsqrt(max(lane_energy, 1e-10)), norms before and after,
+//                       scale[l] = bf16(gain * (pre_norm / max(post_norm, 1e-10)))
+//   tail_apply_kernel : u = bf16(v * scale[lane]); on the fp32 master weight w (bf16 bits
+//                       p, uint16 mantissa): w <- (w - w [gate w >= 0] wd lr) - u lr, split
+//                       back into p and mantissa (gate: the slow rail)
+//
+// Every rounding follows the page's fp32 tensor operations one at a time (no FMA).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/anvil.h"
+#include "anvil_device.cuh"
+#include "anvil_tail.h"
+
+namespace anvil {
+
+// ---------------------------------------------------------------- lane powers
+// Lanes along rows (m >= n): one warp per (matrix, row), lanes of the warp stride the
+// columns; a fixed shuffle tree adds the 32 partial sums.
+// Lanes along columns (m < n): a block covers 32 columns of one matrix with 8 row
+// slices; slice k sums rows k, k+8, ...; the 8 slice sums are added in order.
+__global__ void __launch_bounds__(256) lane_power_kernel(const __grid_constant__ TailParams p) {
+    const int b = blockIdx.y;
+    const TailBank& B = p.bank[b];
+    const int mn = B.m * B.n;
+    if (B.m >= B.n) {
+        const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+        const int lane = threadIdx.x & 31;
+        if (warp_id >= static_cast<long long>(B.g) * B.m) return;
+        const int mat = static_cast<int>(warp_id / B.m), row = static_cast<int>(warp_id % B.m);
+        const uint16_t* v = B.update + static_cast<size_t>(mat) * mn + static_cast<size_t>(row) * B.n;
+        float s = 0.f;
+        for (int j = lane; j < B.n; j += 32) {
+            const float x = bf2f(v[j]);
+            s = __fadd_rn(s, __fmul_rn(x, x));
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
+        if (lane == 0) B.power[static_cast<size_t>(mat) * B.m + row] = __fdiv_rn(s, static_cast<float>(B.n));
+    } else {
+        __shared__ float part[8][33];
+        const int cblocks = (B.n + 31) / 32;
+        if (blockIdx.x >= static_cast<unsigned>(B.g * cblocks)) return;
+        const int mat = blockIdx.x / cblocks, c0 = (blockIdx.x % cblocks) * 32;
+        const int cx = threadIdx.x & 31, slice = threadIdx.x >> 5;
+        const int col = c0 + cx;
+        const uint16_t* v = B.update + static_cast<size_t>(mat) * mn;
+        float s = 0.f;
+        if (col < B.n)
+            for (int i = slice; i < B.m; i += 8) {
+                const float x = bf2f(v[static_cast<size_t>(i) * B.n + col]);
+                s = __fadd_rn(s, __fmul_rn(x, x));
+            }
+        part[slice][cx] = s;
+        __syncthreads();
+        if (slice == 0 && col < B.n) {
+            float t = part[0][cx];
+            for (int k = 1; k < 8; ++k) t = __fadd_rn(t, part[k][cx]);
+            B.power[static_cast<size_t>(mat) * B.n + col] = __fdiv_rn(t, static_cast<float>(B.m));
+        }
+    }
+}
+
+// ---------------------------------------------------------------- lane scales
+__global__ void __launch_bounds__(256) lane_scale_kernel(const __grid_constant__ TailParams p) {
+    __shared__ float red_p[256], red_q[256];
+    const int gm = blockIdx.x;
+    int bi = 0;
+#pragma unroll 1
+    for (int i = 1; i < p.nbanks; ++i)
+        if (gm >= p.bank[i].mat_begin) bi = i;
+    const TailBank& B = p.bank[bi];
+    const int mat = gm - B.mat_begin;
+    const int nl = B.m >= B.n ? B.m : B.n;
+    const float len = static_cast<float>(B.m >= B.n ? B.n : B.m);
+    const float w = __fsub_rn(1.0f, B.beta2);
+    const float* P = B.power + static_cast<size_t>(mat) * nl;
+    float* E = B.lane_energy + static_cast<size_t>(mat) * nl;
+    float* S = B.scale + static_cast<size_t>(mat) * nl;
+    float sp = 0.f, sq = 0.f;
+    for (int l = threadIdx.x; l < nl; l += blockDim.x) {
+        const float pw = P[l];
+        const float e = __fadd_rn(E[l], __fmul_rn(w, __fsub_rn(pw, E[l])));
+        E[l] = e;
+        const float gain = __frsqrt_rn(e > 1e-10f ? e : 1e-10f);
+        S[l] = gain;
+        sp = __fadd_rn(sp, pw);
+        sq = __fadd_rn(sq, __fmul_rn(__fmul_rn(pw, len), __fmul_rn(gain, gain)));
+    }
+    red_p[threadIdx.x] = sp;
+    red_q[threadIdx.x] = sq;
+    __syncthreads();
+    for (int k = blockDim.x / 2; k > 0; k >>= 1) {
+        if (threadIdx.x < k) {
+            red_p[threadIdx.x] = __fadd_rn(red_p[threadIdx.x], red_p[threadIdx.x + k]);
+            red_q[threadIdx.x] = __fadd_rn(red_q[threadIdx.x], red_q[threadIdx.x + k]);
+        }
+        __syncthreads();
+    }
+    const float pre = __fsqrt_rn(__fmul_rn(red_p[0], len));
+    float post = __fsqrt_rn(red_q[0]);
+    if (post < 1e-10f) post = 1e-10f;
+    const float ratio = __fdiv_rn(pre, post);
+    for (int l = threadIdx.x; l < nl; l += blockDim.x) S[l] = round_bf(__fmul_rn(S[l], ratio));
+}
+
+// ---------------------------------------------------------------- equalise + decay update
+__device__ __forceinline__ void tail_element(float v, float scale, float gate, float wd, float lr,
+                                             uint16_t& p, uint16_t& mt) {
+    const float u = round_bf(__fmul_rn(v, scale));
+    float w = __uint_as_float((static_cast<uint32_t>(p) << 16) | mt);
+    const float aligned = (__fmul_rn(gate, w) >= 0.f) ? 1.f : 0.f;
+    const float decay = __fmul_rn(__fmul_rn(__fmul_rn(w, aligned), wd), lr);
+    w = __fsub_rn(__fsub_rn(w, decay), __fmul_rn(u, lr));
+    const uint32_t bits = __float_as_uint(w);
+    p = static_cast<uint16_t>(bits >> 16);
+    mt = static_cast<uint16_t>(bits & 0xffffu);
+}
+
+// Eight consecutive elements of one row per thread, grid-stride over all banks.
+__global__ void __launch_bounds__(256) tail_apply_kernel(const __grid_constant__ TailParams p) {
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < p.total_chunks;
+         t += stride) {
+        int bi = 0;
+#pragma unroll 1
+        for (int i = 1; i < p.nbanks; ++i)
+            if (t >= p.bank[i].chunk_begin) bi = i;
+        const TailBank& B = p.bank[bi];
+        const long long lt = t - B.chunk_begin;
+        const int cpr = (B.n + 7) / 8;  // chunks per row
+        const long long rowg = lt / cpr;
+        const int c0 = static_cast<int>(lt % cpr) * 8;
+        const int mat = static_cast<int>(rowg / B.m), row = static_cast<int>(rowg % B.m);
+        const size_t mn = static_cast<size_t>(B.m) * B.n;
+        const size_t base = static_cast<size_t>(mat) * mn + static_cast<size_t>(row) * B.n + c0;
+        const float lr = B.eff_lr[mat];
+        const bool rows_lanes = B.m >= B.n;
+        const float* S = B.scale + static_cast<size_t>(mat) * (rows_lanes ? B.m : B.n);
+        const float* gate = B.velocity + static_cast<size_t>(B.g) * mn;  // rail 1
+        if (B.vec8 && c0 + 8 <= B.n) {
+            const uint4 vu = *reinterpret_cast<const uint4*>(B.update + base);
+            uint4 pu = *reinterpret_cast<const uint4*>(B.param + base);
+            uint4 mu = *reinterpret_cast<const uint4*>(B.mantissa + base);
+            const float4 g0 = __ldcs(reinterpret_cast<const float4*>(gate + base));
+            const float4 g1 = __ldcs(reinterpret_cast<const float4*>(gate + base + 4));
+            const uint32_t vw[4] = {vu.x, vu.y, vu.z, vu.w};
+            uint32_t pw[4] = {pu.x, pu.y, pu.z, pu.w};
+            uint32_t mw[4] = {mu.x, mu.y, mu.z, mu.w};
+            const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int q = k >> 1, hi = k & 1;
+                const float v = bf2f(static_cast<uint16_t>(hi ? vw[q] >> 16 : vw[q] & 0xffffu));
+                uint16_t pp = static_cast<uint16_t>(hi ? pw[q] >> 16 : pw[q] & 0xffffu);
+                uint16_t mm = static_cast<uint16_t>(hi ? mw[q] >> 16 : mw[q] & 0xffffu);
+                tail_element(v, rows_lanes ? S[row] : S[c0 + k], gv[k], B.eff_wd, lr, pp, mm);
+                pw[q] = hi ? ((pw[q] & 0xffffu) | (static_cast<uint32_t>(pp) << 16))
+                           : ((pw[q] & 0xffff0000u) | pp);
+                mw[q] = hi ? ((mw[q] & 0xffffu) | (static_cast<uint32_t>(mm) << 16))
+                           : ((mw[q] & 0xffff0000u) | mm);
+            }
+            *reinterpret_cast<uint4*>(B.param + base) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+            *reinterpret_cast<uint4*>(B.mantissa + base) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+        } else {
+            for (int k = 0; k < 8 && c0 + k < B.n; ++k) {
+                uint16_t pp = B.param[base + k], mm = B.mantissa[base + k];
+                tail_element(bf2f(B.update[base + k]), rows_lanes ? S[row] : S[c0 + k], gate[base + k],
+                             B.eff_wd, lr, pp, mm);
+                B.param[base + k] = pp;
+                B.mantissa[base + k] = mm;
+            }
+        }
+    }
+}
+
+cudaError_t launch_tail_power(const TailParams& p, cudaStream_t stream) {
+    // grid.x covers the largest bank, grid.y the banks
+    unsigned gx = 1;
+    for (int i = 0; i < p.nbanks; ++i) {
+        const TailBank& B = p.bank[i];
+        const unsigned need = B.m >= B.n
+                                  ? static_cast<unsigned>((static_cast<long long>(B.g) * B.m * 32 + 255) / 256)
+                                  : static_cast<unsigned>(B.g * ((B.n + 31) / 32));
+        if (need > gx) gx = need;
+    }
+    lane_power_kernel<<<dim3(gx, p.nbanks), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tail_scale(const TailParams& p, cudaStream_t stream) {
+    lane_scale_kernel<<<p.total_mats, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tail_apply(const TailParams& p, cudaStream_t stream) {
+    long long blocks = (p.total_chunks + 255) / 256;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (blocks < 1) blocks = 1;
+    tail_apply_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace anvil
