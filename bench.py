@@ -376,6 +376,46 @@ def run_anvil(args, world, rank, local):
                   if k in ("gram", "gram_norm", "sqpoly", "xupdate", "xupdate_out")) / prof_steps
     mom_ms = per_kind.get("momentum", [1, 0.0])[1] / prof_steps
 
+    # ---- the page's update tail after the step (equaliser + sign-aligned decay update
+    # on a bf16 + mantissa master weight), timed alone on graph replays
+    tails, tail_ws = [], None
+    gen = torch.Generator(device=dev).manual_seed(5)
+    for b in banks:
+        g_, m_, n_ = b.shape
+        nl = m_ if m_ >= n_ else n_
+        w0 = torch.randn((g_, m_, n_), device=dev, generator=gen) * 0.05
+        bits = w0.view(torch.int32)
+        tails.append(anvil.Tail(b.out, b.velocity,
+                                torch.zeros((g_, nl), dtype=torch.float32, device=dev),
+                                (bits >> 16).to(torch.int16).view(torch.bfloat16).contiguous(),
+                                (bits & 0xFFFF).to(torch.int16).contiguous(),
+                                torch.full((g_,), 0.02, dtype=torch.float32, device=dev), 0.1, 0.95))
+    tail_ws = torch.empty(anvil.tail_workspace_bytes([b.shape for b in banks]), dtype=torch.uint8,
+                          device=dev)
+    with torch.cuda.stream(stream):
+        anvil.update_tail(tails, tail_ws, stream=stream)
+        g_tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_tail, stream=stream):
+            anvil.update_tail(tails, tail_ws, stream=stream)
+        for _ in range(nwarm):
+            g_tail.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    tail_reps = max(nsteps, 20)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(tail_reps):
+            g_tail.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    tail_ms = t0.elapsed_time(t1) / tail_reps
+    tail_bytes = sum(b.shape[0] * b.shape[1] * b.shape[2] for b in banks) * 16.0
+    update_tail = {"ms_per_step": tail_ms, "achieved": tail_bytes / (tail_ms / 1000.0) / 1e9,
+                   "unit": "GB/s", "frac": tail_bytes / (tail_ms / 1000.0) / 1e9 / peaks["hbm_gbs"],
+                   "bytes_per_step": tail_bytes,
+                   "note": "3 launches: lane powers (2 B/elem), lane scales, fused equalise + "
+                           "decay (14 B/elem)"}
+
     # ---- end to end: every step copies its gradients in from pinned host memory and
     # its outputs back; the copies of neighbouring steps overlap the current step's
     # compute (two device buffer sets, one upload and one download stream), all inside
@@ -463,7 +503,7 @@ def run_anvil(args, world, rank, local):
             "gemm_phase_frac_of_peak": (alg / (gemm_ms / 1000.0) / 1e12) / peaks["bf16_tflops_sustained"],
             "momentum_frac_of_hbm": (work["momentum"] / (mom_ms / 1000.0) / 1e9) / peaks["hbm_gbs"],
             "profiled_ms_per_step": prof_ms_step,
-            "roofline": roofline, "kernels": kernels,
+            "roofline": roofline, "kernels": kernels, "update_tail": update_tail,
             "e2e": {"value": mats * world / (e2e_ms / 1000.0), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": launches_per_step * nsteps,

@@ -60,18 +60,20 @@ typedef struct { float momentum, fast_beta, fast_weight, slow_beta; } anvil_scal
 
 /* One bank of g matrices of m x n.  All pointers are DEVICE pointers, row-major,
  * caller-owned:
- *   grad      [g, m, n]    fp32, read only (never written)
+ *   grad      [g, m, n]    fp32, or bf16 bits when grad_bf16 != 0 (the page's bank
+ *                          gradient is bf16); read only (never written)
  *   velocity  [2, g, m, n] fp32, read and written in place; rail 0 fast, rail 1 slow
  *   out       [g, m, n]    bf16 bits, written
- * grad and velocity must be 4-byte aligned, out 2-byte aligned; out must not
- * overlap grad, velocity or any buffer of another bank in the same call.
+ * grad must be aligned to its element size, velocity to 4 bytes, out to 2 bytes; out
+ * must not overlap grad, velocity or any buffer of another bank in the same call.
  * `scalars` is used when the call's device scalar array is NULL. */
 typedef struct {
-    const float* grad;
+    const void* grad;
     float* velocity;
     uint16_t* out;
     int g, m, n;
     anvil_scalars scalars;
+    int grad_bf16;
 } anvil_bank_desc;
 
 #define ANVIL_MAX_MAPS 16     /* maps per call */

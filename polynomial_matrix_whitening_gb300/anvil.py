@@ -54,7 +54,7 @@ class Scalars(ctypes.Structure):
 class BankDesc(ctypes.Structure):
     _fields_ = [("grad", ctypes.c_void_p), ("velocity", ctypes.c_void_p), ("out", ctypes.c_void_p),
                 ("g", ctypes.c_int), ("m", ctypes.c_int), ("n", ctypes.c_int),
-                ("scalars", Scalars)]
+                ("scalars", Scalars), ("grad_bf16", ctypes.c_int)]
 
 
 class Trace(ctypes.Structure):
@@ -148,7 +148,8 @@ def _stream_arg(stream):
 
 def _desc(grad, velocity, out, scalars=None):
     import torch
-    assert grad.dtype == torch.float32 and velocity.dtype == torch.float32, "grad/velocity fp32"
+    assert grad.dtype in (torch.float32, torch.bfloat16), "grad fp32 or bf16"
+    assert velocity.dtype == torch.float32, "velocity fp32"
     assert out.dtype == torch.bfloat16, "out is bf16"
     assert grad.is_contiguous() and velocity.is_contiguous() and out.is_contiguous()
     g, m, n = grad.shape
@@ -156,11 +157,12 @@ def _desc(grad, velocity, out, scalars=None):
     s = scalars or {}
     return BankDesc(grad.data_ptr(), velocity.data_ptr(), out.data_ptr(), g, m, n,
                     Scalars(float(s.get("momentum", 0.95)), float(s.get("fast_beta", 0.85)),
-                            float(s.get("fast_weight", 0.4385)), float(s.get("slow_beta", 0.98))))
+                            float(s.get("fast_weight", 0.4385)), float(s.get("slow_beta", 0.98))),
+                    1 if grad.dtype == torch.bfloat16 else 0)
 
 
-def _raw_desc(g, m, n, grad=0, velocity=0, out=0):
-    return BankDesc(grad, velocity, out, g, m, n, Scalars(0.95, 0.85, 0.4385, 0.98))
+def _raw_desc(g, m, n, grad=0, velocity=0, out=0, grad_bf16=0):
+    return BankDesc(grad, velocity, out, g, m, n, Scalars(0.95, 0.85, 0.4385, 0.98), grad_bf16)
 
 
 def workspace_bytes(shapes):
@@ -220,6 +222,8 @@ def multi_bank_step(banks, workspace, maps=None, margin=1.05, eps=1e-6, d_scalar
 def bank_step(grad, velocity, out, momentum=0.95, fast_beta=0.85, fast_weight=0.4385,
               slow_beta=0.98, maps=None, margin=1.05, eps=1e-6, stream=None):
     """One bank, host scalars, library-owned workspace (the page's anvil_cascade call)."""
+    import torch
+    assert grad.dtype == torch.float32, "anvil_bank_step takes fp32 grads; use multi_bank_step for bf16"
     _desc(grad, velocity, out)
     g, m, n = grad.shape
     marr, nm = (None, 0) if maps is None else _maps_arg(maps)
@@ -236,6 +240,8 @@ def bank_step_noalloc(grad, velocity, out, momentum=0.95, fast_beta=0.85, fast_w
                       slow_beta=0.98, maps=None, margin=1.05, eps=1e-6, stream=None):
     """bank_step with the library's fixed device scratch (no allocation by the call); for
     callers that cannot allocate device memory.  Calls that overlap on the GPU race."""
+    import torch
+    assert grad.dtype == torch.float32, "anvil_bank_step_noalloc takes fp32 grads"
     _desc(grad, velocity, out)
     g, m, n = grad.shape
     marr, nm = (None, 0) if maps is None else _maps_arg(maps)

@@ -200,11 +200,12 @@ anvil_status check_banks(const anvil_bank_desc* banks, int nbanks, const Layout&
     for (int i = 0; i < nbanks; ++i) {
         const anvil_bank_desc& b = banks[i];
         if (!b.grad || !b.velocity || !b.out) return ANVIL_ERR_INVALID_ARG;
-        if ((reinterpret_cast<uintptr_t>(b.grad) & 3) || (reinterpret_cast<uintptr_t>(b.velocity) & 3) ||
+        const uintptr_t gsz = b.grad_bf16 ? 2 : 4;
+        if ((reinterpret_cast<uintptr_t>(b.grad) & (gsz - 1)) || (reinterpret_cast<uintptr_t>(b.velocity) & 3) ||
             (reinterpret_cast<uintptr_t>(b.out) & 1))
             return ANVIL_ERR_ALIGNMENT;
         const size_t cnt = static_cast<size_t>(b.g) * b.m * b.n;
-        rg[i][0] = {reinterpret_cast<uintptr_t>(b.grad), reinterpret_cast<uintptr_t>(b.grad + cnt)};
+        rg[i][0] = {reinterpret_cast<uintptr_t>(b.grad), reinterpret_cast<uintptr_t>(b.grad) + gsz * cnt};
         rg[i][1] = {reinterpret_cast<uintptr_t>(b.velocity), reinterpret_cast<uintptr_t>(b.velocity + 2 * cnt)};
         rg[i][2] = {reinterpret_cast<uintptr_t>(b.out), reinterpret_cast<uintptr_t>(b.out + cnt)};
     }
@@ -273,7 +274,8 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
                           reinterpret_cast<uintptr_t>(workspace) + L.total};
         for (int i = 0; i < nbanks; ++i) {
             const size_t cnt = static_cast<size_t>(banks[i].g) * banks[i].m * banks[i].n;
-            const Range r[3] = {{reinterpret_cast<uintptr_t>(banks[i].grad), reinterpret_cast<uintptr_t>(banks[i].grad + cnt)},
+            const uintptr_t gsz = banks[i].grad_bf16 ? 2 : 4;
+            const Range r[3] = {{reinterpret_cast<uintptr_t>(banks[i].grad), reinterpret_cast<uintptr_t>(banks[i].grad) + gsz * cnt},
                                 {reinterpret_cast<uintptr_t>(banks[i].velocity), reinterpret_cast<uintptr_t>(banks[i].velocity + 2 * cnt)},
                                 {reinterpret_cast<uintptr_t>(banks[i].out), reinterpret_cast<uintptr_t>(banks[i].out + cnt)}};
             for (int k = 0; k < 3; ++k)
@@ -340,7 +342,8 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
             M.tiles_r = (G.tall ? G.L_pad : G.s_pad) / LBLK;
             M.tiles_c = (G.tall ? G.s_pad : G.L_pad) / LBLK;
             M.tile_begin = tiles;
-            M.vec4 = (G.n % 4 == 0) && !(reinterpret_cast<uintptr_t>(b.grad) & 15) &&
+            M.grad_bf16 = b.grad_bf16 ? 1 : 0;
+            M.vec4 = (G.n % 4 == 0) && !(reinterpret_cast<uintptr_t>(b.grad) & (b.grad_bf16 ? 7 : 15)) &&
                      !(reinterpret_cast<uintptr_t>(b.velocity) & 15);
             M.momentum = b.scalars.momentum;
             M.fast_beta = b.scalars.fast_beta;
@@ -707,6 +710,7 @@ anvil_status anvil_bank_step(const float* grad, float* velocity, int g, int m, i
     b.scalars.fast_beta = fast_beta;
     b.scalars.fast_weight = fast_weight;
     b.scalars.slow_beta = slow_beta;
+    b.grad_bf16 = 0;
     if (!maps) {
         maps = kAnvilMaps;
         nmaps = 6;
@@ -850,6 +854,7 @@ anvil_status anvil_bank_step_noalloc(const float* grad, float* velocity, int g, 
     b.scalars.fast_beta = fast_beta;
     b.scalars.fast_weight = fast_weight;
     b.scalars.slow_beta = slow_beta;
+    b.grad_bf16 = 0;
     if (!maps) {
         maps = kAnvilMaps;
         nmaps = 6;

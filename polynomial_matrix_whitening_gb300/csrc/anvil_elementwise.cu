@@ -50,7 +50,8 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
 
     const int m = B.m, n = B.n;
     const size_t mn = static_cast<size_t>(m) * n;
-    const float* G = B.grad + static_cast<size_t>(mat) * mn;
+    const float* G = static_cast<const float*>(B.grad) + static_cast<size_t>(mat) * mn;
+    const uint16_t* Gh = static_cast<const uint16_t*>(B.grad) + static_cast<size_t>(mat) * mn;
     float* V0 = B.velocity + static_cast<size_t>(mat) * mn;
     float* V1 = V0 + static_cast<size_t>(B.g) * mn;
     uint16_t* Y = B.y + static_cast<size_t>(mat) * B.s_pad * B.L_pad;
@@ -70,7 +71,14 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
             if (B.vec4) {
                 const bool row_in = c < n;  // n % 4 == 0: all four or none
                 if (row_in) {
-                    const float4 g4 = __ldcs(reinterpret_cast<const float4*>(G + base));
+                    float4 g4;
+                    if (B.grad_bf16) {
+                        const uint2 h = __ldcs(reinterpret_cast<const uint2*>(Gh + base));
+                        g4 = make_float4(bf2f(static_cast<uint16_t>(h.x & 0xffffu)), bf2f(static_cast<uint16_t>(h.x >> 16)),
+                                         bf2f(static_cast<uint16_t>(h.y & 0xffffu)), bf2f(static_cast<uint16_t>(h.y >> 16)));
+                    } else {
+                        g4 = __ldcs(reinterpret_cast<const float4*>(G + base));
+                    }
                     const float4 a4 = __ldcs(reinterpret_cast<const float4*>(V0 + base));
                     const float4 b4 = __ldcs(reinterpret_cast<const float4*>(V1 + base));
                     g[0] = g4.x; g[1] = g4.y; g[2] = g4.z; g[3] = g4.w;
@@ -83,7 +91,7 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     in[q] = c + q < n;
-                    g[q] = in[q] ? G[base + q] : 0.f;
+                    g[q] = in[q] ? (B.grad_bf16 ? bf2f(Gh[base + q]) : G[base + q]) : 0.f;
                     v0[q] = in[q] ? V0[base + q] : 0.f;
                     v1[q] = in[q] ? V1[base + q] : 0.f;
                 }

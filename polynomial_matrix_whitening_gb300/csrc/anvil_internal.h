@@ -34,14 +34,15 @@ enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_BOUNDS = 2u };
 
 // ---------------------------------------------------------------- momentum + cast
 struct MomentumBank {
-    const float* grad;   // [g, m, n]
+    const void* grad;    // fp32, or bf16 bits when grad_bf16   // [g, m, n]
     float* velocity;     // [2, g, m, n]
     uint16_t* y;         // Y_raw [g, s_pad, L_pad]
     float* part;         // [g, nlb, s_pad]: sums of squares of the bf16 values per 64-block
     int g, m, n, tall, s_pad, L_pad, nlb;
     int tiles_r, tiles_c;  // 64x64 tiles over the padded natural extent [rows, cols]
     int tile_begin;        // first tile of this bank in the grouped grid
-    int vec4;              // n % 4 == 0 and 16-byte aligned grad/velocity: float4 path
+    int vec4;              // n % 4 == 0 and aligned grad/velocity: 4-element vector path
+    int grad_bf16;
     float momentum, fast_beta, fast_weight, slow_beta;
 };
 struct MomentumParams {

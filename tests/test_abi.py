@@ -1,6 +1,8 @@
 """Host-side checks of libanvil's C ABI that need no GPU: the library loads, exports
 every function include/anvil.h declares, holds the page's ANVIL_MAPS, and rejects bad
-arguments with the documented status before it makes any CUDA call."""
+arguments with the documented status before it makes any CUDA call.  Every call here
+fails validation (the pointers are fake), so nothing reaches a GPU even where one is
+present."""
 import ctypes
 
 import numpy as np
@@ -42,8 +44,8 @@ def _call(descs, maps=None, nmaps=6, ws=1 << 40, ws_bytes=1 << 40, margin=1.05, 
 G = 1 << 32  # fake, aligned device addresses far apart
 
 
-def d(g=2, m=40, n=24, grad=G, vel=2 * G, out=3 * G):
-    return anvil._raw_desc(g, m, n, grad, vel, out)
+def d(g=2, m=40, n=24, grad=G, vel=2 * G, out=3 * G, grad_bf16=0):
+    return anvil._raw_desc(g, m, n, grad, vel, out, grad_bf16)
 
 
 def test_workspace_bytes():
@@ -65,6 +67,7 @@ def test_workspace_bytes():
     (dict(n=-1), anvil.ERR_INVALID_ARG),
     (dict(m=20000), anvil.ERR_UNSUPPORTED_SHAPE),
     (dict(grad=G + 2), anvil.ERR_ALIGNMENT),
+    (dict(grad=G + 1, grad_bf16=1), anvil.ERR_ALIGNMENT),
     (dict(out=3 * G + 1), anvil.ERR_ALIGNMENT),
     (dict(out=G), anvil.ERR_ALIAS),            # out == grad
     (dict(out=2 * G + 4), anvil.ERR_ALIAS),    # out inside velocity

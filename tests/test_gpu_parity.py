@@ -216,6 +216,28 @@ def test_other_coefficient_sets(A, name, shape):
         assert rel(f64(got[i]), f64(out[i])) <= OUT_RTOL, (name, i)
 
 
+@pytest.mark.parametrize("shape", [(22, 256, 768), (3, 300, 130), (2, 130, 257)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_bf16_grad_input(A, shape):
+    """The page's bank gradient is bf16: the same step from bf16 gradient bits (the oracle
+    reads them as their exact fp32 values)."""
+    g, m, n = shape
+    grad, vel = W.random_case(90 + m, g, m, n)
+    gh = oracle.f32_to_bf16(grad)
+    sc = dict(momentum=0.95, fast_beta=0.85, fast_weight=0.4385, slow_beta=0.98)
+    dev = torch.device("cuda")
+    bank = A.Bank(torch.from_numpy(gh.view(np.int16)).to(dev).view(torch.bfloat16),
+                  torch.from_numpy(vel).to(dev), torch.empty(shape, dtype=torch.bfloat16, device=dev), **sc)
+    A.multi_bank_step([bank], A.alloc_workspace([shape]))
+    torch.cuda.synchronize()
+    out, vel_or = oracle.bank_step(oracle.bf16_to_f32(gh), vel, **sc)
+    vg = bank.velocity.cpu().numpy()
+    assert np.max(np.abs(vg - vel_or)) <= VEL_RTOL * np.max(np.abs(vel_or))
+    got = bits(bank.out)
+    for i in range(g):
+        assert rel(f64(got[i]), f64(out[i])) <= OUT_RTOL
+
+
 def test_zero_grad_gives_zero_output(A):
     shape = (2, 300, 130)
     grad = np.zeros(shape, np.float32)
