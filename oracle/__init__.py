@@ -80,6 +80,7 @@ def lib():
         L.oracle_bank_step.restype = i
         L.oracle_rail_equalizer.argtypes = [vp, i, i, i, vp, f, vp]
         L.oracle_sign_aligned_decay.argtypes = [vp, vp, vp, vp, i, l, f, vp]
+        L.oracle_adam_step.argtypes = [vp, vp, vp, vp, l, f, f, f, f, f]
         L.oracle_num_threads.restype = i
         L.oracle_set_num_threads.argtypes = [i]
         _lib = L
@@ -223,3 +224,16 @@ def update_tail(v_bits, lane_energy, beta2, p_bits, mantissa, gate, wd, lr):
     v_eq, le = rail_equalizer(v_bits, lane_energy, beta2)
     p, mt = sign_aligned_decay(p_bits, mantissa, v_eq, gate, wd, lr)
     return p, mt, le, v_eq
+
+
+def adam_step(p, g, exp_avg, exp_avg_sq, beta1, beta2, eps, step_size, eff_wd):
+    """The page's Adam step with cautious weight decay (fp32, elementwise).
+    Returns (p, exp_avg, exp_avg_sq) as new arrays."""
+    p = np.array(p, np.float32, copy=True, order="C")
+    m = np.array(exp_avg, np.float32, copy=True, order="C")
+    v = np.array(exp_avg_sq, np.float32, copy=True, order="C")
+    g = np.ascontiguousarray(g, np.float32)
+    assert p.shape == g.shape == m.shape == v.shape
+    lib().oracle_adam_step(_ptr(p), _ptr(g), _ptr(m), _ptr(v), p.size, beta1, beta2, eps, step_size,
+                           eff_wd)
+    return p, m, v

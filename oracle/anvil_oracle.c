@@ -390,6 +390,29 @@ EXPORT void oracle_sign_aligned_decay(uint16_t* p, uint16_t* mantissa, const uin
     }
 }
 
+/* ---- Adam with cautious weight decay: anvil.py, `_adam_update_step` ----
+ * Elementwise over count fp32 values, the page's tensor operations in order, one rounding
+ * each (step_size = lr * sqrt(1 - beta2^t) / (1 - beta1^t) and eff_wd are the caller's):
+ *   exp_avg    = exp_avg * beta1 + (1 - beta1) * g
+ *   exp_avg_sq = exp_avg_sq * beta2 + ((1 - beta2) * g) * g
+ *   update     = (exp_avg / (sqrt(exp_avg_sq) + eps)) * step_size
+ *   update     = update + (eff_wd * p) * [update * p > 0]
+ *   p          = p - update */
+EXPORT void oracle_adam_step(float* p, const float* g, float* exp_avg, float* exp_avg_sq, long count,
+                             float beta1, float beta2, float eps, float step_size, float eff_wd) {
+    const float c1 = 1.0f - beta1, c2 = 1.0f - beta2;
+    for (long e = 0; e < count; ++e) {
+        const float m = exp_avg[e] * beta1 + c1 * g[e];
+        const float v = exp_avg_sq[e] * beta2 + (c2 * g[e]) * g[e];
+        exp_avg[e] = m;
+        exp_avg_sq[e] = v;
+        float u = (m / (sqrtf(v) + eps)) * step_size;
+        const float mask = (u * p[e] > 0.0f) ? 1.0f : 0.0f;
+        u = u + (eff_wd * p[e]) * mask;
+        p[e] = p[e] - u;
+    }
+}
+
 EXPORT int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -32,6 +32,9 @@ MUTATIONS = {
                            "const float aligned = (gate[e] * w <= 0.0f) ? 1.0f : 0.0f;"),
     "decay_without_lr": ("w = (w - ((w * aligned) * wd) * lrm) - u * lrm;", "w = (w - (w * aligned) * wd) - u * lrm;"),
     "no_norm_restore": ("const float ratio = pre_norm / post_norm;", "const float ratio = 1.0f;"),
+    "adam_mask_reversed": ("const float mask = (u * p[e] > 0.0f) ? 1.0f : 0.0f;",
+                           "const float mask = (u * p[e] < 0.0f) ? 1.0f : 0.0f;"),
+    "adam_second_moment_unsquared": ("(c2 * g[e]) * g[e]", "(c2 * g[e])"),
 }
 
 

@@ -115,3 +115,37 @@ def test_decay_bit_split_round_trips():
                                         np.ones((1, 64), np.float32), 0.0, np.zeros(1, np.float32))
     np.testing.assert_array_equal(p2, p)
     np.testing.assert_array_equal(mt2, mt)
+
+
+# --------------------------------------------------------------------------- Adam
+
+def test_adam_first_step_closed_form():
+    """From zero moments: m = (1-b1) g, v = (1-b2) g^2, and with the bias-corrected step
+    size lr sqrt(1-b2)/(1-b1) the update is lr g / (|g| + eps / sqrt(1-b2)) (no decay)."""
+    rng = np.random.default_rng(8)
+    g = (rng.standard_normal(4096) * 0.01).astype(np.float32)
+    p = (rng.standard_normal(4096) * 0.1).astype(np.float32)
+    b1, b2, eps, lr = 0.9, 0.95, 1e-8, 0.01
+    step = lr * np.sqrt(1 - b2) / (1 - b1)
+    p2, m, v = oracle.adam_step(p, g, np.zeros_like(g), np.zeros_like(g), b1, b2, eps, step, 0.0)
+    G = g.astype(np.float64)
+    np.testing.assert_allclose(m, (1 - np.float32(b1)) * G, rtol=1e-6)
+    np.testing.assert_allclose(v, (1 - np.float64(np.float32(b2))) * G * G, rtol=1e-6)
+    want = p - lr * G / (np.abs(G) + eps / np.sqrt(1 - b2))
+    # a handful of fp32 roundings of values of size |p| + lr
+    assert np.all(np.abs(p2 - want) <= 8 * U32 * (np.abs(p) + lr) + 1e-6 * lr)
+
+
+def test_adam_cautious_decay_only_where_update_and_weight_agree():
+    rng = np.random.default_rng(9)
+    g = (rng.standard_normal(2048) * 0.01).astype(np.float32)
+    p = (rng.standard_normal(2048) * 0.1).astype(np.float32)
+    m0 = (rng.standard_normal(2048) * 0.01).astype(np.float32)
+    v0 = (np.abs(rng.standard_normal(2048)) * 1e-4).astype(np.float32)
+    a = oracle.adam_step(p, g, m0, v0, 0.9, 0.95, 1e-8, 0.01, 0.0)[0]
+    b = oracle.adam_step(p, g, m0, v0, 0.9, 0.95, 1e-8, 0.01, 0.05)[0]
+    upd = p.astype(np.float64) - a
+    decayed = b != a
+    assert np.array_equal(decayed, (upd * p > 0) & (p != 0))
+    scale = np.abs(p) + np.abs(upd)
+    assert np.all(np.abs((a - b) - 0.05 * p)[decayed] <= 8 * U32 * scale[decayed])
