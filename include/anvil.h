@@ -185,6 +185,20 @@ size_t anvil_tail_workspace_bytes(const anvil_tail_desc* banks, int nbanks);
 anvil_status anvil_update_tail(const anvil_tail_desc* banks, int nbanks, void* workspace,
                                size_t workspace_bytes, void* stream);
 
+/* The page's Adam step for the parameters outside the ANVIL banks (`_adam_update_step`:
+ * bias-corrected Adam with cautious weight decay), elementwise over count fp32 values,
+ * DEVICE pointers, caller-owned, read and written in place except grad:
+ *   exp_avg    = exp_avg * beta1 + (1 - beta1) * grad
+ *   exp_avg_sq = exp_avg_sq * beta2 + ((1 - beta2) * grad) * grad
+ *   u = (exp_avg / (sqrt(exp_avg_sq) + eps)) * step_size
+ *   u = u + (eff_wd * param) * [u * param > 0];   param = param - u
+ * step_size (lr * sqrt(1 - beta2^t) / (1 - beta1^t)) and eff_wd are the caller's, as on
+ * the page.  Buffers 4-byte aligned; param, exp_avg and exp_avg_sq must not overlap any
+ * other buffer of the call.  One launch on the stream; allocates nothing. */
+anvil_status anvil_adam_step(float* param, const float* grad, float* exp_avg, float* exp_avg_sq,
+                             size_t count, float beta1, float beta2, float eps, float step_size,
+                             float eff_wd, void* stream);
+
 /* Per-stage dumps of one bank step, for parity testing (not the hot path).
  * DEVICE pointers, each optional (NULL = skip), in the page's layout:
  *   X_raw [g, m, n] bf16            bf16 cast of the momentum lookahead
@@ -219,8 +233,8 @@ anvil_status anvil_device_error(int clear);
 anvil_status anvil_selftest_wait_timeout(unsigned timeout_us, void* stream);
 
 /* Per-launch timing for benchmarks.  Between anvil_profile_begin and
- * anvil_profile_end, every kernel launch of anvil_multi_bank_step,
- * anvil_bank_step and anvil_update_tail in the process is bracketed by two CUDA events
+ * anvil_profile_end, every kernel launch of anvil_multi_bank_step, anvil_bank_step,
+ * anvil_update_tail and anvil_adam_step in the process is bracketed by two CUDA events
  * recorded on the call's stream (at most max_records launches; later ones are
  * not timed).  begin creates the events (a host call: do not begin, or step
  * with profiling on, while a stream is capturing).  end synchronises, writes up
@@ -237,7 +251,8 @@ typedef enum {
     ANVIL_KERNEL_XUPDATE_OUT = 7,  /* the last map's X-update, written to out */
     ANVIL_KERNEL_TAIL_POWER = 8,   /* update tail: lane powers */
     ANVIL_KERNEL_TAIL_SCALE = 9,   /* update tail: lane energies and scales */
-    ANVIL_KERNEL_TAIL_APPLY = 10   /* update tail: equalise + sign-aligned decay update */
+    ANVIL_KERNEL_TAIL_APPLY = 10,  /* update tail: equalise + sign-aligned decay update */
+    ANVIL_KERNEL_ADAM = 11         /* Adam step */
 } anvil_kernel_kind;
 
 typedef struct { int kind; float ms; } anvil_profile_record;

@@ -31,7 +31,7 @@ STATUS = {0: "ANVIL_OK", 1: "ANVIL_ERR_INVALID_ARG", 2: "ANVIL_ERR_UNSUPPORTED_S
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_ALIGNMENT, ERR_ALIAS, ERR_WORKSPACE, \
     ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(9)
 KERNEL_KINDS = ("momentum", "norm_d", "normalize", "gram_norm", "gram", "sqpoly", "xupdate",
-                "xupdate_out", "tail_power", "tail_scale", "tail_apply")
+                "xupdate_out", "tail_power", "tail_scale", "tail_apply", "adam")
 MAX_MAPS, MAX_BANKS = 16, 8
 
 
@@ -94,6 +94,8 @@ _lib.anvil_tail_workspace_bytes.argtypes = [ctypes.POINTER(TailDesc), _i]
 _lib.anvil_tail_workspace_bytes.restype = _sz
 _lib.anvil_update_tail.argtypes = [ctypes.POINTER(TailDesc), _i, _vp, _sz, _vp]
 _lib.anvil_update_tail.restype = _i
+_lib.anvil_adam_step.argtypes = [_vp, _vp, _vp, _vp, _sz, _f, _f, _f, _f, _f, _vp]
+_lib.anvil_adam_step.restype = _i
 _lib.anvil_device_error.argtypes = [_i]
 _lib.anvil_device_error.restype = _i
 _lib.anvil_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
@@ -311,6 +313,16 @@ def update_tail(tails, workspace, stream=None):
     st = _lib.anvil_update_tail(descs, len(tails), workspace.data_ptr(),
                                 workspace.numel() * workspace.element_size(), _stream_arg(stream))
     _check(st, "anvil_update_tail")
+
+
+def adam_step(param, grad, exp_avg, exp_avg_sq, beta1, beta2, eps, step_size, eff_wd, stream=None):
+    """The page's Adam step with cautious weight decay, in place on fp32 CUDA tensors."""
+    import torch
+    for t in (param, grad, exp_avg, exp_avg_sq):
+        assert t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and t.numel() == param.numel()
+    st = _lib.anvil_adam_step(param.data_ptr(), grad.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(),
+                              param.numel(), beta1, beta2, eps, step_size, eff_wd, _stream_arg(stream))
+    _check(st, "anvil_adam_step")
 
 
 def device_error(clear=True):

@@ -23,6 +23,7 @@
 
 #include "../../include/anvil.h"
 #include "anvil_internal.h"
+#include "anvil_adam.h"
 #include "anvil_tail.h"
 
 using namespace anvil;
@@ -684,6 +685,43 @@ anvil_status anvil_update_tail(const anvil_tail_desc* banks, int nbanks, void* w
     if ((e = profiled(ANVIL_KERNEL_TAIL_APPLY, s, [&] { return launch_tail_apply(tp, s); })))
         return cuda_fail(e, "tail apply launch");
     return ANVIL_OK;
+}
+
+anvil_status anvil_adam_step(float* param, const float* grad, float* exp_avg, float* exp_avg_sq,
+                             size_t count, float beta1, float beta2, float eps, float step_size,
+                             float eff_wd, void* stream) {
+    if (!param || !grad || !exp_avg || !exp_avg_sq || count == 0) return ANVIL_ERR_INVALID_ARG;
+    const uintptr_t ptrs[4] = {reinterpret_cast<uintptr_t>(param), reinterpret_cast<uintptr_t>(grad),
+                               reinterpret_cast<uintptr_t>(exp_avg), reinterpret_cast<uintptr_t>(exp_avg_sq)};
+    bool vec = true;
+    for (int i = 0; i < 4; ++i) {
+        if (ptrs[i] & 3) return ANVIL_ERR_ALIGNMENT;
+        vec = vec && !(ptrs[i] & 15);
+    }
+    for (int i = 0; i < 4; ++i)
+        for (int j = 0; j < 4; ++j)
+            if (i != j && (i != 1) && overlap({ptrs[i], ptrs[i] + 4 * count}, {ptrs[j], ptrs[j] + 4 * count}))
+                return ANVIL_ERR_ALIAS;
+    anvil_status st;
+    DeviceState* dev = nullptr;
+    if ((st = device_setup(&dev)) != ANVIL_OK) return st;
+    AdamParams a;
+    a.p = param;
+    a.g = grad;
+    a.m = exp_avg;
+    a.v = exp_avg_sq;
+    a.count = static_cast<long long>(count);
+    a.vec = vec ? 1 : 0;
+    a.beta1 = beta1;
+    a.beta2 = beta2;
+    a.c1 = 1.0f - beta1;
+    a.c2 = 1.0f - beta2;
+    a.eps = eps;
+    a.step_size = step_size;
+    a.eff_wd = eff_wd;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = profiled(ANVIL_KERNEL_ADAM, s, [&] { return launch_adam(a, s); });
+    return e ? cuda_fail(e, "adam launch") : ANVIL_OK;
 }
 
 anvil_status anvil_bank_step_traced(const anvil_bank_desc* bank, const anvil_scalars* d_scalars,

@@ -98,3 +98,31 @@ def test_workspace_errors():
     assert _call([d()], ws=0) == anvil.ERR_WORKSPACE
     assert _call([d()], ws=7 * G, ws_bytes=need - 1) == anvil.ERR_WORKSPACE
     assert _call([d()], ws=7 * G + 128, ws_bytes=need) == anvil.ERR_ALIGNMENT
+
+
+def test_adam_argument_errors():
+    f = L.anvil_adam_step
+    ok = dict(p=G, g=2 * G, m=3 * G, v=4 * G)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(a["p"], a["g"], a["m"], a["v"], kw.get("count", 100), 0.9, 0.95, 1e-8, 0.01, 0.0, None)
+    assert call(p=0) == anvil.ERR_INVALID_ARG
+    assert call(count=0) == anvil.ERR_INVALID_ARG
+    assert call(m=3 * G + 2) == anvil.ERR_ALIGNMENT
+    assert call(m=G + 64) == anvil.ERR_ALIAS      # exp_avg overlaps the parameter
+    assert call(v=2 * G + 8) == anvil.ERR_ALIAS   # exp_avg_sq overlaps the gradient
+
+
+def test_tail_argument_errors():
+    def tail(**kw):
+        base = dict(update=G, velocity=2 * G, lane_energy=3 * G, param=4 * G, mantissa=5 * G,
+                    eff_lr=6 * G, g=2, m=40, n=24, eff_wd=0.1, beta2=0.95)
+        base.update(kw)
+        d = anvil.TailDesc(*[base[k] for k, _ in anvil.TailDesc._fields_])
+        return L.anvil_update_tail(ctypes.byref(d), 1, 1 << 40, 1 << 40, None)
+    assert tail(update=0) == anvil.ERR_INVALID_ARG
+    assert tail(g=0) == anvil.ERR_INVALID_ARG
+    assert tail(param=4 * G + 1) == anvil.ERR_ALIGNMENT
+    assert tail(mantissa=4 * G + 16) == anvil.ERR_ALIAS   # mantissa over the parameter
+    assert tail(lane_energy=2 * G) == anvil.ERR_ALIAS     # state written over the rails

@@ -118,3 +118,27 @@ def test_step_then_tail_matches_oracle_step_then_tail(A):
     for i in range(shape[0]):
         assert np.linalg.norm(dg[i] - do[i]) <= 1e-2 * np.linalg.norm(do[i])
     np.testing.assert_allclose(t.lane_energy.cpu().numpy(), le_o, rtol=2e-2)
+
+
+# --------------------------------------------------------------------------- Adam
+
+@pytest.mark.parametrize("count,offset", [(1 << 20, 0), (1000003, 0), (4096, 1)])
+def test_adam_step_matches_oracle_bitwise(A, count, offset):
+    """Same fp32 operations in the same order on both sides: identical bits.  The offset
+    case starts the buffers one float off 16-byte alignment (scalar path)."""
+    rng = np.random.default_rng(count)
+    p = (rng.standard_normal(count) * 0.1).astype(np.float32)
+    g = (rng.standard_normal(count) * 0.01).astype(np.float32)
+    m = (rng.standard_normal(count) * 0.01).astype(np.float32)
+    v = (np.abs(rng.standard_normal(count)) * 1e-4).astype(np.float32)
+    args = (0.9, 0.95, 1e-8, 0.0123, 0.0004)
+    want = oracle.adam_step(p, g, m, v, *args)
+    dev = [torch.zeros(count + offset, dtype=torch.float32, device="cuda") for _ in range(4)]
+    views = [d[offset:] for d in dev]
+    for d, x in zip(views, (p, g, m, v)):
+        d.copy_(torch.from_numpy(x))
+    for _ in range(1):
+        A.adam_step(views[0], views[1], views[2], views[3], *args)
+    torch.cuda.synchronize()
+    for got, w in zip((views[0], views[2], views[3]), want):
+        np.testing.assert_array_equal(got.cpu().numpy(), w)
