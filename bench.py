@@ -416,6 +416,27 @@ def run_anvil(args, world, rank, local):
                    "note": "3 launches: lane powers (2 B/elem), lane scales, fused equalise + "
                            "decay (14 B/elem)"}
 
+    # ---- the page's Adam step on an lm_head-sized fp32 parameter (768 x 50304)
+    cnt = 768 * 50304
+    adam_t = [torch.randn(cnt, device=dev, generator=gen) * s_ for s_ in (0.1, 0.01, 0.01)]
+    adam_t.append(torch.rand(cnt, device=dev, generator=gen) * 1e-4)
+    with torch.cuda.stream(stream):
+        for _ in range(nwarm):
+            anvil.adam_step(adam_t[0], adam_t[1], adam_t[2], adam_t[3], 0.9, 0.95, 1e-8, 1e-3, 0.0,
+                            stream=stream)
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(max(nsteps, 20)):
+            anvil.adam_step(adam_t[0], adam_t[1], adam_t[2], adam_t[3], 0.9, 0.95, 1e-8, 1e-3, 0.0,
+                            stream=stream)
+        a1.record(stream)
+    torch.cuda.synchronize()
+    adam_ms = a0.elapsed_time(a1) / max(nsteps, 20)
+    adam_gbs = cnt * 28.0 / (adam_ms / 1000.0) / 1e9
+    adam = {"params": cnt, "ms": adam_ms, "achieved": adam_gbs, "unit": "GB/s",
+            "frac": adam_gbs / peaks["hbm_gbs"], "bytes_per_param": 28}
+    del adam_t
+
     # ---- end to end: every step copies its gradients in from pinned host memory and
     # its outputs back; the copies of neighbouring steps overlap the current step's
     # compute (two device buffer sets, one upload and one download stream), all inside
@@ -503,7 +524,7 @@ def run_anvil(args, world, rank, local):
             "gemm_phase_frac_of_peak": (alg / (gemm_ms / 1000.0) / 1e12) / peaks["bf16_tflops_sustained"],
             "momentum_frac_of_hbm": (work["momentum"] / (mom_ms / 1000.0) / 1e9) / peaks["hbm_gbs"],
             "profiled_ms_per_step": prof_ms_step,
-            "roofline": roofline, "kernels": kernels, "update_tail": update_tail,
+            "roofline": roofline, "kernels": kernels, "update_tail": update_tail, "adam": adam,
             "e2e": {"value": mats * world / (e2e_ms / 1000.0), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": launches_per_step * nsteps,
