@@ -62,6 +62,19 @@ __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
     return (static_cast<uint64_t>(w & 0xffff0000u) << 32) | (w << 16);
 }
 
+// ---- programmatic dependent launch ---------------------------------------------------
+// A kernel launched with programmatic stream serialisation may start while the previous
+// kernel of the stream finishes; it must wait here before touching anything that kernel
+// writes or reads.  Without that launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait_previous() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next kernel of the stream be scheduled (it still waits for this one to finish
+// before it touches memory).
+__device__ __forceinline__ void pdl_allow_next() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier -----------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));

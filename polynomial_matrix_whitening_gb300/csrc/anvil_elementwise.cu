@@ -22,6 +22,8 @@ __device__ unsigned g_error_word;
 // operation at a time (no fused multiply-add): lerp(s, e, w) = s + w (e - s).
 __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ MomentumParams p) {
     __shared__ __align__(16) uint16_t tileT[64][64 + 8];  // tall: [s-index][L-index]
+    pdl_allow_next();
+    pdl_wait_previous();
 
     const int t = blockIdx.x;
     int bi = 0;
@@ -161,8 +163,7 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
 }
 
 cudaError_t launch_momentum(const MomentumParams& p, cudaStream_t stream) {
-    momentum_kernel<<<p.total_tiles, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(momentum_kernel, dim3(p.total_tiles), dim3(256), 0, stream, p);
 }
 
 // One block per matrix.  Diagonal entry i of the first Gram is the fp32 sum of the
@@ -170,6 +171,8 @@ cudaError_t launch_momentum(const MomentumParams& p, cudaStream_t stream) {
 // those in fp32.
 __global__ void __launch_bounds__(256) norm_d_kernel(const __grid_constant__ NormParams p) {
     __shared__ float red[256];
+    pdl_allow_next();
+    pdl_wait_previous();
     const int gm = blockIdx.x;
     int bi = 0;
 #pragma unroll 1
@@ -197,8 +200,7 @@ __global__ void __launch_bounds__(256) norm_d_kernel(const __grid_constant__ Nor
 }
 
 cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream) {
-    norm_d_kernel<<<p.total_mats, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(norm_d_kernel, dim3(p.total_mats), dim3(256), 0, stream, p);
 }
 
 // Y_out <- bf16(float(Y) / d) over 8-element (16-byte) vectors, grid-stride over all banks,
@@ -215,6 +217,8 @@ __device__ __forceinline__ uint4 normalize_vec(uint4 u, float d) {
 }
 
 __global__ void __launch_bounds__(256) normalize_kernel(const __grid_constant__ NormParams p) {
+    pdl_allow_next();
+    pdl_wait_previous();
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long v0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
          v0 < p.total_vecs; v0 += 4 * stride) {
@@ -250,8 +254,7 @@ cudaError_t launch_normalize(const NormParams& p, cudaStream_t stream) {
     long long blocks = (p.total_vecs + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;
-    normalize_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(normalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
 }
 
 // ---------------------------------------------------------------- tracing

@@ -185,6 +185,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int aborted;
 
+    pdl_allow_next();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the MMAs), 1 = peer
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     tc_fence_before();
     cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
     tc_fence_after();
+    pdl_wait_previous();  // everything above overlapped the previous kernel's tail
     const uint32_t tmem = tmem_slot;
     int issued = 0;        // producer: k-blocks whose loads were armed (in the whole CTA life)
     int epi_tiles = 0;     // epilogue: tiles whose input staging loads were armed
@@ -487,11 +489,14 @@ static cudaError_t launch_op(const GemmParams& p, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e) return e;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // the prologue may overlap the previous kernel's tail (see pdl_wait_previous)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = OpTraits<OP>::SMEM;
     cfg.stream = stream;
@@ -507,6 +512,7 @@ static cudaError_t launch_op(const GemmParams& p, cudaStream_t stream) {
     }
     const int pairs = p.total_tiles < maxp ? p.total_tiles : maxp;
     cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, gemm_kernel<OP>, p);
 }
 

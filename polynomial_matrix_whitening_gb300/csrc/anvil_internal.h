@@ -29,6 +29,25 @@ constexpr int MAX_LAUNCH_BANKS = 4;  // banks grouped into one GEMM launch
 
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
+// Launches `kernel` with programmatic stream serialisation: its prologue may overlap the
+// tail of the previous kernel on the stream; the kernel calls pdl_wait_previous() before
+// touching memory.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Bits of the device error word (set with atomicOr, read by anvil_device_error).
 enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_BOUNDS = 2u };
 
