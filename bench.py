@@ -2,7 +2,7 @@
 """Benchmark of the ANVIL optimizer step on GB300: one full step over the three
 projection banks (qk 22x256x768, vo 22x768x768, mlp 22x2816x768; 66 matrices), mixed
 synthetic inputs (half Gaussian, half rank-32 plus 1e-3 noise), post-engage scalars,
-each step one CUDA-graph replay of the grouped launch sequence.
+each step one CUDA-graph replay of its three launches (momentum, d, the cascade).
 
 Prints one JSON line (rank 0).  ``value`` is whole-job matrices/s with the inputs
 resident in HBM; ``e2e`` is the same metric through the same C-ABI call with the
@@ -41,18 +41,16 @@ from polynomial_matrix_whitening_gb300 import workloads as W  # noqa: E402
 METRIC = "ANVIL bank-step matrices/s and TFLOP/s; % of GB300 bf16 tensor peak"
 UNIT = "matrices/s"
 WORKLOAD = "full_step"
+GEMM_KINDS = ("gram", "gram_norm", "sqpoly", "xupdate", "xupdate_out", "cascade")
 
 # ncu DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
 # kernel kind on this workload, from the capture summarised under profiles/; valid only
 # while the kernel source hashes to the recorded value.
-NCU_TRAFFIC = {
-    # profiles/gemm_full_step.md: X-update of map 1 over all three banks
-    "xupdate": {"bytes_per_launch": 281.1e6, "source_hash": "aa89ca42115ad2e7"},
-}
+NCU_TRAFFIC = {}
 
 
 def kernel_source_hash(kind):
-    name = "anvil_elementwise.cu" if kind in ("momentum", "norm_d", "normalize") else "anvil_gemm.cu"
+    name = "anvil_elementwise.cu" if kind in ("momentum", "norm_d") else "anvil_gemm.cu"
     with open(os.path.join(ROOT, "polynomial_matrix_whitening_gb300", "csrc", name), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
@@ -83,7 +81,7 @@ def algorithmic_work(banks, nmaps=6):
     """Per launch of each kernel kind over all banks: flops (GEMMs, symmetric products
     counted on one triangle) or bytes (elementwise kernels)."""
     w = {"gram": 0.0, "gram_norm": 0.0, "sqpoly": 0.0, "xupdate": 0.0, "xupdate_out": 0.0,
-         "momentum": 0.0, "normalize": 0.0, "norm_d": 0.0}
+         "momentum": 0.0, "normalize": 0.0, "norm_d": 0.0, "cascade": 0.0}
     for g, m, n, s, L in bank_dims(banks):
         w["gram"] += g * s * (s + 1) * L
         w["gram_norm"] += g * s * (s + 1) * L
@@ -93,6 +91,9 @@ def algorithmic_work(banks, nmaps=6):
         w["momentum"] += g * m * n * 22.0        # 4 B grad + 2x(4+4) B rails + 2 B X
         w["normalize"] += g * m * n * 4.0        # read + write bf16
         w["norm_d"] += g * m * 4.0
+        # the cascade kernel: every product of every map (the normalisation's bytes are
+        # not counted: the kernel is bound by the tensor pipe)
+        w["cascade"] += g * nmaps * (s * (s + 1) * L + s * (s + 1) * s + 2.0 * s * s * L)
     return w
 
 
@@ -297,7 +298,7 @@ def run_anvil(args, world, rank, local):
 
     with torch.cuda.stream(stream):
         graphs = [capture(p) for p in pool_d]
-    launches_per_step = 3 * 6 + 3
+    launches_per_step = 3   # momentum, norm_d, the cascade
     nsteps, nwarm = args.steps, args.warmup
 
     # ---- timed region: K graph replays, inputs resident in HBM
@@ -351,7 +352,7 @@ def run_anvil(args, world, rank, local):
     kernels = {}
     for kind, (cnt, tot) in per_kind.items():
         avg = tot / cnt
-        gemm = kind in ("gram", "gram_norm", "sqpoly", "xupdate", "xupdate_out")
+        gemm = kind in GEMM_KINDS
         rate = work[kind] / (avg / 1000.0)
         kernels[kind] = {
             "launches_per_step": cnt / prof_steps, "avg_ms": round(avg, 5),
@@ -372,8 +373,7 @@ def run_anvil(args, world, rank, local):
                 "peak": peaks["bf16_tflops_sustained"] if gemm else peaks["hbm_gbs"],
                 "unit": dk["unit"], "frac": dk["frac"], "traffic": traffic,
                 "peak_source": f"{peaks['source']} ({'bf16 sustained' if gemm else 'HBM copy'})"}
-    gemm_ms = sum(per_kind[k][1] for k in per_kind
-                  if k in ("gram", "gram_norm", "sqpoly", "xupdate", "xupdate_out")) / prof_steps
+    gemm_ms = sum(per_kind[k][1] for k in per_kind if k in GEMM_KINDS) / prof_steps
     mom_ms = per_kind.get("momentum", [1, 0.0])[1] / prof_steps
 
     # ---- the page's update tail after the step (equaliser + sign-aligned decay update
@@ -516,7 +516,7 @@ def run_anvil(args, world, rank, local):
                        "inputs": "matrices 0-10 N(0,0.02^2), 11-21 rank-32 + 1e-3 noise; pool of 4",
                        "scalars": "post-engage: momentum 0.95, fast_beta 0.85, fast_weight 0.4385, "
                                   "slow_beta 0.98",
-                       "maps": "6 ANVIL_MAPS", "graph": "one CUDA graph per step",
+                       "maps": "6 ANVIL_MAPS", "graph": "one CUDA graph per step (3 kernels)",
                        "l2": "inputs larger than L2 (grads 260 MB + rails 520 MB per step)",
                        "parallelism": f"replicas x{world}"},
             "tflops_algorithmic": alg / (ms_max / 1000.0) / 1e12 * world,
@@ -535,7 +535,7 @@ def run_anvil(args, world, rank, local):
 
 def run_ncu_case():
     """Two eager (non-graph) steps of the bench workload, one grad draw: a short program for
-    ncu captures (18 GEMM launches per step; the third of the second step is an X-update)."""
+    ncu captures (three launches per step: momentum, norm_d, the cascade)."""
     import torch
     from polynomial_matrix_whitening_gb300 import anvil
     dev = torch.device("cuda", 0)

@@ -21,10 +21,9 @@
  * Every number is computed on the GPU by this library's own kernels; there is
  * no CPU path.  All calls are asynchronous on the given stream (a
  * cudaStream_t / CUstream handle passed as void*; NULL = legacy default
- * stream).  One kernel of each step (the normalisation) runs on a second stream of the
- * library's, forked from and joined back to the caller's stream by events (a captured
- * graph holds it as a parallel branch).  No call below allocates, frees or
- * synchronises, except
+ * stream).  A step is three kernels on that stream: momentum + cast, the normaliser d,
+ * and one persistent kernel for the whole cascade (the normalisation and every product of
+ * every map).  No call below allocates, frees or synchronises, except
  * anvil_bank_step on its first use of a size (documented there) and the
  * diagnostic anvil_device_error.  Errors are returned as status codes; no
  * exception crosses the ABI.
@@ -215,7 +214,9 @@ typedef struct {
 } anvil_trace;
 
 /* anvil_multi_bank_step for one bank, plus the dumps.  Same arguments and
- * workspace rules; out receives the same result as without tracing. */
+ * workspace rules; out receives the same result as without tracing.  The cascade
+ * runs one phase per launch here (with the dumps copied out in between); a trace
+ * with every pointer NULL gives that phase-by-phase run without dumps. */
 anvil_status anvil_bank_step_traced(const anvil_bank_desc* bank, const anvil_scalars* d_scalars,
                                     const anvil_map* maps, int nmaps, float margin, float eps,
                                     void* workspace, size_t workspace_bytes,
@@ -243,7 +244,7 @@ anvil_status anvil_selftest_wait_timeout(unsigned timeout_us, void* stream);
 typedef enum {
     ANVIL_KERNEL_MOMENTUM = 0,     /* momentum + cast + diagonal partials */
     ANVIL_KERNEL_NORM_D = 1,       /* d per matrix */
-    ANVIL_KERNEL_NORMALIZE = 2,    /* X <- bf16(X / d), on the second stream */
+    ANVIL_KERNEL_NORMALIZE = 2,    /* X <- bf16(X / d) (traced runs: one launch per phase) */
     ANVIL_KERNEL_GRAM_NORM = 3,    /* first Gram, A = bf16(bf16(X X^T) / d^2) */
     ANVIL_KERNEL_GRAM = 4,         /* A = bf16(X X^T) */
     ANVIL_KERNEL_SQPOLY = 5,       /* B = bf16(b A + c A A) */
@@ -252,7 +253,8 @@ typedef enum {
     ANVIL_KERNEL_TAIL_POWER = 8,   /* update tail: lane powers */
     ANVIL_KERNEL_TAIL_SCALE = 9,   /* update tail: lane energies and scales */
     ANVIL_KERNEL_TAIL_APPLY = 10,  /* update tail: equalise + sign-aligned decay update */
-    ANVIL_KERNEL_ADAM = 11         /* Adam step */
+    ANVIL_KERNEL_ADAM = 11,        /* Adam step */
+    ANVIL_KERNEL_CASCADE = 12      /* every product phase of every map, one persistent launch */
 } anvil_kernel_kind;
 
 typedef struct { int kind; float ms; } anvil_profile_record;

@@ -31,7 +31,7 @@ STATUS = {0: "ANVIL_OK", 1: "ANVIL_ERR_INVALID_ARG", 2: "ANVIL_ERR_UNSUPPORTED_S
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_ALIGNMENT, ERR_ALIAS, ERR_WORKSPACE, \
     ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(9)
 KERNEL_KINDS = ("momentum", "norm_d", "normalize", "gram_norm", "gram", "sqpoly", "xupdate",
-                "xupdate_out", "tail_power", "tail_scale", "tail_apply", "adam")
+                "xupdate_out", "tail_power", "tail_scale", "tail_apply", "adam", "cascade")
 MAX_MAPS, MAX_BANKS = 16, 8
 
 

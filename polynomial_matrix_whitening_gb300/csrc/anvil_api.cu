@@ -2,16 +2,17 @@
 // workspace layout, TMA tensor maps, and the launch sequence of one ANVIL step
 // (page "modded-nanogpt track_1_short/optim/anvil.py", anvil_cascade):
 //
-//   momentum + cast (+ diagonal partials)   -> Y0 = X_raw
-//   d = sqrt(tr) * margin + eps             (tr from the bf16 diagonal of the first Gram)
-//   A = bf16(bf16(Y0 Y0^T) / d^2), then map 0's B     } on the caller's stream, while
-//   Y1 = bf16(Y0 / d)                                  } the second stream normalises
-//   map k = 0..nmaps-1, reading Y[(k+1)%2], writing Y[k%2] (out for the last map):
-//     [k > 0] A = bf16(Y Y^T);  B = bf16(b A + c A A);  Y' = bf16(a Y + B Y)
-//   (map 0's X-update waits for the normalisation)
+//   momentum + cast (+ diagonal partials)   -> Y0 = X_raw          (momentum_kernel)
+//   d = sqrt(tr) * margin + eps             (tr from the bf16 diagonal of the first Gram;
+//                                             norm_d_kernel, which also zeroes the
+//                                             cascade's completion counters)
+//   the cascade (cascade_kernel, one persistent launch over every phase):
+//     A = bf16(bf16(Y0 Y0^T) / d^2);  Y1 = bf16(Y0 / d)
+//     map k = 0..nmaps-1, reading Y[(k+1)%2], writing Y[k%2] (out for the last map):
+//       [k > 0] A = bf16(Y Y^T);  B = bf16(b A + c A A);  Y' = bf16(a Y + B Y)
 //
-// Every phase is one grouped launch over all banks of the call (GEMM phases: two when
-// more than four banks), 3 + 3 * nmaps launches in all.
+// Three launches per step for any number of banks; a traced step runs the cascade one
+// phase per launch and copies the intermediate values out between them.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -21,12 +22,16 @@
 #include <algorithm>
 #include <mutex>
 
+
 #include "../../include/anvil.h"
 #include "anvil_internal.h"
 #include "anvil_adam.h"
 #include "anvil_tail.h"
 
 using namespace anvil;
+
+static_assert(ANVIL_MAX_MAPS <= MAX_CASCADE_MAPS, "phase table too small for ANVIL_MAX_MAPS");
+static_assert(sizeof(CascadeParams) <= 32764, "cascade parameters exceed the kernel parameter limit");
 
 namespace {
 
@@ -53,8 +58,6 @@ struct DeviceState {
     anvil_status status = ANVIL_OK;
     unsigned* err = nullptr;
     int sm_count = 0;
-    cudaStream_t side = nullptr;  // the normalisation's stream
-    cudaEvent_t fork = nullptr, join = nullptr;
 };
 std::mutex g_dev_mutex;
 DeviceState g_dev[64];
@@ -99,10 +102,6 @@ anvil_status device_setup(DeviceState** out) {
             return cuda_fail(e, "cudaDeviceGetAttribute");
         st.err = device_error_word();
         if (!st.err) return cuda_fail(cudaGetLastError(), "cudaGetSymbolAddress(error word)");
-        if ((e = cudaStreamCreateWithFlags(&st.side, cudaStreamNonBlocking)) ||
-            (e = cudaEventCreateWithFlags(&st.fork, cudaEventDisableTiming)) ||
-            (e = cudaEventCreateWithFlags(&st.join, cudaEventDisableTiming)))
-            return cuda_fail(e, "stream/event creation");
         st.ready = true;
     }
     *out = &st;
@@ -147,7 +146,7 @@ struct Layout {
     Geom bank[ANVIL_MAX_BANKS];
     int nbanks, total_mats;
     size_t d_bytes, part_elems, y_elems, a_elems;
-    size_t off_d, off_part, off_y0, off_y1, off_a, off_b, total;
+    size_t off_d, off_cnt, off_part, off_y0, off_y1, off_a, off_b, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -182,7 +181,8 @@ anvil_status make_layout(const anvil_bank_desc* banks, int nbanks, Layout* L) {
         L->a_elems += static_cast<size_t>(b.g) * G.s_pad * G.s_pad;
     }
     L->off_d = 0;
-    L->off_part = align256(L->off_d + sizeof(float) * L->total_mats);
+    L->off_cnt = align256(L->off_d + sizeof(float) * L->total_mats);
+    L->off_part = align256(L->off_cnt + 2 * sizeof(unsigned) * L->total_mats);
     L->off_y0 = align256(L->off_part + sizeof(float) * L->part_elems);
     L->off_y1 = align256(L->off_y0 + 2 * L->y_elems);
     L->off_a = align256(L->off_y1 + 2 * L->y_elems);
@@ -255,7 +255,7 @@ struct BankPtrs {
     uint16_t* b;
     float* part;
     float* d;
-    CUtensorMap tm_yk[2], tm_yn[2], tm_a, tm_b, tm_at, tm_bt, tm_out;
+    CUtensorMap tm[TM_COUNT];
     bool out_tma;
 };
 
@@ -300,19 +300,16 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         B.part = reinterpret_cast<float*>(ws + L.off_part) + G.part_off;
         B.d = d_all + G.mat_begin;
         for (int k = 0; k < 2; ++k) {
-            if ((st = encode_map(&B.tm_yk[k], B.y[k], G.g, G.s_pad, G.L_pad, BK, TILE))) return st;
-            if ((st = encode_map(&B.tm_yn[k], B.y[k], G.g, G.s_pad, G.L_pad, BK, BK))) return st;
+            if ((st = encode_map(&B.tm[TM_YK0 + k], B.y[k], G.g, G.s_pad, G.L_pad, BK, TILE))) return st;
+            if ((st = encode_map(&B.tm[TM_YN0 + k], B.y[k], G.g, G.s_pad, G.L_pad, BK, BK))) return st;
         }
-        if ((st = encode_map(&B.tm_a, B.a, G.g, G.s_pad, G.s_pad, BK, TILE))) return st;
-        if ((st = encode_map(&B.tm_b, B.b, G.g, G.s_pad, G.s_pad, BK, TILE))) return st;
-        if ((st = encode_map(&B.tm_at, B.a, G.g, G.s_pad, G.s_pad, TILE, BK, false))) return st;
-        if ((st = encode_map(&B.tm_bt, B.b, G.g, G.s_pad, G.s_pad, TILE, BK, false))) return st;
-        // the last X-update stores `out` [g, m, n] by TMA when its rows are 16-byte aligned:
-        // wide banks as Y boxes {64, 128}, tall banks as transposed boxes {128, 64}
-        B.out_tma = (G.n % 8 == 0) && !(reinterpret_cast<uintptr_t>(banks[i].out) & 15);
-        if (B.out_tma &&
-            (st = encode_map(&B.tm_out, banks[i].out, G.g, G.m, G.n, G.tall ? TILE : BK,
-                             G.tall ? BK : TILE, !G.tall)))
+        if ((st = encode_map(&B.tm[TM_A], B.a, G.g, G.s_pad, G.s_pad, BK, TILE))) return st;
+        if ((st = encode_map(&B.tm[TM_B], B.b, G.g, G.s_pad, G.s_pad, BK, TILE))) return st;
+        // the last X-update of a wide bank stores `out` [g, m, n] by TMA (boxes of Y) when
+        // its rows are 16-byte aligned; tall banks (out = Y^T) and the rest take plain stores
+        memset(&B.tm[TM_OUT], 0, sizeof(CUtensorMap));
+        B.out_tma = !G.tall && (G.n % 8 == 0) && !(reinterpret_cast<uintptr_t>(banks[i].out) & 15);
+        if (B.out_tma && (st = encode_map(&B.tm[TM_OUT], banks[i].out, G.g, G.m, G.n, BK, TILE)))
             return st;
     }
 
@@ -364,24 +361,17 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
     np.margin = margin;
     np.eps = eps;
     np.d = d_all;
+    np.counters = reinterpret_cast<unsigned*>(ws + L.off_cnt);
     np.err = dev->err;
-    {
-        long long vecs = 0;
-        for (int i = 0; i < nbanks; ++i) {
-            const Geom& G = L.bank[i];
-            NormBank& N = np.bank[i];
-            N.y = P[i].y[0];
-            N.y_out = P[i].y[1];
-            N.part = P[i].part;
-            N.g = G.g;
-            N.s_pad = G.s_pad;
-            N.L_pad = G.L_pad;
-            N.nlb = G.nlb;
-            N.mat_begin = G.mat_begin;
-            N.vec_begin = vecs;
-            vecs += static_cast<long long>(G.g) * G.s_pad * G.L_pad / 8;
-        }
-        np.total_vecs = vecs;
+    for (int i = 0; i < nbanks; ++i) {
+        const Geom& G = L.bank[i];
+        NormBank& N = np.bank[i];
+        N.part = P[i].part;
+        N.g = G.g;
+        N.s_pad = G.s_pad;
+        N.L_pad = G.L_pad;
+        N.nlb = G.nlb;
+        N.mat_begin = G.mat_begin;
     }
     if ((e = profiled(ANVIL_KERNEL_NORM_D, stream, [&] { return launch_norm_d(np, stream); })))
         return cuda_fail(e, "norm_d launch");
@@ -395,7 +385,17 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
             return cuda_fail(e, "trace");
     }
 
-    // GEMM banks, heaviest tiles first within each launch group.
+    // ---- the cascade: every phase of every map in one persistent launch (one launch per
+    // phase when tracing, with the intermediate values copied out between them)
+    CascadeParams cparams;
+    CascadeParams* cp = &cparams;
+    memset(cp, 0, sizeof(*cp));
+    cp->nbanks = nbanks;
+    cp->sm_count = dev->sm_count;
+    cp->chain = reinterpret_cast<unsigned*>(ws + L.off_cnt);
+    cp->norm = cp->chain + L.total_mats;
+    cp->err = dev->err;
+    // banks in the call's order, heaviest tiles first (the first items of each phase)
     int order[ANVIL_MAX_BANKS];
     for (int i = 0; i < nbanks; ++i) order[i] = i;
     std::stable_sort(order, order + nbanks, [&](int x, int y) {
@@ -403,127 +403,113 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         const long long wy = static_cast<long long>(L.bank[y].s_pad) * L.bank[y].L_pad;
         return wx > wy;
     });
-
-    auto gemm_phase = [&](GemmOp op, int k, const anvil_map& mp) -> anvil_status {
-        for (int first = 0; first < nbanks; first += MAX_LAUNCH_BANKS) {
-            GemmParams gp;
-            memset(&gp, 0, sizeof(gp));
-            gp.a = mp.a;
-            gp.b = mp.b;
-            gp.c = mp.c;
-            gp.err = dev->err;
-            gp.sm_count = dev->sm_count;
-            int tiles = 0, nb = 0;
-            for (int q = first; q < nbanks && q < first + MAX_LAUNCH_BANKS; ++q, ++nb) {
-                const int i = order[q];
-                const Geom& G = L.bank[i];
-                const BankPtrs& B = P[i];
-                GemmBank& gb = gp.bank[nb];
-                // the first Gram reads X_raw (Y0); map k reads Y[(k+1)%2], writes Y[k%2]
-                const int cur = op == OP_GRAM_NORM ? 0 : ((k + 1) & 1);
-                gb.g = G.g;
-                gb.s_pad = G.s_pad;
-                gb.L_pad = G.L_pad;
-                gb.m = G.m;
-                gb.n = G.n;
-                gb.tall = G.tall;
-                gb.T = G.s_pad / PAIR;
-                gb.d = B.d;
-                switch (op) {
-                    case OP_GRAM:
-                    case OP_GRAM_NORM:
-                        gb.tm_a = B.tm_yk[cur];
-                        gb.tm_b = B.tm_yk[cur];
-                        gb.tm_d = B.tm_a;
-                        gb.tm_e = B.tm_at;
-                        gb.dst = B.a;
-                        gb.nt_n = gb.T;
-                        gb.tiles_per_mat = gb.T * (gb.T + 1) / 2;
-                        gb.num_kb = G.L_pad / BK;
-                        break;
-                    case OP_SQPOLY:
-                        gb.tm_a = B.tm_a;
-                        gb.tm_b = B.tm_a;
-                        gb.tm_c = B.tm_a;
-                        gb.tm_d = B.tm_b;
-                        gb.tm_e = B.tm_bt;
-                        gb.src = B.a;
-                        gb.dst = B.b;
-                        gb.nt_n = gb.T;
-                        gb.tiles_per_mat = gb.T * (gb.T + 1) / 2;
-                        gb.num_kb = G.s_pad / BK;
-                        break;
-                    case OP_XUPDATE:
-                    case OP_XUPDATE_OUT:
-                        gb.tm_a = B.tm_b;
-                        gb.tm_b = B.tm_yn[cur];
-                        gb.tm_c = B.tm_yk[cur];
-                        if (op == OP_XUPDATE) {
-                            gb.tm_d = B.tm_yk[cur ^ 1];
-                        } else if (B.out_tma) {
-                            gb.out_tma = 1;
-                            if (G.tall) gb.tm_e = B.tm_out;
-                            else gb.tm_d = B.tm_out;
-                        }
-                        gb.src = B.y[cur];
-                        gb.dst = op == OP_XUPDATE ? B.y[cur ^ 1] : banks[i].out;
-                        gb.nt_n = G.L_pad / gemm_tile_cols(op);
-                        gb.tiles_per_mat = gb.T * gb.nt_n;
-                        gb.num_kb = G.s_pad / BK;
-                        break;
+    for (int q = 0; q < nbanks; ++q) {
+        const int i = order[q];
+        const Geom& G = L.bank[i];
+        const BankPtrs& B = P[i];
+        CascadeBank& cb = cp->bank[q];
+        memcpy(cb.tm, B.tm, sizeof(cb.tm));
+        cb.a = B.a;
+        cb.b = B.b;
+        cb.out = banks[i].out;
+        cb.d = B.d;
+        cb.g = G.g;
+        cb.s_pad = G.s_pad;
+        cb.L_pad = G.L_pad;
+        cb.m = G.m;
+        cb.n = G.n;
+        cb.tall = G.tall;
+        cb.out_tma = B.out_tma ? 1 : 0;
+        cb.T = G.s_pad / PAIR;
+        cb.ntl = G.L_pad / PAIR;
+        cb.mat_begin = G.mat_begin;
+    }
+    // the phase list: GRAM_NORM, NORMALIZE, then per map k [GRAM], SQPOLY, XUPDATE; map k
+    // reads Y[(k+1)%2] and writes Y[k%2] (out for the last map)
+    {
+        unsigned chain_total[ANVIL_MAX_BANKS] = {0};  // chain signals per matrix so far
+        int items = 0, nph = 0;
+        auto add = [&](int op, int ma, int mb, int min, int mout, const anvil_map& mp, bool after_norm) {
+            CascadePhase& ph = cp->phase[nph++];
+            ph.op = op;
+            ph.map_a = ma;
+            ph.map_b = mb;
+            ph.map_in = min;
+            ph.map_out = mout;
+            ph.a = mp.a;
+            ph.b = mp.b;
+            ph.c = mp.c;
+            ph.item_begin = items;
+            int local = 0;
+            for (int q = 0; q < nbanks; ++q) {
+                const CascadeBank& cb = cp->bank[q];
+                const bool sym = op == OP_GRAM || op == OP_GRAM_NORM || op == OP_SQPOLY;
+                const int tpm = sym ? cb.T * (cb.T + 1) / 2 : cb.T * cb.ntl;
+                ph.bank_begin[q] = local;
+                local += cb.g * tpm;
+                if (op == OP_NORMALIZE) {
+                    ph.need_chain[q] = 0;
+                    ph.need_norm[q] = 0;
+                } else {
+                    ph.need_chain[q] = chain_total[q];
+                    ph.need_norm[q] = after_norm ? SIGNALS_PER_TILE * cb.T * cb.ntl : 0u;
+                    chain_total[q] += SIGNALS_PER_TILE * static_cast<unsigned>(tpm);
                 }
-                gb.tile_begin = tiles;
-                tiles += G.g * gb.tiles_per_mat;
             }
-            gp.nbanks = nb;
-            gp.total_tiles = tiles;
-            static const int kinds[5] = {ANVIL_KERNEL_GRAM, ANVIL_KERNEL_GRAM_NORM, ANVIL_KERNEL_SQPOLY,
-                                         ANVIL_KERNEL_XUPDATE, ANVIL_KERNEL_XUPDATE_OUT};
-            cudaError_t ee = profiled(kinds[op], stream, [&] { return launch_gemm(op, gp, stream); });
-            if (ee) return cuda_fail(ee, "gemm launch");
+            items += local;
+        };
+        const anvil_map none = {0.f, 0.f, 0.f};
+        add(OP_GRAM_NORM, TM_YK0, TM_YK0, -1, TM_A, none, false);
+        add(OP_NORMALIZE, -1, -1, TM_YK0, TM_YK1, none, false);
+        for (int k = 0; k < nmaps; ++k) {
+            const int cur = (k + 1) & 1;
+            const bool last = k == nmaps - 1;
+            if (k > 0) add(OP_GRAM, TM_YK0 + cur, TM_YK0 + cur, -1, TM_A, maps[k], false);
+            add(OP_SQPOLY, TM_A, TM_A, TM_A, TM_B, maps[k], false);
+            add(last ? OP_XUPDATE_OUT : OP_XUPDATE, TM_B, TM_YN0 + cur, TM_YK0 + cur,
+                last ? TM_OUT : TM_YK0 + (cur ^ 1), maps[k], k == 0);
         }
-        return ANVIL_OK;
+        cp->nphases = nph;
+        cp->phase[nph].item_begin = items;
+    }
+    auto run_phases = [&](int first, int end, int kind) -> anvil_status {
+        cp->first_phase = first;
+        cp->end_phase = end;
+        cudaError_t ee = profiled(kind, stream, [&] { return launch_cascade(*cp, stream); });
+        return ee ? cuda_fail(ee, "cascade launch") : ANVIL_OK;
     };
+    if (!trace) return run_phases(0, cp->nphases, ANVIL_KERNEL_CASCADE);
 
-    const anvil_map none = {0.f, 0.f, 0.f};
-    // normalisation (Y1 = bf16(Y0 / d)) on the second stream, beside the first Gram
-    if ((e = cudaEventRecord(dev->fork, stream)) || (e = cudaStreamWaitEvent(dev->side, dev->fork, 0)))
-        return cuda_fail(e, "fork");
-    if ((e = profiled(ANVIL_KERNEL_NORMALIZE, dev->side, [&] { return launch_normalize(np, dev->side); })))
-        return cuda_fail(e, "normalize launch");
-    if ((e = cudaEventRecord(dev->join, dev->side))) return cuda_fail(e, "join");
-    if ((st = gemm_phase(OP_GRAM_NORM, 0, none))) return st;
+    static const int kinds[6] = {ANVIL_KERNEL_GRAM, ANVIL_KERNEL_GRAM_NORM, ANVIL_KERNEL_SQPOLY,
+                                 ANVIL_KERNEL_XUPDATE, ANVIL_KERNEL_XUPDATE_OUT, ANVIL_KERNEL_NORMALIZE};
     const Geom& G0 = L.bank[0];
     const size_t nx1 = static_cast<size_t>(G0.g) * G0.m * G0.n;
     const size_t na1 = static_cast<size_t>(G0.g) * G0.s * G0.s;
-    for (int k = 0; k < nmaps; ++k) {
-        if (k > 0 && (st = gemm_phase(OP_GRAM, k, maps[k]))) return st;
-        if (trace && trace->A &&
+    for (int ph = 0, k = 0; ph < cp->nphases; ++ph) {
+        const int op = cp->phase[ph].op;
+        if ((st = run_phases(ph, ph + 1, kinds[op]))) return st;
+        if (op == OP_NORMALIZE && trace->X &&
+            (e = launch_extract_x(P[0].y[1], trace->X, G0.g, G0.m, G0.n, G0.tall, G0.s_pad, G0.L_pad,
+                                  stream)))
+            return cuda_fail(e, "trace");
+        if ((op == OP_GRAM || op == OP_GRAM_NORM) && trace->A &&
             (e = launch_extract_sq(P[0].a, trace->A + k * na1, G0.g, G0.s, G0.s_pad, stream)))
             return cuda_fail(e, "trace");
-        if ((st = gemm_phase(OP_SQPOLY, k, maps[k]))) return st;
-        if (trace && trace->B &&
+        if (op == OP_SQPOLY && trace->B &&
             (e = launch_extract_sq(P[0].b, trace->B + k * na1, G0.g, G0.s, G0.s_pad, stream)))
             return cuda_fail(e, "trace");
-        if (k == 0) {
-            // map 0's X-update is the first reader of the normalised X
-            if ((e = cudaStreamWaitEvent(stream, dev->join, 0))) return cuda_fail(e, "join");
-            if (trace && trace->X &&
-                (e = launch_extract_x(P[0].y[1], trace->X, G0.g, G0.m, G0.n, G0.tall, G0.s_pad,
-                                      G0.L_pad, stream)))
-                return cuda_fail(e, "trace");
-        }
-        const bool last = k == nmaps - 1;
-        if ((st = gemm_phase(last ? OP_XUPDATE_OUT : OP_XUPDATE, k, maps[k]))) return st;
-        if (trace && trace->X) {
-            if (last) {
-                if ((e = cudaMemcpyAsync(trace->X + (k + 1) * nx1, banks[0].out, 2 * nx1,
-                                         cudaMemcpyDeviceToDevice, stream)))
+        if (op == OP_XUPDATE || op == OP_XUPDATE_OUT) {
+            if (trace->X) {
+                if (op == OP_XUPDATE_OUT) {
+                    if ((e = cudaMemcpyAsync(trace->X + (k + 1) * nx1, banks[0].out, 2 * nx1,
+                                             cudaMemcpyDeviceToDevice, stream)))
+                        return cuda_fail(e, "trace");
+                } else if ((e = launch_extract_x(P[0].y[k & 1], trace->X + (k + 1) * nx1, G0.g, G0.m,
+                                                 G0.n, G0.tall, G0.s_pad, G0.L_pad, stream))) {
                     return cuda_fail(e, "trace");
-            } else if ((e = launch_extract_x(P[0].y[k & 1], trace->X + (k + 1) * nx1, G0.g,
-                                             G0.m, G0.n, G0.tall, G0.s_pad, G0.L_pad, stream))) {
-                return cuda_fail(e, "trace");
+                }
             }
+            ++k;
         }
     }
     return ANVIL_OK;

@@ -102,6 +102,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of the phase with this parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Waits until the phase with this parity completes, or gives up after `limit_ns`,
 // recording DEVERR_TIMEOUT.  Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err,
@@ -158,6 +170,10 @@ __device__ __forceinline__ void bulk_wait_read_but_one() {
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Waits until every committed bulk store but the two most recent has completed.
+__device__ __forceinline__ void bulk_wait_all_but_two() {
+    asm volatile("cp.async.bulk.wait_group 2;" ::: "memory");
+}
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy
 // (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -166,6 +182,21 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // Barrier over a subset of the CTA's warps (id 1..15; `count` threads, a multiple of 32).
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier over `count` threads that also ORs a flag across them: every thread gets
+// the same answer, so a group can leave a loop together.
+__device__ __forceinline__ bool named_barrier_or(int id, int count, bool flag) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "barrier.cta.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(flag ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 // ---- clusters (2-CTA pairs) -------------------------------------------------------------

@@ -3,8 +3,8 @@
 //     track_1_short/optim/anvil.py", anvil_cascade, first block), writing X in the
 //     small-side-major working layout and the per-64-block sums of squares of the bf16
 //     values, from which the first Gram's diagonal (hence the trace) is read;
-//   * norm_d_kernel: d = sqrt(tr) * FROBENIUS_MARGIN + FROBENIUS_EPS per matrix;
-//   * normalize_kernel: X <- bf16(X / d) into the other working buffer;
+//   * norm_d_kernel: d = sqrt(tr) * FROBENIUS_MARGIN + FROBENIUS_EPS per matrix (the
+//     division X / d itself is a phase of the cascade kernel, anvil_gemm.cu);
 //   * extraction kernels for the traced (parity-test) path and the wait self-test.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(256) norm_d_kernel(const __grid_constant__ Nor
         if (gm >= p.bank[i].mat_begin) bi = i;
     const NormBank& B = p.bank[bi];
     const int lm = gm - B.mat_begin;
+    if (threadIdx.x < 2) p.counters[threadIdx.x * p.total_mats + gm] = 0u;
     const float* part = B.part + static_cast<size_t>(lm) * B.nlb * B.s_pad;  // [nlb][s_pad]
     float acc = 0.f;
     for (int i = threadIdx.x; i < B.s_pad; i += blockDim.x) {
@@ -201,60 +202,6 @@ __global__ void __launch_bounds__(256) norm_d_kernel(const __grid_constant__ Nor
 
 cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream) {
     return launch_pdl(norm_d_kernel, dim3(p.total_mats), dim3(256), 0, stream, p);
-}
-
-// Y_out <- bf16(float(Y) / d) over 8-element (16-byte) vectors, grid-stride over all banks,
-// four vectors per thread per iteration (four 16-byte loads in flight).
-__device__ __forceinline__ uint4 normalize_vec(uint4 u, float d) {
-    uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float lo = __fdiv_rn(bf2f(static_cast<uint16_t>(w[q] & 0xffffu)), d);
-        const float hi = __fdiv_rn(bf2f(static_cast<uint16_t>(w[q] >> 16)), d);
-        w[q] = static_cast<uint32_t>(f2bf(lo)) | (static_cast<uint32_t>(f2bf(hi)) << 16);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-__global__ void __launch_bounds__(256) normalize_kernel(const __grid_constant__ NormParams p) {
-    pdl_allow_next();
-    pdl_wait_previous();
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long v0 = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-         v0 < p.total_vecs; v0 += 4 * stride) {
-        uint4 u[4];
-        const uint16_t* src[4];
-        uint16_t* dst[4];
-        float d[4];
-        bool in[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const long long v = v0 + k * stride;
-            in[k] = v < p.total_vecs;
-            if (!in[k]) continue;
-            int bi = 0;
-#pragma unroll 1
-            for (int i = 1; i < p.nbanks; ++i)
-                if (v >= p.bank[i].vec_begin) bi = i;
-            const NormBank& B = p.bank[bi];
-            const long long lv = v - B.vec_begin;
-            const long long per_mat = static_cast<long long>(B.s_pad) * B.L_pad / 8;
-            d[k] = p.d[B.mat_begin + static_cast<int>(lv / per_mat)];
-            src[k] = B.y + 8 * lv;
-            dst[k] = B.y_out + 8 * lv;
-            u[k] = __ldcs(reinterpret_cast<const uint4*>(src[k]));
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (in[k]) *reinterpret_cast<uint4*>(dst[k]) = normalize_vec(u[k], d[k]);
-    }
-}
-
-cudaError_t launch_normalize(const NormParams& p, cudaStream_t stream) {
-    long long blocks = (p.total_vecs + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
-    if (blocks < 1) blocks = 1;
-    return launch_pdl(normalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
 }
 
 // ---------------------------------------------------------------- tracing

@@ -1,38 +1,45 @@
-// anvil_gemm.cu -- the three contractions of every spectral map of the ANVIL cascade
-// (page "modded-nanogpt track_1_short/optim/anvil.py", anvil_cascade: the XTX / XXT,
-// ba_plus_cAA and baddbmm steps), as one batched tcgen05 GEMM kernel for sm_103a:
+// anvil_gemm.cu -- the ANVIL cascade (page "modded-nanogpt track_1_short/optim/anvil.py",
+// anvil_cascade: the XTX / XXT, ba_plus_cAA and baddbmm steps of every spectral map, and
+// the division of X by its normaliser) as ONE persistent tcgen05 kernel for sm_103a that
+// walks every phase of a step:
 //
-//   OP_GRAM / OP_GRAM_NORM : A  = bf16(Y Y^T)            [/ d^2 for the first Gram]
-//   OP_SQPOLY              : B  = bf16(b A + c A A)
-//   OP_XUPDATE(_OUT)       : Y' = bf16(a Y + B Y)        [written to out for the last map]
+//   OP_GRAM_NORM : A  = bf16(bf16(Y Y^T) / d^2)     (the first Gram, on X_raw)
+//   OP_NORMALIZE : Y1 = bf16(Y0 / d)                (no product: epilogue warps only)
+//   OP_GRAM      : A  = bf16(Y Y^T)
+//   OP_SQPOLY    : B  = bf16(b A + c A A)
+//   OP_XUPDATE   : Y' = bf16(a Y + B Y)             (OP_XUPDATE_OUT: the last, into out)
 //
-// in the small-side-major layout of anvil_internal.h.  A and B are symmetric, so the
-// Gram and the A A product compute only the upper-triangle 256x256 tiles and store each
-// off-diagonal tile twice (itself and its mirror).  A A contracts A's rows with A's
-// rows (A A = A A^T), so every operand is K-major except Y in the X-update, which is
-// read MN-major (contiguous along the output columns).
+// in the small-side-major layout of anvil_internal.h.  A and B are symmetric: the Gram
+// and A A compute only the upper-triangle 256x256 blocks and store each off-diagonal
+// block twice (itself, and its mirror).  A A contracts A's rows with A's rows (A A =
+// A A^T), so every operand is K-major except Y in the X-update, read MN-major.
 //
-// CTA pairs: the kernel runs in clusters of two CTAs on two SMs; each pair computes one
-// 256x256 output tile with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16).  CTA
-// rank r of the pair loads rows 128r..128r+127 of the tile's A operand and columns
-// 128r..128r+127 of its B operand, and holds output rows 128r.. in its own TMEM, so
-// each SM streams 32 KB of operands per 64-deep k-block for 2 x 128 x 256 x 64 MACs.
-// Persistent and warp-specialised: each pair walks output tiles in a snake order over
-// every matrix of up to four banks (heaviest bank first).  Warp 0 (one lane) issues TMA
-// loads into a STAGES-deep shared-memory ring, counted on the leader CTA's barrier;
-// warp 1 owns the TMEM allocation (in both CTAs) and, in the leader CTA only, issues the
-// MMAs into one of two 256-column fp32 accumulators and commits to both CTAs' barriers;
-// warps 2-5 of each CTA read the other accumulator back with tcgen05.ld (warp w owns
-// TMEM lanes 32 (w % 4) ..) and run the fused epilogue, so a tile's epilogue overlaps
-// the next tile's MMAs.
+// Work items.  An item is one 256x256 output tile of one matrix in one phase.  Items are
+// numbered phase by phase and handed to the persistent grid of CTA pairs in a snake
+// order, each pair visiting its items in increasing order.  An item loads nothing before
+// the phases it reads are complete for its matrix: every finished tile adds to a
+// per-matrix completion counter in global memory (a release add once the tile's stores
+// have landed) and an item's loads wait (acquire) until its matrix's counters reach the
+// totals its phase needs (the adds come from a publisher warp, so that no epilogue
+// thread waits for its own stores to drain).  A pair therefore moves on to the next
+// phase of one matrix while other matrices are still in the previous one, with no kernel
+// boundary between the phases.  Each phase of a matrix reads only what the phases before it wrote and
+// waits for all of them, which also orders every reuse of the A, B and Y buffers.
+// An epilogue never blocks on another pair's tile while its own last tile is still
+// unpublished, and the lowest-numbered unfinished item never waits, so the walk always
+// progresses (every pair of the grid is co-resident: one CTA per SM).
 //
-// The epilogue works by quarters of 64 output columns through two shared-memory
-// staging buffers: the epilogue input (A for sqpoly, Y for the X-update) arrives by
-// TMA into a 128x64 box (128-byte swizzle, conflict-free 16-byte reads), the result
-// is written back in place and leaves by TMA store; a transposed 64x128 box carries
-// the mirror tile of the symmetric products (and the last X-update of a tall bank,
-// whose output is X = Y^T).  The last X-update of a bank whose column count is not a
-// multiple of 8 writes `out` with plain bounds-checked stores instead.
+// CTA pairs.  Clusters of two CTAs on two SMs compute a tile with tcgen05.mma.cta_group::2
+// (M = 256, N = 256, K = 16): CTA rank r loads rows 128r.. of the tile's A operand and
+// columns 128r.. of its B operand (TMA, completions counted on the leader's barrier) and
+// holds output rows 128r.. in its TMEM.  Warp 0 (one lane) issues the TMA loads into a
+// 5-stage ring; warp 1 allocates 512 TMEM columns in both CTAs and, in the leader only,
+// issues the MMAs into one of two 256-column accumulators, committing to both CTAs'
+// barriers; warps 2-9 (two groups of four, one per column half) run the fused epilogue on
+// the other accumulator; warp 10 publishes finished tiles.  The epilogue input tile (A for B = bA + cAA, Y for the X-update
+// and the normalisation) arrives by TMA into 128x64 boxes (128-byte swizzle), is updated
+// in place with packed f32x2 arithmetic and leaves by TMA store; mirror tiles (and the
+// X^T output of tall banks) leave as plain stores, 64 contiguous bytes per warp.
 //
 // Every wait is bounded (anvil_device.cuh): a wait that gives up sets the device error
 // word and an abort flag; all roles stop, in-flight copies and MMAs are waited for
@@ -45,136 +52,288 @@
 
 namespace anvil {
 
-constexpr int SMEM_MAX = 227 * 1024;  // opt-in dynamic shared memory per block
-constexpr int QBOX = TILE * 64 * 2;   // one 128 x 64 bf16 staging box (16 KB)
-constexpr int EPI_GROUPS = 2;         // epilogue warp groups, one per half of the columns
-
-template <int OP>
-struct OpTraits {
-    static constexpr bool sym = (OP == OP_GRAM || OP == OP_GRAM_NORM || OP == OP_SQPOLY);
-    static constexpr bool xupdate = (OP == OP_XUPDATE || OP == OP_XUPDATE_OUT);
-    static constexpr bool has_in = (OP == OP_SQPOLY) || xupdate;   // epilogue reads a tile
-    static constexpr bool has_t = sym || OP == OP_XUPDATE_OUT;     // transposed staging box
-    static constexpr int BN = PAIR;                                // output columns per CTA
-    static constexpr int NQ = BN / 64;                             // quarters per tile
-    static constexpr int A_STAGE = TILE * BK * 2;                  // 16 KB: this CTA's A rows
-    static constexpr int B_STAGE = TILE * BK * 2;                  // 16 KB: this CTA's B half
-    static constexpr int STAGE = A_STAGE + B_STAGE;
-    // staging boxes (16 KB each): ops with an input stage the whole tile's input (one box
-    // per quarter, loaded as soon as the epilogue starts the tile) and update it in place;
-    // the Gram has one output box per epilogue group; mirrored / transposed outputs add
-    // one transposed box per group.
-    static constexpr int NDIR = has_in ? NQ : EPI_GROUPS;
-    static constexpr int NT = has_t ? EPI_GROUPS : 0;
-    static constexpr int STAGING = (NDIR + NT) * QBOX;
-    static constexpr int STAGES = (SMEM_MAX - 2048 - STAGING) / STAGE;
-    static constexpr int SMEM = STAGES * STAGE + STAGING + 1024;   // + alignment slack
-    static constexpr uint32_t TMEM_COLS = 2 * BN;                  // two accumulators
-};
-
+constexpr int SMEM_MAX = 227 * 1024;    // opt-in dynamic shared memory per block
+constexpr int QBOX = TILE * 64 * 2;     // one 128 x 64 bf16 staging box (16 KB)
+constexpr int NBOX = 4;                 // staging boxes: one per quarter of a CTA's tile
+constexpr int A_STAGE = TILE * BK * 2;  // 16 KB: this CTA's A rows of a k-block
+constexpr int B_STAGE = TILE * BK * 2;  // 16 KB: this CTA's B half of a k-block
+constexpr int STAGE = A_STAGE + B_STAGE;
+constexpr int STAGES = (SMEM_MAX - 2048 - NBOX * QBOX) / STAGE;  // 5
+constexpr int GEMM_SMEM = STAGES * STAGE + NBOX * QBOX + 1024;   // + alignment slack
+constexpr int BN = PAIR;     // output columns per CTA
+constexpr int NQ = BN / 64;  // quarters (64 columns) per tile
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int EPI_GROUPS = 2;
+constexpr int PUB_DEPTH = 4;  // completion messages in flight per epilogue group
 // warp 0: TMA producer; warp 1: TMEM owner and MMA issuer; warps 2-9: epilogue, in two
-// groups of four (one warp per TMEM lane quadrant), group h owning quarters 2h, 2h+1.
-constexpr int GEMM_THREADS = 64 + EPI_GROUPS * 128;
+// groups of four (one warp per TMEM lane quadrant), group h owning quarters 2h, 2h+1;
+// warp 10: publisher of finished tiles.
+constexpr int PUB_WARP = 2 + EPI_GROUPS * 4;
+constexpr int GEMM_THREADS = 32 * (PUB_WARP + 1);
 
-__device__ __forceinline__ void load32_bf16(const uint16_t* src, float (&f)[32]) {
-    const uint4* p = reinterpret_cast<const uint4*>(src);
-    uint4 u[4];
-#pragma unroll
-    for (int v = 0; v < 4; ++v) u[v] = p[v];
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-        const uint32_t w[4] = {u[v].x, u[v].y, u[v].z, u[v].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            f[8 * v + 2 * q] = bf2f(static_cast<uint16_t>(w[q] & 0xffffu));
-            f[8 * v + 2 * q + 1] = bf2f(static_cast<uint16_t>(w[q] >> 16));
-        }
-    }
+__host__ __device__ constexpr bool op_sym(int op) {
+    return op == OP_GRAM || op == OP_GRAM_NORM || op == OP_SQPOLY;
 }
-
-__device__ __forceinline__ void store32_bf16(uint16_t* dst, const uint16_t (&o)[32]) {
-    uint4* p = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            w[q] = static_cast<uint32_t>(o[8 * v + 2 * q]) |
-                   (static_cast<uint32_t>(o[8 * v + 2 * q + 1]) << 16);
-        p[v] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+__host__ __device__ constexpr bool op_xupdate(int op) {
+    return op == OP_XUPDATE || op == OP_XUPDATE_OUT;
 }
+__host__ __device__ constexpr bool op_gram(int op) { return op == OP_GRAM || op == OP_GRAM_NORM; }
 
-struct TileCoord {
-    int bi, mat, ti, tj;
+struct Item {
+    int ph, bank, mat, bi, bj;
 };
 
-// The k-th tile of pair c in a persistent grid of G pairs: tiles are handed out in rounds
-// of G, alternating direction (a snake), so the heavy tiles at the front of the order
-// spread evenly.  Returns >= total when the pair has no k-th tile.
-__device__ __forceinline__ int snake_tile(int k, int c, int G) {
+// The k-th item of pair c in a persistent grid of G pairs: items are handed out in
+// rounds of G, alternating direction (a snake), so each pair's items increase with k.
+__device__ __forceinline__ int snake_item(int k, int c, int G) {
     return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
-// Tile t of the grouped launch -> (bank, matrix, row block, column block), in 256s.
-template <int OP>
-__device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
-    TileCoord c;
-    c.bi = 0;
+// Item t (an index into the call's item list) -> phase, bank, matrix, block row and
+// column.  `ph` is the caller's phase cursor: items are visited in increasing order.
+__device__ __forceinline__ Item decode_item(const CascadeParams& p, int t, int& ph) {
+    while (ph + 1 < p.end_phase && t >= p.phase[ph + 1].item_begin) ++ph;
+    const CascadePhase& P = p.phase[ph];
+    int local = t - P.item_begin;
+    int bi = 0;
 #pragma unroll 1
     for (int i = 1; i < p.nbanks; ++i)
-        if (t >= p.bank[i].tile_begin) c.bi = i;
-    const GemmBank& bk = p.bank[c.bi];
-    const int local = t - bk.tile_begin;
-    c.mat = local / bk.tiles_per_mat;
-    int r = local - c.mat * bk.tiles_per_mat;
-    if (OpTraits<OP>::sym) {
-        c.ti = 0;
-        while (r >= bk.T - c.ti) {
-            r -= bk.T - c.ti;
-            ++c.ti;
+        if (local >= P.bank_begin[i]) bi = i;
+    local -= P.bank_begin[bi];
+    const CascadeBank& B = p.bank[bi];
+    Item it;
+    it.ph = ph;
+    it.bank = bi;
+    const int T = B.T;
+    const bool sym = op_sym(P.op);
+    const int tpm = sym ? T * (T + 1) / 2 : T * B.ntl;
+    it.mat = local / tpm;
+    int r = local - it.mat * tpm;
+    if (sym) {
+        int ti = 0;
+        while (r >= T - ti) {
+            r -= T - ti;
+            ++ti;
         }
-        c.tj = c.ti + r;
+        it.bi = ti;
+        it.bj = ti + r;
     } else {
-        c.ti = r / bk.nt_n;
-        c.tj = r - c.ti * bk.nt_n;
+        it.bi = r / B.ntl;
+        it.bj = r - it.bi * B.ntl;
     }
-    return c;
+    return it;
 }
 
-// The elementwise part of each op's epilogue, on fp32 accumulator value v and (where
-// the op has one) the bf16 input value x at the same position.
-template <int OP>
-__device__ __forceinline__ uint16_t epi_value(const GemmParams& p, float v, float x, float dd) {
-    if (OP == OP_GRAM) return f2bf(v);
-    if (OP == OP_GRAM_NORM) return f2bf(__fdiv_rn(round_bf(v), dd));  // bf16(bf16(acc) / d^2)
-    if (OP == OP_SQPOLY) return f2bf(__fadd_rn(__fmul_rn(p.b, x), __fmul_rn(p.c, v)));
-    return f2bf(__fadd_rn(__fmul_rn(p.a, x), v));                   // a Y + acc
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
-// The same on a pair: accumulator values v (packed fp32 pair), input word xw (two bf16);
-// returns two bf16.  Rounding is identical to epi_value (each product and sum rounded).
+// Whether the phases item `it` reads are complete for its matrix (no wait).
+__device__ __forceinline__ bool deps_ready(const CascadeParams& p, const Item& it) {
+    const CascadePhase& P = p.phase[it.ph];
+    const unsigned nc = P.need_chain[it.bank], nn = P.need_norm[it.bank];
+    const int m = p.bank[it.bank].mat_begin + it.mat;
+    if (nc && ld_acquire(p.chain + m) < nc) return false;
+    if (nn && ld_acquire(p.norm + m) < nn) return false;
+    return true;
+}
+
+// Waits (bounded) for the same; then orders this thread's later TMA loads after it.
+__device__ __forceinline__ bool deps_wait(const CascadeParams& p, const Item& it) {
+    if (!deps_ready(p, it)) {
+        const unsigned long long t0 = globaltimer_ns();
+        for (uint32_t i = 1;; ++i) {
+            __nanosleep(100);
+            if (deps_ready(p, it)) break;
+            if ((i & 15u) == 0 && globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                atomicOr(p.err, DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
+}
+
+// The completion counter a finished tile adds to.
+__device__ __forceinline__ unsigned* tile_counter(const CascadeParams& p, const Item& it) {
+    return (p.phase[it.ph].op == OP_NORMALIZE ? p.norm : p.chain) + p.bank[it.bank].mat_begin + it.mat;
+}
+
+// The elementwise part of each op's epilogue on a pair: accumulator values v (packed fp32
+// pair) and input word xw (two bf16); returns two bf16.  Each product and sum is rounded
+// on its own (the page's fp32 tensor operations one at a time); divisions are correctly
+// rounded.
 template <int OP>
 __device__ __forceinline__ uint32_t epi_pair(uint64_t v, uint32_t xw, uint64_t coef_x,
                                              uint64_t coef_v, float dd) {
     if (OP == OP_GRAM) return f2_to_bf2(v);
-    if (OP == OP_GRAM_NORM) {
-        // bf16(bf16(acc) / d^2), the quotient correctly rounded in fp32
+    if (OP == OP_GRAM_NORM) {  // bf16(bf16(acc) / d^2)
         const float lo = __fdiv_rn(round_bf(__uint_as_float(static_cast<uint32_t>(v))), dd);
         const float hi = __fdiv_rn(round_bf(__uint_as_float(static_cast<uint32_t>(v >> 32))), dd);
         return f2_to_bf2(f2_pack(lo, hi));
     }
-    const uint64_t t = f2_mul(coef_x, bf2_to_f2(xw));  // b A  or  a Y
+    if (OP == OP_NORMALIZE) {  // bf16(Y / d)
+        const float lo = __fdiv_rn(bf2f(static_cast<uint16_t>(xw & 0xffffu)), dd);
+        const float hi = __fdiv_rn(bf2f(static_cast<uint16_t>(xw >> 16)), dd);
+        return f2_to_bf2(f2_pack(lo, hi));
+    }
+    const uint64_t t = f2_mul(coef_x, bf2_to_f2(xw));                     // b A  or  a Y
     if (OP == OP_SQPOLY) return f2_to_bf2(f2_add(t, f2_mul(coef_v, v)));  // + c acc
-    return f2_to_bf2(f2_add(t, v));                                          // + acc
+    return f2_to_bf2(f2_add(t, v));                                       // + acc
 }
 
+__device__ __forceinline__ uint16_t half_of(const uint32_t (&o)[4], int e) {
+    return static_cast<uint16_t>((e & 1) ? (o[e >> 1] >> 16) : (o[e >> 1] & 0xffffu));
+}
+
+// Per-thread epilogue state of one group.
+struct EpiCtx {
+    uint8_t* stg;        // staging boxes
+    uint64_t* epi_bar;   // input-load barriers, one per quarter
+    int r;               // row of the CTA's tile this thread owns
+    int grp, lane;
+    bool leader;         // lane 0 of the group's first warp
+    int last_box;        // staging box of the group's latest TMA store (-1: none)
+    bool fail;           // one of this thread's waits gave up
+    int npub;            // completion messages sent to the publisher
+};
+
+// A release add makes this thread wait for its own stores in flight, so the epilogue
+// hands each finished tile to the publisher warp instead: the group leader, once the
+// tile's TMA stores have completed (and after the group barrier that follows its plain
+// stores), writes the counter's address into a mailbox slot and arrives on the slot's
+// barrier (release, CTA scope); the publisher acquires it and performs the release add
+// at GPU scope.  A null address ends the group's messages.
+struct Mailbox {
+    uint64_t full[EPI_GROUPS][PUB_DEPTH];
+    uint64_t empty[EPI_GROUPS][PUB_DEPTH];
+    unsigned* slot[EPI_GROUPS][PUB_DEPTH];
+};
+
+__device__ __forceinline__ void send_done(Mailbox& mb, EpiCtx& x, unsigned* cnt, unsigned* err) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");  // the tile's TMA stores, then the message
+    const int k = x.npub++;
+    const int s = k % PUB_DEPTH;
+    if (!mbar_wait(&mb.empty[x.grp][s], ((k / PUB_DEPTH) & 1) ^ 1, err)) x.fail = true;
+    mb.slot[x.grp][s] = cnt;
+    mbar_arrive_cta(&mb.full[x.grp][s]);
+}
+
+// The quarters of one tile that this thread's group owns: read the accumulator (tbase:
+// TMEM address of the thread's lane quadrant in the accumulator; unused by NORMALIZE),
+// combine with the input box, store.  tempty: the leader CTA's barrier for this
+// accumulator.  A wait that gives up sets x.fail and the tile runs to its end all the
+// same (its values are then meaningless), so every thread of the group reaches every
+// group barrier.
 template <int OP>
-__global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
-    using TR = OpTraits<OP>;
-    constexpr int BN = TR::BN;
-    constexpr int STAGES = TR::STAGES;
-    constexpr int NQ = TR::NQ;
+__device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBank& bk,
+                                         const CascadePhase& P, const Item& c, uint32_t rank,
+                                         EpiCtx& x, uint32_t tbase, uint32_t tempty, uint32_t in_phase) {
+    constexpr bool has_acc = OP != OP_NORMALIZE;
+    constexpr bool has_in = !op_gram(OP);
+    constexpr bool sym = op_sym(OP);
+    const int row0 = c.bi * PAIR + TILE * static_cast<int>(rank);  // this CTA's first row
+    const int col0 = c.bj * PAIR;
+    const int r = x.r;
+    // the direct tile leaves by TMA except the last X-update into an `out` that cannot
+    // take it (a tall bank's X = Y^T, or rows not 16-byte aligned)
+    const bool tma_direct = OP != OP_XUPDATE_OUT || bk.out_tma;
+    const bool mirror = sym && c.bi != c.bj;
+    const uint64_t coef_x = f2_pack(OP == OP_SQPOLY ? P.b : P.a, OP == OP_SQPOLY ? P.b : P.a);
+    const uint64_t coef_v = f2_pack(P.c, P.c);
+    float dd = 0.f;
+    if (OP == OP_GRAM_NORM) {
+        const float d = bk.d[c.mat];
+        dd = __fmul_rn(d, d);
+    } else if (OP == OP_NORMALIZE) {
+        dd = bk.d[c.mat];
+    }
+    uint16_t* const sym_dst = OP == OP_SQPOLY ? bk.b : bk.a;
+    for (int q = 2 * x.grp; q < 2 * x.grp + 2; ++q) {
+        int box = q;
+        if (!has_in) {
+            // a free Gram output box: not the one of the latest store, and every older
+            // store has finished reading its box
+            box = x.last_box == 2 * x.grp ? 2 * x.grp + 1 : 2 * x.grp;
+            if (x.leader) bulk_wait_read_but_one();
+            named_barrier_sync(1 + x.grp, 128);
+        } else if (!mbar_wait(&x.epi_bar[q], in_phase, p.err)) {
+            x.fail = true;
+        }
+        uint8_t* drow = x.stg + box * QBOX + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            float v[32];
+            if (has_acc) tmem_ld_32x32b_x32(tbase + q * 64 + cc * 32, v);
+            const int cb = col0 + q * 64 + cc * 32;  // first column of this chunk
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                // 16-byte chunk j of this 128-byte row sits at chunk j ^ (r % 8)
+                const int j = cc * 4 + w;
+                uint4* cp = reinterpret_cast<uint4*>(drow + ((j ^ (r & 7)) << 4));
+                uint32_t xw[4] = {0u, 0u, 0u, 0u};
+                if (has_in) {
+                    const uint4 u = *cp;
+                    xw[0] = u.x; xw[1] = u.y; xw[2] = u.z; xw[3] = u.w;
+                }
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    o[e] = epi_pair<OP>(has_acc ? f2_pack(v[8 * w + 2 * e], v[8 * w + 2 * e + 1]) : 0ull,
+                                        xw[e], coef_x, coef_v, dd);
+                if (tma_direct) *cp = make_uint4(o[0], o[1], o[2], o[3]);
+                const int c8 = cb + 8 * w;  // column of o[0]'s low half
+                if (sym) {
+                    if (mirror) {
+                        // element (row0 + r, c8 + e) -> (c8 + e, row0 + r): the 32 lanes of a
+                        // warp write 64 contiguous bytes per element
+                        uint16_t* base = sym_dst + static_cast<size_t>(c.mat) * bk.s_pad * bk.s_pad +
+                                         row0 + r;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            base[static_cast<size_t>(c8 + e) * bk.s_pad] = half_of(o, e);
+                    }
+                } else if (OP == OP_XUPDATE_OUT && !tma_direct) {
+                    uint16_t* out = bk.out + static_cast<size_t>(c.mat) * bk.m * bk.n;
+                    if (bk.tall) {
+                        // X = Y^T: element (row0 + r, c8 + e) -> out row c8 + e, column row0 + r
+                        if (row0 + r < bk.n) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                if (c8 + e < bk.m)
+                                    out[static_cast<size_t>(c8 + e) * bk.n + row0 + r] = half_of(o, e);
+                        }
+                    } else if (row0 + r < bk.m) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if (c8 + e < bk.n)
+                                out[static_cast<size_t>(row0 + r) * bk.n + c8 + e] = half_of(o, e);
+                    }
+                }
+            }
+        }
+        if (has_acc && q == 2 * x.grp + 1) {
+            // the accumulator is free once every epilogue warp of both CTAs has read it
+            tc_fence_before();
+            __syncwarp();
+            if (x.lane == 0) mbar_arrive_cluster(tempty);
+        }
+        fence_proxy_async_smem();
+        named_barrier_sync(1 + x.grp, 128);
+        if (tma_direct) {
+            if (x.leader) {
+                tma_store_3d(&bk.tm[P.map_out], x.stg + box * QBOX, col0 + 64 * q, row0, c.mat);
+                bulk_commit_group();
+            }
+            x.last_box = box;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_constant__ CascadeParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];
     __shared__ __align__(8) uint64_t empty_bar[STAGES];
@@ -182,6 +341,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     __shared__ __align__(8) uint64_t tempty_bar[2];
     __shared__ __align__(8) uint64_t mma_done_bar;
     __shared__ __align__(8) uint64_t epi_bar[NQ];  // epilogue input loads, one per quarter
+    __shared__ __align__(8) Mailbox mbox;
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int aborted;
 
@@ -189,6 +349,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the MMAs), 1 = peer
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int item0 = p.phase[p.first_phase].item_begin;
+    const int nitems = p.phase[p.end_phase].item_begin - item0;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
@@ -202,82 +364,105 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             mbar_init(&tempty_bar[b], 2 * 4 * EPI_GROUPS);  // each epilogue warp, both CTAs
         }
         for (int q = 0; q < NQ; ++q) mbar_init(&epi_bar[q], 1);
+        for (int g = 0; g < EPI_GROUPS; ++g)
+            for (int s = 0; s < PUB_DEPTH; ++s) {
+                mbar_init(&mbox.full[g][s], 1);
+                mbar_init(&mbox.empty[g][s], 1);
+            }
         mbar_init(&mma_done_bar, 1);
         fence_mbar_init();
         aborted = 0;
     }
     if (threadIdx.x == 32) {
-        for (int i = 0; i < p.nbanks; ++i) {
-            tma_prefetch_desc(&p.bank[i].tm_a);
-            tma_prefetch_desc(&p.bank[i].tm_b);
-            if (TR::has_in) tma_prefetch_desc(&p.bank[i].tm_c);
-            tma_prefetch_desc(&p.bank[i].tm_d);
-            if (TR::has_t) tma_prefetch_desc(&p.bank[i].tm_e);
-        }
+        for (int i = 0; i < p.nbanks; ++i)
+            for (int k = 0; k < TM_COUNT; ++k)
+                if (k != TM_OUT || p.bank[i].out_tma) tma_prefetch_desc(&p.bank[i].tm[k]);
     }
-    if (warp == 1) tmem_alloc_pair(&tmem_slot, TR::TMEM_COLS);
+    if (warp == 1) tmem_alloc_pair(&tmem_slot, TMEM_COLS);
     tc_fence_before();
     cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
     tc_fence_after();
     pdl_wait_previous();  // everything above overlapped the previous kernel's tail
     const uint32_t tmem = tmem_slot;
-    int issued = 0;        // producer: k-blocks whose loads were armed (in the whole CTA life)
-    int epi_tiles = 0;     // epilogue: tiles whose input staging loads were armed
+    int issued = 0;      // producer: k-blocks whose loads were armed (in the whole CTA life)
+    int epi_tiles = 0;   // epilogue group: tiles whose input loads were armed
 
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer
-            int it = 0;
+            int it = 0, ph = p.first_phase;
             for (int k = 0;; ++k) {
-                const int t = snake_tile(k, pair, npairs);
-                if (t >= p.total_tiles || aborted) break;
-                const TileCoord c = decode_tile<OP>(p, t);
-                const GemmBank& bk = p.bank[c.bi];
-                const int arow = c.ti * PAIR + TILE * rank;  // this CTA's A rows
-                const int bofs = c.tj * PAIR + TILE * rank;  // this CTA's B rows (or Y columns)
-                for (int kb = 0; kb < bk.num_kb; ++kb, ++it) {
+                const int t = snake_item(k, pair, npairs);
+                if (t >= nitems || aborted) break;
+                const Item c = decode_item(p, item0 + t, ph);
+                const CascadePhase& P = p.phase[c.ph];
+                if (P.op == OP_NORMALIZE) continue;
+                const CascadeBank& bk = p.bank[c.bank];
+                if (!deps_wait(p, c)) {
+                    aborted = 1;
+                    break;
+                }
+                const bool xu = op_xupdate(P.op);
+                const CUtensorMap* tma = &bk.tm[P.map_a];
+                const CUtensorMap* tmb = &bk.tm[P.map_b];
+                const int nkb = (op_gram(P.op) ? bk.L_pad : bk.s_pad) / BK;
+                const int arow = c.bi * PAIR + TILE * static_cast<int>(rank);  // this CTA's A rows
+                const int bofs = c.bj * PAIR + TILE * static_cast<int>(rank);  // its B rows / Y columns
+                bool ok = true;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t r = static_cast<uint32_t>(it / STAGES);
                     if (!mbar_wait(&empty_bar[s], (r & 1u) ^ 1u, p.err)) {
-                        aborted = 1;
+                        ok = false;
                         break;
                     }
-                    uint8_t* sa = smem + s * TR::STAGE;
-                    uint8_t* sb = sa + TR::A_STAGE;
+                    uint8_t* sa = smem + s * STAGE;
+                    uint8_t* sb = sa + A_STAGE;
                     // both CTAs' bytes complete on the leader's barrier of this stage
                     const uint32_t fb = map_to_rank(&full_bar[s], 0);
-                    if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * TR::STAGE);
-                    tma_load_3d_pair(sa, &bk.tm_a, fb, kb * BK, arow, c.mat);
-                    if (TR::xupdate) {
+                    if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * STAGE);
+                    tma_load_3d_pair(sa, tma, fb, kb * BK, arow, c.mat);
+                    if (xu) {
                         // Y rows kb*64 .. +63 (the contraction index), this CTA's 128 of the
                         // tile's columns in two 64-column boxes: MN-major chunks 8 KB apart.
-                        tma_load_3d_pair(sb, &bk.tm_b, fb, bofs, kb * BK, c.mat);
-                        tma_load_3d_pair(sb + 8192, &bk.tm_b, fb, bofs + 64, kb * BK, c.mat);
+                        tma_load_3d_pair(sb, tmb, fb, bofs, kb * BK, c.mat);
+                        tma_load_3d_pair(sb + 8192, tmb, fb, bofs + 64, kb * BK, c.mat);
                     } else {
-                        tma_load_3d_pair(sb, &bk.tm_b, fb, kb * BK, bofs, c.mat);
+                        tma_load_3d_pair(sb, tmb, fb, kb * BK, bofs, c.mat);
                     }
                     issued = it + 1;
+                }
+                if (!ok) {
+                    aborted = 1;
+                    break;
                 }
             }
         }
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             // ---------------- MMA issuer (leader CTA)
-            constexpr uint32_t idesc = idesc_bf16_f32(PAIR, PAIR, false, TR::xupdate);
-            int it = 0;
+            constexpr uint32_t idesc_kk = idesc_bf16_f32(PAIR, PAIR, false, false);
+            constexpr uint32_t idesc_kn = idesc_bf16_f32(PAIR, PAIR, false, true);
+            int it = 0, mt = 0, ph = p.first_phase;
             for (int lt = 0;; ++lt) {
-                const int t = snake_tile(lt, pair, npairs);
-                if (t >= p.total_tiles || aborted) break;
-                const TileCoord c = decode_tile<OP>(p, t);
-                const int nkb = p.bank[c.bi].num_kb;
-                const int ab = lt & 1;
-                const uint32_t u = static_cast<uint32_t>(lt >> 1);
+                const int t = snake_item(lt, pair, npairs);
+                if (t >= nitems || aborted) break;
+                const Item c = decode_item(p, item0 + t, ph);
+                const CascadePhase& P = p.phase[c.ph];
+                if (P.op == OP_NORMALIZE) continue;
+                const CascadeBank& bk = p.bank[c.bank];
+                const bool xu = op_xupdate(P.op);
+                const int nkb = (op_gram(P.op) ? bk.L_pad : bk.s_pad) / BK;
+                const int ab = mt & 1;
+                const uint32_t u = static_cast<uint32_t>(mt >> 1);
+                ++mt;
                 if (!mbar_wait(&tempty_bar[ab], (u & 1u) ^ 1u, p.err)) {
                     aborted = 1;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t dacc = tmem + static_cast<uint32_t>(ab * BN);
+                const uint32_t idesc = xu ? idesc_kn : idesc_kk;
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % STAGES;
@@ -287,13 +472,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(smem + s * TR::STAGE);
-                    const uint32_t b0 = a0 + TR::A_STAGE;
+                    const uint32_t a0 = smem_u32(smem + s * STAGE);
+                    const uint32_t b0 = a0 + A_STAGE;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                        const uint64_t bd = TR::xupdate ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
-                                                        : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                        const uint64_t bd = xu ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
+                                               : smem_desc_sw128(b0 + kk * 32, 16, 1024);
                         umma_bf16_pair(dacc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     umma_commit_pair(&empty_bar[s], 3);  // frees stage s in both CTAs
@@ -311,158 +496,128 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
             // peer CTA: its TMEM is written by the leader's MMAs; wait for the last one
             mbar_wait(&mma_done_bar, 0, p.err);
         }
+    } else if (warp == PUB_WARP) {
+        if (lane == 0) {
+            // ---------------- publisher: one release add per finished tile and group
+            int k[EPI_GROUPS] = {0, 0};
+            int open = EPI_GROUPS;
+            unsigned long long t0 = globaltimer_ns();
+            while (open > 0) {
+                bool got = false;
+                for (int g = 0; g < EPI_GROUPS; ++g) {
+                    if (k[g] < 0) continue;
+                    const int s = k[g] % PUB_DEPTH;
+                    if (!mbar_test_wait(smem_u32(&mbox.full[g][s]), (k[g] / PUB_DEPTH) & 1)) continue;
+                    unsigned* cnt = mbox.slot[g][s];
+                    if (cnt) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(cnt) : "memory");
+                    mbar_arrive_cta(&mbox.empty[g][s]);
+                    k[g] = cnt ? k[g] + 1 : -1;
+                    if (!cnt) --open;
+                    got = true;
+                }
+                if (got) {
+                    t0 = globaltimer_ns();
+                } else {
+                    __nanosleep(128);
+                    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+                        atomicOr(p.err, DEVERR_TIMEOUT);
+                        aborted = 1;
+                        break;
+                    }
+                }
+            }
+        }
     } else {
         // ---------------- epilogue: warps 2-9, TMEM lane quadrant = warp % 4
         const int quad = warp & 3;
-        const int grp = (warp - 2) >> 2;          // column half of this warp group
-        const int r = quad * 32 + lane;           // row within the tile
-        const bool leader = ((warp - 2) & 3) == 0 && lane == 0;
-        uint8_t* stg = smem + STAGES * TR::STAGE;  // staging boxes (1024-aligned)
+        EpiCtx x;
+        x.stg = smem + STAGES * STAGE;  // staging boxes (1024-aligned)
+        x.epi_bar = epi_bar;
+        x.r = quad * 32 + lane;
+        x.grp = (warp - 2) >> 2;
+        x.lane = lane;
+        x.leader = ((warp - 2) & 3) == 0 && lane == 0;
+        x.last_box = -1;
+        x.fail = false;
+        x.npub = 0;
         const uint32_t tempty_leader0 = map_to_rank(&tempty_bar[0], 0);
         const uint32_t tempty_leader1 = map_to_rank(&tempty_bar[1], 0);
-        const uint64_t coef_x = f2_pack(OP == OP_SQPOLY ? p.b : p.a, OP == OP_SQPOLY ? p.b : p.a);
-        const uint64_t coef_v = f2_pack(p.c, p.c);
+        int ph = p.first_phase, mt = 0;
+        bool pending = false;  // the group's latest tile, published after the next one
+        Item pend = {0, 0, 0, 0, 0};
         for (int lt = 0;; ++lt) {
-            const int t = snake_tile(lt, pair, npairs);
-            if (t >= p.total_tiles || aborted) break;
-            const TileCoord c = decode_tile<OP>(p, t);
-            const GemmBank& bk = p.bank[c.bi];
-            const int ab = lt & 1;
-            const uint32_t u = static_cast<uint32_t>(lt >> 1);
-            const int row0 = c.ti * PAIR + TILE * rank;  // this CTA's first output row
-            const int col0 = c.tj * PAIR;                // first column
-            // what this tile stores: the tile itself, and/or its transpose
-            const bool to_direct = TR::sym || OP == OP_XUPDATE || (OP == OP_XUPDATE_OUT && !bk.tall);
-            const bool to_mirror = (TR::sym && c.ti != c.tj) || (OP == OP_XUPDATE_OUT && bk.tall);
-            const bool staged = OP != OP_XUPDATE_OUT || bk.out_tma;
-            float dd = 0.f;
-            if (OP == OP_GRAM_NORM) {
-                const float d = bk.d[c.mat];
-                dd = __fmul_rn(d, d);
+            // the group stops together: at its last item, or once any wait of any role
+            // (or of any thread of the group) gave up
+            if (named_barrier_or(1 + x.grp, 128, x.fail || aborted)) {
+                aborted = 1;
+                break;
             }
-
+            const int t = snake_item(lt, pair, npairs);
+            if (t >= nitems) break;
+            const Item c = decode_item(p, item0 + t, ph);
+            const CascadePhase& P = p.phase[c.ph];
+            const CascadeBank& bk = p.bank[c.bank];
+            const int op = P.op;
+            // what the tile reads must be complete; never block on other pairs while this
+            // group's last tile is unpublished
+            if (x.leader && !deps_ready(p, c)) {
+                if (pending) {
+                    bulk_wait_all();
+                    send_done(mbox, x, tile_counter(p, pend), p.err);
+                    pending = false;
+                }
+                if (!deps_wait(p, c)) x.fail = true;
+            }
             const uint32_t in_phase = static_cast<uint32_t>(epi_tiles) & 1u;
-            if (staged && TR::has_in) {
-                // this group's quarters of the tile's input, once this group's earlier
+            if (!op_gram(op)) {
+                // the group's quarters of the tile's input, once the group's earlier TMA
                 // stores have finished reading the boxes
-                if (leader) {
+                if (x.leader) {
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
                     bulk_wait_read_all();
-                    for (int q = 2 * grp; q < 2 * grp + 2; ++q) {
+                    for (int q = 2 * x.grp; q < 2 * x.grp + 2; ++q) {
                         mbar_arrive_expect_tx(&epi_bar[q], QBOX);
-                        tma_load_3d(stg + q * QBOX, &bk.tm_c, &epi_bar[q], col0 + 64 * q, row0, c.mat);
+                        tma_load_3d(x.stg + q * QBOX, &bk.tm[P.map_in], &epi_bar[q],
+                                    c.bj * PAIR + 64 * q, c.bi * PAIR + TILE * static_cast<int>(rank), c.mat);
                     }
                 }
                 ++epi_tiles;
+                x.last_box = -1;  // every box of the group is now an input box
             }
-            if (!mbar_wait(&tfull_bar[ab], u & 1u, p.err)) {
-                aborted = 1;
-                break;
+            uint32_t tbase = 0, tempty = 0;
+            if (op != OP_NORMALIZE) {
+                const int ab = mt & 1;
+                const uint32_t u = static_cast<uint32_t>(mt >> 1);
+                ++mt;
+                if (!mbar_wait(&tfull_bar[ab], u & 1u, p.err)) x.fail = true;
+                tc_fence_after();
+                tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(ab * BN);
+                tempty = ab ? tempty_leader1 : tempty_leader0;
             }
-            tc_fence_after();
-            const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) +
-                                   static_cast<uint32_t>(ab * BN);
-
-            if (!staged) {
-                // OP_XUPDATE_OUT into an `out` whose rows are not 16-byte aligned: plain
-                // bounds-checked stores straight from the accumulator (this group's half).
-                const int m = bk.m, n = bk.n;
-                uint16_t* out = bk.dst + static_cast<size_t>(c.mat) * m * n;
-                const int row = row0 + r;
-#pragma unroll 1
-                for (int cc = 4 * grp; cc < 4 * grp + 4; ++cc) {
-                    const int cb = col0 + cc * 32;
-                    float x[32];
-                    load32_bf16(bk.src + (static_cast<size_t>(c.mat) * bk.s_pad + row) * bk.L_pad + cb, x);
-                    float v[32];
-                    tmem_ld_32x32b_x32(tbase + cc * 32, v);
-                    uint16_t o[32];
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) o[q] = epi_value<OP>(p, v[q], x[q], dd);
-                    if (!bk.tall) {
-                        if (row < m)
-                            for (int q = 0; q < 32; ++q)
-                                if (cb + q < n) out[static_cast<size_t>(row) * n + cb + q] = o[q];
-                    } else if (row < n) {
-                        for (int q = 0; q < 32; ++q)
-                            if (cb + q < m) out[static_cast<size_t>(cb + q) * n + row] = o[q];
-                    }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(ab ? tempty_leader1 : tempty_leader0);
-                continue;
+            switch (op) {
+                case OP_GRAM: epi_tile<OP_GRAM>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
+                case OP_GRAM_NORM: epi_tile<OP_GRAM_NORM>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
+                case OP_SQPOLY: epi_tile<OP_SQPOLY>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
+                case OP_XUPDATE: epi_tile<OP_XUPDATE>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
+                case OP_XUPDATE_OUT: epi_tile<OP_XUPDATE_OUT>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
+                default: epi_tile<OP_NORMALIZE>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
             }
-
-            bool ok = true;
-            for (int q = 2 * grp; q < 2 * grp + 2; ++q) {
-                // direct box: the tile's q-th input box (updated in place), or the group's
-                // output box; transposed box: the group's
-                uint8_t* dbox = stg + (TR::has_in ? q : grp) * QBOX;
-                uint8_t* tbox = stg + (TR::NDIR + grp) * QBOX;  // 64 rows x 128 cols, plain
-                if (!TR::has_in || TR::has_t) {
-                    // the boxes written below must be free of this group's last store
-                    if (leader) bulk_wait_read_all();
-                    named_barrier_sync(1 + grp, 128);
-                }
-                if (TR::has_in && !mbar_wait(&epi_bar[q], in_phase, p.err)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t* drow = dbox + r * 128;
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    float v[32];
-                    tmem_ld_32x32b_x32(tbase + q * 64 + cc * 32, v);
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) {
-                        // 16-byte chunk j of this 128-byte row sits at chunk j ^ (r % 8)
-                        const int j = cc * 4 + w;
-                        uint4* cp = reinterpret_cast<uint4*>(drow + ((j ^ (r & 7)) << 4));
-                        uint32_t xw[4] = {0u, 0u, 0u, 0u};
-                        if (TR::has_in) {
-                            const uint4 x = *cp;
-                            xw[0] = x.x; xw[1] = x.y; xw[2] = x.z; xw[3] = x.w;
-                        }
-                        uint32_t o[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            o[e] = epi_pair<OP>(f2_pack(v[8 * w + 2 * e], v[8 * w + 2 * e + 1]), xw[e],
-                                                coef_x, coef_v, dd);
-                        if (to_direct) *cp = make_uint4(o[0], o[1], o[2], o[3]);
-                        if (TR::has_t && to_mirror) {
-                            // transposed box: element (row r, column 8j + e) at [8j + e][r]
-                            uint16_t* tcol = reinterpret_cast<uint16_t*>(tbox) + r;
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                tcol[(8 * j + 2 * e) * TILE] = static_cast<uint16_t>(o[e] & 0xffffu);
-                                tcol[(8 * j + 2 * e + 1) * TILE] = static_cast<uint16_t>(o[e] >> 16);
-                            }
-                        }
-                    }
-                }
-                if (q == 2 * grp + 1) {
-                    // accumulator ab is free once every epilogue warp of both CTAs has read it
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(ab ? tempty_leader1 : tempty_leader0);
-                }
-                fence_proxy_async_smem();
-                named_barrier_sync(1 + grp, 128);
-                if (leader) {
-                    if (to_direct) tma_store_3d(&bk.tm_d, dbox, col0 + 64 * q, row0, c.mat);
-                    if (TR::has_t && to_mirror) tma_store_3d(&bk.tm_e, tbox, row0, col0 + 64 * q, c.mat);
-                    bulk_commit_group();
-                }
+            // publish the group's previous tile: its stores are older than this tile's two
+            // (one per quarter), so they have long completed
+            if (x.leader && pending) {
+                if (op != OP_XUPDATE_OUT || bk.out_tma) bulk_wait_all_but_two();
+                else bulk_wait_all();
+                send_done(mbox, x, tile_counter(p, pend), p.err);
             }
-            if (!ok) {
-                aborted = 1;
-                break;
-            }
+            pending = true;
+            pend = c;
         }
-        if (leader) {
+        if (x.leader) {
             bulk_wait_all();  // every store of this group has completed
-            if (aborted && epi_tiles > 0)  // and every staging load it armed has landed
-                for (int q = 2 * grp; q < 2 * grp + 2; ++q)
+            if (pending && !aborted) send_done(mbox, x, tile_counter(p, pend), p.err);
+            send_done(mbox, x, nullptr, p.err);  // the group's last message
+            if (aborted && epi_tiles > 0)  // and every input load it armed has landed
+                for (int q = 2 * x.grp; q < 2 * x.grp + 2; ++q)
                     mbar_wait(&epi_bar[q], static_cast<uint32_t>(epi_tiles - 1) & 1u, p.err);
         }
     }
@@ -478,13 +633,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_kernel(const __grid_cons
     tc_fence_before();
     cluster_sync();  // neither CTA leaves while the pair still uses its memory
     tc_fence_after();
-    if (warp == 1) tmem_dealloc_pair(tmem, TR::TMEM_COLS);
+    if (warp == 1) tmem_dealloc_pair(tmem, TMEM_COLS);
 }
 
-static int g_max_pairs[5][64];  // co-resident CTA pairs per op and device (0 = unknown)
+static int g_max_pairs[64];  // co-resident CTA pairs per device (0 = unknown)
 
-template <int OP>
-static cudaError_t launch_op(const GemmParams& p, cudaStream_t stream) {
+cudaError_t launch_cascade(const CascadeParams& p, cudaStream_t stream) {
+    const int nitems = p.phase[p.end_phase].item_begin - p.phase[p.first_phase].item_begin;
+    if (nitems <= 0) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e) return e;
@@ -498,51 +654,27 @@ static cudaError_t launch_op(const GemmParams& p, cudaStream_t stream) {
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = OpTraits<OP>::SMEM;
+    cfg.dynamicSmemBytes = GEMM_SMEM;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int& maxp = g_max_pairs[OP][dev & 63];
+    int& maxp = g_max_pairs[dev & 63];
     if (maxp == 0) {
         cfg.gridDim = dim3(2 * (p.sm_count / 2), 1, 1);
         int clusters = 0;
-        e = cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel<OP>, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&clusters, cascade_kernel, &cfg);
         if (e) return e;
         maxp = clusters > 0 ? clusters : 1;
     }
-    const int pairs = p.total_tiles < maxp ? p.total_tiles : maxp;
+    // no more pairs than can be resident at once: items wait on other pairs' items
+    const int pairs = nitems < maxp ? nitems : maxp;
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<OP>, p);
+    return cudaLaunchKernelEx(&cfg, cascade_kernel, p);
 }
-
-cudaError_t launch_gemm(GemmOp op, const GemmParams& p, cudaStream_t stream) {
-    if (p.total_tiles <= 0) return cudaSuccess;
-    switch (op) {
-        case OP_GRAM: return launch_op<OP_GRAM>(p, stream);
-        case OP_GRAM_NORM: return launch_op<OP_GRAM_NORM>(p, stream);
-        case OP_SQPOLY: return launch_op<OP_SQPOLY>(p, stream);
-        case OP_XUPDATE: return launch_op<OP_XUPDATE>(p, stream);
-        case OP_XUPDATE_OUT: return launch_op<OP_XUPDATE_OUT>(p, stream);
-    }
-    return cudaErrorInvalidValue;
-}
-
-int gemm_tile_cols(GemmOp) { return PAIR; }
 
 cudaError_t gemm_prepare() {
-    cudaError_t e;
-#define ANVIL_SET_SMEM(OPV)                                                                  \
-    if ((e = cudaFuncSetAttribute(gemm_kernel<OPV>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                  OpTraits<OPV>::SMEM)))                                     \
-        return e;
-    ANVIL_SET_SMEM(OP_GRAM)
-    ANVIL_SET_SMEM(OP_GRAM_NORM)
-    ANVIL_SET_SMEM(OP_SQPOLY)
-    ANVIL_SET_SMEM(OP_XUPDATE)
-    ANVIL_SET_SMEM(OP_XUPDATE_OUT)
-#undef ANVIL_SET_SMEM
-    return cudaSuccess;
+    return cudaFuncSetAttribute(cascade_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
 }
 
 }  // namespace anvil

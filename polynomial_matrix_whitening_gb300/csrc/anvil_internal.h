@@ -25,7 +25,6 @@ constexpr int LPAD = 256;            // padding unit of the long side
 constexpr int BK = 64;               // GEMM k-block: one 128-byte swizzle row of bf16
 constexpr int LBLK = 64;             // momentum-kernel tile edge; one diagonal partial each
 constexpr int MAX_BANKS = 8;         // banks per call
-constexpr int MAX_LAUNCH_BANKS = 4;  // banks grouped into one GEMM launch
 
 inline int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
@@ -74,62 +73,92 @@ cudaError_t launch_momentum(const MomentumParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- d and normalisation
 struct NormBank {
-    const uint16_t* y;  // X_raw [g, s_pad, L_pad]
-    uint16_t* y_out;    // normalised X [g, s_pad, L_pad]
     const float* part;  // [g, nlb, s_pad]
     int g, s_pad, L_pad, nlb;
     int mat_begin;      // first matrix of this bank among all matrices of the call
-    long long vec_begin;  // first 8-element vector of this bank in the grouped grid
 };
 struct NormParams {
     NormBank bank[MAX_BANKS];
     int nbanks, total_mats;
-    long long total_vecs;
     float margin, eps;
     float* d;  // [total_mats]
+    unsigned* counters;  // [2 * total_mats] cascade completion counters, zeroed by norm_d
     unsigned* err;
 };
-// d[mat] = sqrt(sum_i float(bf16(sum of the partials of i))) * margin + eps.
+// d[mat] = sqrt(sum_i float(bf16(sum of the partials of i))) * margin + eps; also zeroes
+// the matrix's cascade completion counters.
 cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream);
-// Y_out <- bf16(float(Y) / d[mat]) over every bank.
-cudaError_t launch_normalize(const NormParams& p, cudaStream_t stream);
 
-// ---------------------------------------------------------------- tcgen05 GEMMs
-enum GemmOp : int {
+// ---------------------------------------------------------------- the cascade kernel
+// One persistent tcgen05 kernel walks every phase of the cascade (anvil_gemm.cu).
+enum PhaseOp : int {
     OP_GRAM = 0,        // A = bf16(Y Y^T)                    (upper tiles, mirrored)
-    OP_GRAM_NORM = 1,   // A = bf16(bf16(Y Y^T) / d^2)        (the first Gram)
+    OP_GRAM_NORM = 1,   // A = bf16(bf16(Y Y^T) / d^2)        (the first Gram, on X_raw)
     OP_SQPOLY = 2,      // B = bf16(b A + c A A)              (upper tiles, mirrored)
     OP_XUPDATE = 3,     // Y' = bf16(a Y + B Y)
-    OP_XUPDATE_OUT = 4  // the same, written to out in the natural [m, n] layout
+    OP_XUPDATE_OUT = 4, // the same, written to out in the natural [m, n] layout
+    OP_NORMALIZE = 5    // Y1 = bf16(Y0 / d)                  (no product)
 };
 
-struct GemmBank {
-    CUtensorMap tm_a;     // A operand, K-major, box {64, 128, 1}
-    CUtensorMap tm_b;     // B operand: K-major box {64, 128, 1}, or (xupdate) MN-major {64, 64, 1}
-    CUtensorMap tm_c;     // epilogue input (A for sqpoly, Y for xupdate), box {64, 128, 1}
-    CUtensorMap tm_d;     // epilogue output, box {64, 128, 1}, 128-byte swizzle
-    CUtensorMap tm_e;     // transposed epilogue output (mirror tile / tall out), box {128, 64, 1}
-    const uint16_t* src;  // epilogue input: A (sqpoly) or Y (xupdate)
-    uint16_t* dst;        // output
-    const float* d;       // [g] normaliser of this bank's matrices (gram_norm)
-    int g, s_pad, L_pad, m, n, tall;
-    int out_tma;          // xupdate_out: `out` rows are 16-byte aligned (TMA stores)
-    int T;                // s_pad / PAIR (row blocks)
-    int nt_n;             // column blocks (T for sym ops, L_pad / PAIR for xupdate)
-    int tiles_per_mat;
-    int tile_begin;
-    int num_kb;           // k-blocks of BK
+// Tensor maps of one bank (3-D bf16 over [g][rows][cols]).
+enum MapSlot : int {
+    TM_YK0 = 0,  // Y0, box {64, 128}, 128-byte swizzle: K-major operand, epilogue boxes
+    TM_YK1 = 1,  // Y1, the same
+    TM_YN0 = 2,  // Y0, box {64, 64}: MN-major operand of the X-update
+    TM_YN1 = 3,  // Y1, the same
+    TM_A = 4,    // A [g][s_pad][s_pad], box {64, 128}
+    TM_B = 5,    // B, the same
+    TM_OUT = 6,  // out [g][m][n], box {64, 128} (wide banks whose rows are 16-byte aligned)
+    TM_COUNT = 7
 };
-struct GemmParams {
-    GemmBank bank[MAX_LAUNCH_BANKS];
-    int nbanks, total_tiles;
-    int sm_count;  // persistent grid: CTA pairs up to the co-resident limit
-    float a, b, c;
+
+constexpr int MAX_CASCADE_MAPS = 16;                      // spectral maps per call
+constexpr int MAX_PHASES = 3 * MAX_CASCADE_MAPS + 1;      // GRAM_NORM, NORMALIZE, 3 per map - 1
+
+struct CascadeBank {
+    CUtensorMap tm[TM_COUNT];
+    uint16_t* a;        // A [g, s_pad, s_pad]
+    uint16_t* b;        // B [g, s_pad, s_pad]
+    uint16_t* out;      // out [g, m, n]
+    const float* d;     // [g] normaliser of this bank's matrices
+    int g, s_pad, L_pad, m, n, tall;
+    int out_tma;        // out is written through TM_OUT (wide bank, rows 16-byte aligned)
+    int T, ntl;         // s_pad / PAIR and L_pad / PAIR: row and column blocks of Y
+    int mat_begin;      // first matrix of this bank among all matrices of the call
+};
+
+// A phase: one op over every matrix of every bank.  Its items are 256 x 256 output
+// tiles (upper-triangle blocks for the symmetric ops), bank by bank in the call's bank
+// order, matrix by matrix, block row by block row.
+struct CascadePhase {
+    int op;
+    int map_a, map_b, map_in, map_out;  // MapSlot of each operand (-1: none)
+    float a, b, c;                      // the map's coefficients
+    int item_begin;                     // first item of this phase in the call's item list
+    int bank_begin[MAX_BANKS];          // first item of each bank, relative to item_begin
+    // before an item of matrix i loads anything: chain[i] >= need_chain[bank] and
+    // norm[i] >= need_norm[bank] (0: no wait)
+    unsigned need_chain[MAX_BANKS];
+    unsigned need_norm[MAX_BANKS];
+};
+
+struct CascadeParams {
+    CascadeBank bank[MAX_BANKS];
+    CascadePhase phase[MAX_PHASES + 1];  // phase[nphases].item_begin = the item count
+    int nbanks, nphases;
+    int first_phase, end_phase;  // this launch runs phases [first_phase, end_phase)
+    int sm_count;
+    // Completion counters per matrix, zeroed by norm_d_kernel each step: every finished
+    // tile adds one per epilogue warp group per CTA (4 per tile) to chain[] (the chain of
+    // product phases, each of which waits for the one before it) or, for a normalisation
+    // tile, to norm[].
+    unsigned* chain;
+    unsigned* norm;
     unsigned* err;
 };
-cudaError_t launch_gemm(GemmOp op, const GemmParams& p, cudaStream_t stream);
-int gemm_tile_cols(GemmOp op);  // output tile columns of this op's kernel
-cudaError_t gemm_prepare();  // sets the GEMM kernels' shared-memory limit on this device
+constexpr unsigned SIGNALS_PER_TILE = 4;
+cudaError_t launch_cascade(const CascadeParams& p, cudaStream_t stream);
+cudaError_t gemm_prepare();  // sets the cascade kernel's shared-memory limit on this device
 
 // ---------------------------------------------------------------- tracing / self-test
 // dst [g, m, n] (natural layout) <- Y [g, s_pad, L_pad] (small-side-major), bf16.
