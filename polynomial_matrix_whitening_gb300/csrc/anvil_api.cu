@@ -26,6 +26,7 @@
 #include "../../include/anvil.h"
 #include "anvil_internal.h"
 #include "anvil_adam.h"
+#include "anvil_schedule.h"
 #include "anvil_tail.h"
 
 using namespace anvil;
@@ -182,7 +183,7 @@ anvil_status make_layout(const anvil_bank_desc* banks, int nbanks, Layout* L) {
     }
     L->off_d = 0;
     L->off_cnt = align256(L->off_d + sizeof(float) * L->total_mats);
-    L->off_part = align256(L->off_cnt + 2 * sizeof(unsigned) * L->total_mats);
+    L->off_part = align256(L->off_cnt + sizeof(unsigned) * (2 * L->total_mats + SCHED_COUNTERS));
     L->off_y0 = align256(L->off_part + sizeof(float) * L->part_elems);
     L->off_y1 = align256(L->off_y0 + 2 * L->y_elems);
     L->off_a = align256(L->off_y1 + 2 * L->y_elems);
@@ -394,6 +395,7 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
     cp->sm_count = dev->sm_count;
     cp->chain = reinterpret_cast<unsigned*>(ws + L.off_cnt);
     cp->norm = cp->chain + L.total_mats;
+    unsigned* sched_ctr = cp->norm + L.total_mats;  // [SCHED_COUNTERS]
     cp->err = dev->err;
     // banks in the call's order, heaviest tiles first (the first items of each phase)
     int order[ANVIL_MAX_BANKS];
@@ -424,61 +426,17 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         cb.ntl = G.L_pad / PAIR;
         cb.mat_begin = G.mat_begin;
     }
-    // the phase list: GRAM_NORM, NORMALIZE, then per map k [GRAM], SQPOLY, XUPDATE; map k
-    // reads Y[(k+1)%2] and writes Y[k%2] (out for the last map)
-    {
-        unsigned chain_total[ANVIL_MAX_BANKS] = {0};  // chain signals per matrix so far
-        int items = 0, nph = 0;
-        auto add = [&](int op, int ma, int mb, int min, int mout, const anvil_map& mp, bool after_norm) {
-            CascadePhase& ph = cp->phase[nph++];
-            ph.op = op;
-            ph.map_a = ma;
-            ph.map_b = mb;
-            ph.map_in = min;
-            ph.map_out = mout;
-            ph.a = mp.a;
-            ph.b = mp.b;
-            ph.c = mp.c;
-            ph.item_begin = items;
-            int local = 0;
-            for (int q = 0; q < nbanks; ++q) {
-                const CascadeBank& cb = cp->bank[q];
-                const bool sym = op == OP_GRAM || op == OP_GRAM_NORM || op == OP_SQPOLY;
-                const int tpm = sym ? cb.T * (cb.T + 1) / 2 : cb.T * cb.ntl;
-                ph.bank_begin[q] = local;
-                local += cb.g * tpm;
-                if (op == OP_NORMALIZE) {
-                    ph.need_chain[q] = 0;
-                    ph.need_norm[q] = 0;
-                } else {
-                    ph.need_chain[q] = chain_total[q];
-                    ph.need_norm[q] = after_norm ? SIGNALS_PER_TILE * cb.T * cb.ntl : 0u;
-                    chain_total[q] += SIGNALS_PER_TILE * static_cast<unsigned>(tpm);
-                }
-            }
-            items += local;
-        };
-        const anvil_map none = {0.f, 0.f, 0.f};
-        add(OP_GRAM_NORM, TM_YK0, TM_YK0, -1, TM_A, none, false);
-        add(OP_NORMALIZE, -1, -1, TM_YK0, TM_YK1, none, false);
-        for (int k = 0; k < nmaps; ++k) {
-            const int cur = (k + 1) & 1;
-            const bool last = k == nmaps - 1;
-            if (k > 0) add(OP_GRAM, TM_YK0 + cur, TM_YK0 + cur, -1, TM_A, maps[k], false);
-            add(OP_SQPOLY, TM_A, TM_A, TM_A, TM_B, maps[k], false);
-            add(last ? OP_XUPDATE_OUT : OP_XUPDATE, TM_B, TM_YN0 + cur, TM_YK0 + cur,
-                last ? TM_OUT : TM_YK0 + (cur ^ 1), maps[k], k == 0);
-        }
-        cp->nphases = nph;
-        cp->phase[nph].item_begin = items;
-    }
-    auto run_phases = [&](int first, int end, int kind) -> anvil_status {
-        cp->first_phase = first;
-        cp->end_phase = end;
+    build_phases(cp, maps, nmaps);
+    int phase_run[MAX_PHASES + 1];
+    order_phase_major(cp, phase_run);
+    auto run_range = [&](int first, int end, int kind, int slot) -> anvil_status {
+        cp->first_run = first;
+        cp->end_run = end;
+        cp->next_item = sched_ctr + slot;
         cudaError_t ee = profiled(kind, stream, [&] { return launch_cascade(*cp, stream); });
         return ee ? cuda_fail(ee, "cascade launch") : ANVIL_OK;
     };
-    if (!trace) return run_phases(0, cp->nphases, ANVIL_KERNEL_CASCADE);
+    if (!trace) return run_range(0, cp->nruns, ANVIL_KERNEL_CASCADE, 0);
 
     static const int kinds[6] = {ANVIL_KERNEL_GRAM, ANVIL_KERNEL_GRAM_NORM, ANVIL_KERNEL_SQPOLY,
                                  ANVIL_KERNEL_XUPDATE, ANVIL_KERNEL_XUPDATE_OUT, ANVIL_KERNEL_NORMALIZE};
@@ -487,7 +445,7 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
     const size_t na1 = static_cast<size_t>(G0.g) * G0.s * G0.s;
     for (int ph = 0, k = 0; ph < cp->nphases; ++ph) {
         const int op = cp->phase[ph].op;
-        if ((st = run_phases(ph, ph + 1, kinds[op]))) return st;
+        if ((st = run_range(phase_run[ph], phase_run[ph + 1], kinds[op], 1 + ph))) return st;
         if (op == OP_NORMALIZE && trace->X &&
             (e = launch_extract_x(P[0].y[1], trace->X, G0.g, G0.m, G0.n, G0.tall, G0.s_pad, G0.L_pad,
                                   stream)))

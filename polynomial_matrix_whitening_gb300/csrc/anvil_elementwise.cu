@@ -166,6 +166,8 @@ cudaError_t launch_momentum(const MomentumParams& p, cudaStream_t stream) {
     return launch_pdl(momentum_kernel, dim3(p.total_tiles), dim3(256), 0, stream, p);
 }
 
+static_assert(SCHED_COUNTERS <= 256, "norm_d_kernel zeroes the item counters with one block");
+
 // One block per matrix.  Diagonal entry i of the first Gram is the fp32 sum of the
 // squares of row i of Y, rounded to bf16 as the page stores the Gram; the trace sums
 // those in fp32.
@@ -181,6 +183,7 @@ __global__ void __launch_bounds__(256) norm_d_kernel(const __grid_constant__ Nor
     const NormBank& B = p.bank[bi];
     const int lm = gm - B.mat_begin;
     if (threadIdx.x < 2) p.counters[threadIdx.x * p.total_mats + gm] = 0u;
+    if (gm == 0 && threadIdx.x < SCHED_COUNTERS) p.counters[2 * p.total_mats + threadIdx.x] = 0u;
     const float* part = B.part + static_cast<size_t>(lm) * B.nlb * B.s_pad;  // [nlb][s_pad]
     float acc = 0.f;
     for (int i = threadIdx.x; i < B.s_pad; i += blockDim.x) {

@@ -14,9 +14,10 @@
 // block twice (itself, and its mirror).  A A contracts A's rows with A's rows (A A =
 // A A^T), so every operand is K-major except Y in the X-update, read MN-major.
 //
-// Work items.  An item is one 256x256 output tile of one matrix in one phase.  Items are
-// numbered phase by phase and handed to the persistent grid of CTA pairs in a snake
-// order, each pair visiting its items in increasing order.  An item loads nothing before
+// Work items.  An item is one 256x256 output tile of one matrix in one phase.  The host
+// numbers the items by a list of runs (each: one phase of a range of matrices of one
+// bank) and the persistent grid of CTA pairs takes them in list order: a pair ready for
+// work takes the next item from a global counter, so each pair's items increase.  An item loads nothing before
 // the phases it reads are complete for its matrix: every finished tile adds to a
 // per-matrix completion counter in global memory (a release add once the tile's stores
 // have landed) and an item's loads wait (acquire) until its matrix's counters reach the
@@ -67,9 +68,10 @@ constexpr int EPI_GROUPS = 2;
 constexpr int PUB_DEPTH = 4;  // completion messages in flight per epilogue group
 // warp 0: TMA producer; warp 1: TMEM owner and MMA issuer; warps 2-9: epilogue, in two
 // groups of four (one warp per TMEM lane quadrant), group h owning quarters 2h, 2h+1;
-// warp 10: publisher of finished tiles.
+// warp 10: publisher of finished tiles; warp 11: the pair's item scheduler (leader CTA).
 constexpr int PUB_WARP = 2 + EPI_GROUPS * 4;
-constexpr int GEMM_THREADS = 32 * (PUB_WARP + 1);
+constexpr int SCHED_WARP = PUB_WARP + 1;
+constexpr int GEMM_THREADS = 32 * (SCHED_WARP + 1);
 
 __host__ __device__ constexpr bool op_sym(int op) {
     return op == OP_GRAM || op == OP_GRAM_NORM || op == OP_SQPOLY;
@@ -83,32 +85,69 @@ struct Item {
     int ph, bank, mat, bi, bj;
 };
 
-// The k-th item of pair c in a persistent grid of G pairs: items are handed out in
-// rounds of G, alternating direction (a snake), so each pair's items increase with k.
-__device__ __forceinline__ int snake_item(int k, int c, int G) {
-    return k * G + ((k & 1) ? (G - 1 - c) : c);
+// Item schedule of a CTA pair: the leader's scheduler warp takes the pair's next item
+// from the launch's global counter (an atomic add) and writes it into a ring in both
+// CTAs' shared memory; every role of both CTAs reads the ring in order and frees each
+// slot on the leader's barrier.  Items thus go to whichever pair is ready for work, in
+// list order, and each pair's items increase.  The writes need release semantics, which
+// make a thread wait for its own asynchronous copies; the scheduler has none, and the
+// readers free slots with relaxed arrivals (ordered after their read of the slot by a
+// data dependency).
+constexpr int SDEPTH = 4;                         // ring slots
+constexpr int SCONSUMERS = 3 + 2 * EPI_GROUPS;    // both producers, the MMA, every epilogue group
+
+struct SchedRing {
+    uint64_t full[SDEPTH];   // slot written (this CTA)
+    uint64_t empty[SDEPTH];  // slot read by every consumer (leader CTA)
+    int item[SDEPTH];
+};
+
+// Scheduler: publishes item t (>= the item count: no more work) as the k-th entry.
+__device__ __forceinline__ bool sched_push(SchedRing& q, int k, int t, unsigned* err) {
+    const int s = k % SDEPTH;
+    if (!mbar_wait_cluster(&q.empty[s], ((k / SDEPTH) & 1) ^ 1, err)) return false;
+    q.item[s] = t;
+    st_cluster_u32(map_to_rank(&q.item[s], 1), static_cast<uint32_t>(t));
+    mbar_arrive_cta(&q.full[s]);
+    mbar_arrive_cluster(map_to_rank(&q.full[s], 1));
+    return true;
+}
+
+// Any other role: the k-th entry (INT_MAX if the wait gave up).
+__device__ __forceinline__ int sched_take(SchedRing& q, int k, unsigned* err) {
+    const int s = k % SDEPTH;
+    if (!mbar_wait_cluster(&q.full[s], (k / SDEPTH) & 1, err)) return 0x7fffffff;
+    const int t = *reinterpret_cast<volatile int*>(&q.item[s]);
+    const uint32_t one = (static_cast<uint32_t>(t) >> 31) + 1u;  // 1, once t has been read
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+                     map_to_rank(&q.empty[s], 0)),
+                 "r"(one)
+                 : "memory");
+    return t;
 }
 
 // Item t (an index into the call's item list) -> phase, bank, matrix, block row and
-// column.  `ph` is the caller's phase cursor: items are visited in increasing order.
-__device__ __forceinline__ Item decode_item(const CascadeParams& p, int t, int& ph) {
-    while (ph + 1 < p.end_phase && t >= p.phase[ph + 1].item_begin) ++ph;
-    const CascadePhase& P = p.phase[ph];
-    int local = t - P.item_begin;
-    int bi = 0;
-#pragma unroll 1
-    for (int i = 1; i < p.nbanks; ++i)
-        if (local >= P.bank_begin[i]) bi = i;
-    local -= P.bank_begin[bi];
-    const CascadeBank& B = p.bank[bi];
+// column: the run holding t (binary search over this launch's runs), then the tile.
+__device__ __forceinline__ Item decode_item(const CascadeParams& p, int t) {
+    int lo = p.first_run, hi = p.end_run - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.run[mid].begin <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    const CascadeRun& R = p.run[lo];
+    const CascadePhase& P = p.phase[R.phase];
+    const CascadeBank& B = p.bank[R.bank];
     Item it;
-    it.ph = ph;
-    it.bank = bi;
+    it.ph = R.phase;
+    it.bank = R.bank;
     const int T = B.T;
     const bool sym = op_sym(P.op);
     const int tpm = sym ? T * (T + 1) / 2 : T * B.ntl;
-    it.mat = local / tpm;
-    int r = local - it.mat * tpm;
+    const int local = t - R.begin;
+    const int lm = local / tpm;
+    it.mat = R.mat0 + lm;
+    int r = local - lm * tpm;
     if (sym) {
         int ti = 0;
         while (r >= T - ti) {
@@ -263,28 +302,30 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
         } else if (!mbar_wait(&x.epi_bar[q], in_phase, p.err)) {
             x.fail = true;
         }
-        uint8_t* drow = x.stg + box * QBOX + r * 128;
+        const uint32_t drow = smem_u32(x.stg) + static_cast<uint32_t>(box * QBOX + r * 128);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
+            // 16-byte chunk j of this 128-byte row sits at chunk j ^ (r % 8); the chunk's
+            // four input loads go out together, ahead of the accumulator read
+            uint4 xin[4];
+            if (has_in) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) xin[w] = lds128(drow + static_cast<uint32_t>(((cc * 4 + w) ^ (r & 7)) << 4));
+            }
             float v[32];
             if (has_acc) tmem_ld_32x32b_x32(tbase + q * 64 + cc * 32, v);
             const int cb = col0 + q * 64 + cc * 32;  // first column of this chunk
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                // 16-byte chunk j of this 128-byte row sits at chunk j ^ (r % 8)
-                const int j = cc * 4 + w;
-                uint4* cp = reinterpret_cast<uint4*>(drow + ((j ^ (r & 7)) << 4));
-                uint32_t xw[4] = {0u, 0u, 0u, 0u};
-                if (has_in) {
-                    const uint4 u = *cp;
-                    xw[0] = u.x; xw[1] = u.y; xw[2] = u.z; xw[3] = u.w;
-                }
+                const uint32_t xw[4] = {has_in ? xin[w].x : 0u, has_in ? xin[w].y : 0u, has_in ? xin[w].z : 0u,
+                                        has_in ? xin[w].w : 0u};
                 uint32_t o[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     o[e] = epi_pair<OP>(has_acc ? f2_pack(v[8 * w + 2 * e], v[8 * w + 2 * e + 1]) : 0ull,
                                         xw[e], coef_x, coef_v, dd);
-                if (tma_direct) *cp = make_uint4(o[0], o[1], o[2], o[3]);
+                if (tma_direct)
+                    sts128(drow + static_cast<uint32_t>(((cc * 4 + w) ^ (r & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
                 const int c8 = cb + 8 * w;  // column of o[0]'s low half
                 if (sym) {
                     if (mirror) {
@@ -342,15 +383,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
     __shared__ __align__(8) uint64_t mma_done_bar;
     __shared__ __align__(8) uint64_t epi_bar[NQ];  // epilogue input loads, one per quarter
     __shared__ __align__(8) Mailbox mbox;
+    __shared__ __align__(8) SchedRing sring;
+    __shared__ volatile int grp_item[EPI_GROUPS];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int aborted;
 
     pdl_allow_next();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the MMAs), 1 = peer
-    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-    const int item0 = p.phase[p.first_phase].item_begin;
-    const int nitems = p.phase[p.end_phase].item_begin - item0;
+    const int item0 = p.run[p.first_run].begin;
+    const int nitems = p.run[p.end_run].begin - item0;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
@@ -369,6 +411,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 mbar_init(&mbox.full[g][s], 1);
                 mbar_init(&mbox.empty[g][s], 1);
             }
+        for (int s = 0; s < SDEPTH; ++s) {
+            mbar_init(&sring.full[s], 1);
+            mbar_init(&sring.empty[s], SCONSUMERS);
+        }
         mbar_init(&mma_done_bar, 1);
         fence_mbar_init();
         aborted = 0;
@@ -390,11 +436,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer
-            int it = 0, ph = p.first_phase;
+            int it = 0;
             for (int k = 0;; ++k) {
-                const int t = snake_item(k, pair, npairs);
-                if (t >= nitems || aborted) break;
-                const Item c = decode_item(p, item0 + t, ph);
+                const int t = sched_take(sring, k, p.err);
+                if (t == 0x7fffffff) aborted = 1;
+                if (t >= nitems) break;
+                const Item c = decode_item(p, item0 + t);
                 const CascadePhase& P = p.phase[c.ph];
                 if (P.op == OP_NORMALIZE) continue;
                 const CascadeBank& bk = p.bank[c.bank];
@@ -443,11 +490,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
             // ---------------- MMA issuer (leader CTA)
             constexpr uint32_t idesc_kk = idesc_bf16_f32(PAIR, PAIR, false, false);
             constexpr uint32_t idesc_kn = idesc_bf16_f32(PAIR, PAIR, false, true);
-            int it = 0, mt = 0, ph = p.first_phase;
+            int it = 0, mt = 0;
             for (int lt = 0;; ++lt) {
-                const int t = snake_item(lt, pair, npairs);
-                if (t >= nitems || aborted) break;
-                const Item c = decode_item(p, item0 + t, ph);
+                const int t = sched_take(sring, lt, p.err);
+                if (t == 0x7fffffff) aborted = 1;
+                if (t >= nitems) break;
+                const Item c = decode_item(p, item0 + t);
                 const CascadePhase& P = p.phase[c.ph];
                 if (P.op == OP_NORMALIZE) continue;
                 const CascadeBank& bk = p.bank[c.bank];
@@ -496,6 +544,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
             // peer CTA: its TMEM is written by the leader's MMAs; wait for the last one
             mbar_wait(&mma_done_bar, 0, p.err);
         }
+    } else if (warp == SCHED_WARP) {
+        if (lane == 0 && rank == 0) {
+            // ---------------- scheduler (leader CTA)
+            for (int k = 0;; ++k) {
+                const unsigned next = aborted ? static_cast<unsigned>(nitems) : atomicAdd(p.next_item, 1u);
+                const int t = next >= static_cast<unsigned>(nitems) ? nitems : static_cast<int>(next);
+                if (!sched_push(sring, k, t, p.err)) {
+                    aborted = 1;
+                    break;
+                }
+                if (t >= nitems) break;
+            }
+        }
     } else if (warp == PUB_WARP) {
         if (lane == 0) {
             // ---------------- publisher: one release add per finished tile and group
@@ -542,19 +603,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
         x.npub = 0;
         const uint32_t tempty_leader0 = map_to_rank(&tempty_bar[0], 0);
         const uint32_t tempty_leader1 = map_to_rank(&tempty_bar[1], 0);
-        int ph = p.first_phase, mt = 0;
+        int mt = 0;
         bool pending = false;  // the group's latest tile, published after the next one
         Item pend = {0, 0, 0, 0, 0};
         for (int lt = 0;; ++lt) {
+            if (x.leader) {
+                // the group's next item; a wait that may be long never holds back this
+                // group's last tile
+                if (pending && !mbar_test_wait(smem_u32(&sring.full[lt % SDEPTH]), (lt / SDEPTH) & 1)) {
+                    bulk_wait_all();
+                    send_done(mbox, x, tile_counter(p, pend), p.err);
+                    pending = false;
+                }
+                const int tn = sched_take(sring, lt, p.err);
+                if (tn == 0x7fffffff) x.fail = true;
+                grp_item[x.grp] = tn;
+            }
             // the group stops together: at its last item, or once any wait of any role
             // (or of any thread of the group) gave up
             if (named_barrier_or(1 + x.grp, 128, x.fail || aborted)) {
                 aborted = 1;
                 break;
             }
-            const int t = snake_item(lt, pair, npairs);
+            const int t = grp_item[x.grp];
             if (t >= nitems) break;
-            const Item c = decode_item(p, item0 + t, ph);
+            const Item c = decode_item(p, item0 + t);
             const CascadePhase& P = p.phase[c.ph];
             const CascadeBank& bk = p.bank[c.bank];
             const int op = P.op;
@@ -639,7 +712,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
 static int g_max_pairs[64];  // co-resident CTA pairs per device (0 = unknown)
 
 cudaError_t launch_cascade(const CascadeParams& p, cudaStream_t stream) {
-    const int nitems = p.phase[p.end_phase].item_begin - p.phase[p.first_phase].item_begin;
+    const int nitems = p.run[p.end_run].begin - p.run[p.first_run].begin;
     if (nitems <= 0) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

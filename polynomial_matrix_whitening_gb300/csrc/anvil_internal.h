@@ -82,7 +82,7 @@ struct NormParams {
     int nbanks, total_mats;
     float margin, eps;
     float* d;  // [total_mats]
-    unsigned* counters;  // [2 * total_mats] cascade completion counters, zeroed by norm_d
+    unsigned* counters;  // [2 * total_mats + SCHED_COUNTERS] cascade counters, zeroed by norm_d
     unsigned* err;
 };
 // d[mat] = sqrt(sum_i float(bf16(sum of the partials of i))) * margin + eps; also zeroes
@@ -127,26 +127,36 @@ struct CascadeBank {
     int mat_begin;      // first matrix of this bank among all matrices of the call
 };
 
-// A phase: one op over every matrix of every bank.  Its items are 256 x 256 output
-// tiles (upper-triangle blocks for the symmetric ops), bank by bank in the call's bank
-// order, matrix by matrix, block row by block row.
+// A phase: one op of the cascade (over every matrix of every bank).
 struct CascadePhase {
     int op;
     int map_a, map_b, map_in, map_out;  // MapSlot of each operand (-1: none)
     float a, b, c;                      // the map's coefficients
-    int item_begin;                     // first item of this phase in the call's item list
-    int bank_begin[MAX_BANKS];          // first item of each bank, relative to item_begin
-    // before an item of matrix i loads anything: chain[i] >= need_chain[bank] and
-    // norm[i] >= need_norm[bank] (0: no wait)
+    // before an item of matrix i of bank q loads anything: chain[i] >= need_chain[q]
+    // and norm[i] >= need_norm[q] (0: no wait)
     unsigned need_chain[MAX_BANKS];
     unsigned need_norm[MAX_BANKS];
 };
 
+// The order in which the kernel walks its items: a list of runs, each the tiles of one
+// phase for a range of matrices of one bank (matrix by matrix, block row by block row),
+// numbered from `begin`.  Any order is valid in which every phase of a matrix comes after
+// the phases it reads.
+struct CascadeRun {
+    int begin;        // first item (global index) of the run
+    uint8_t phase;
+    uint8_t bank;
+    uint16_t mat0;    // first matrix (within the bank)
+    uint32_t nmat;    // matrices in the run
+};
+constexpr int MAX_RUNS = 1400;
+
 struct CascadeParams {
     CascadeBank bank[MAX_BANKS];
-    CascadePhase phase[MAX_PHASES + 1];  // phase[nphases].item_begin = the item count
-    int nbanks, nphases;
-    int first_phase, end_phase;  // this launch runs phases [first_phase, end_phase)
+    CascadePhase phase[MAX_PHASES];
+    CascadeRun run[MAX_RUNS + 1];  // run[nruns].begin = the item count
+    int nbanks, nphases, nruns;
+    int first_run, end_run;  // this launch walks runs [first_run, end_run)
     int sm_count;
     // Completion counters per matrix, zeroed by norm_d_kernel each step: every finished
     // tile adds one per epilogue warp group per CTA (4 per tile) to chain[] (the chain of
@@ -154,9 +164,14 @@ struct CascadeParams {
     // tile, to norm[].
     unsigned* chain;
     unsigned* norm;
+    // this launch's item counter (zeroed by norm_d_kernel each step): every CTA pair takes
+    // its next item with an atomic add
+    unsigned* next_item;
     unsigned* err;
 };
 constexpr unsigned SIGNALS_PER_TILE = 4;
+// item counters per step: one for the fused launch, one per phase for traced steps
+constexpr int SCHED_COUNTERS = MAX_PHASES + 1;
 cudaError_t launch_cascade(const CascadeParams& p, cudaStream_t stream);
 cudaError_t gemm_prepare();  // sets the cascade kernel's shared-memory limit on this device
 

@@ -1,0 +1,159 @@
+// anvil_schedule.cu -- the host-side phase table and item order of the cascade kernel
+// (anvil_gemm.cu).  The phases are those of the page "modded-nanogpt
+// track_1_short/optim/anvil.py", anvil_cascade, for every bank: the first Gram (on X_raw,
+// divided by d^2), the normalisation X / d, then per spectral map the Gram (after the
+// first map), B = bA + cA^2 and the X-update.  The order is a list of runs (anvil_internal.h).
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "anvil_internal.h"
+#include "anvil_schedule.h"
+
+namespace anvil {
+
+static bool sym_op(int op) { return op == OP_GRAM || op == OP_GRAM_NORM || op == OP_SQPOLY; }
+
+int phase_tiles(const CascadeBank& b, int op) {
+    return sym_op(op) ? b.T * (b.T + 1) / 2 : b.T * b.ntl;
+}
+
+void build_phases(CascadeParams* cp, const anvil_map_coef* maps, int nmaps) {
+    unsigned chain_total[MAX_BANKS] = {0};  // chain signals per matrix of each bank so far
+    int nph = 0;
+    auto add = [&](int op, int ma, int mb, int min, int mout, float a, float b, float c, bool after_norm) {
+        CascadePhase& ph = cp->phase[nph++];
+        ph.op = op;
+        ph.map_a = ma;
+        ph.map_b = mb;
+        ph.map_in = min;
+        ph.map_out = mout;
+        ph.a = a;
+        ph.b = b;
+        ph.c = c;
+        for (int q = 0; q < cp->nbanks; ++q) {
+            const CascadeBank& cb = cp->bank[q];
+            if (op == OP_NORMALIZE) {
+                ph.need_chain[q] = 0;
+                ph.need_norm[q] = 0;
+            } else {
+                ph.need_chain[q] = chain_total[q];
+                ph.need_norm[q] = after_norm ? SIGNALS_PER_TILE * static_cast<unsigned>(cb.T * cb.ntl) : 0u;
+                chain_total[q] += SIGNALS_PER_TILE * static_cast<unsigned>(phase_tiles(cb, op));
+            }
+        }
+    };
+    // map k reads Y[(k+1)%2] and writes Y[k%2] (out for the last map)
+    add(OP_GRAM_NORM, TM_YK0, TM_YK0, -1, TM_A, 0.f, 0.f, 0.f, false);
+    add(OP_NORMALIZE, -1, -1, TM_YK0, TM_YK1, 0.f, 0.f, 0.f, false);
+    for (int k = 0; k < nmaps; ++k) {
+        const int cur = (k + 1) & 1;
+        const bool last = k == nmaps - 1;
+        if (k > 0) add(OP_GRAM, TM_YK0 + cur, TM_YK0 + cur, -1, TM_A, maps[k].a, maps[k].b, maps[k].c, false);
+        add(OP_SQPOLY, TM_A, TM_A, TM_A, TM_B, maps[k].a, maps[k].b, maps[k].c, false);
+        add(last ? OP_XUPDATE_OUT : OP_XUPDATE, TM_B, TM_YN0 + cur, TM_YK0 + cur,
+            last ? TM_OUT : TM_YK0 + (cur ^ 1), maps[k].a, maps[k].b, maps[k].c, k == 0);
+    }
+    cp->nphases = nph;
+}
+
+// Phase by phase, banks in their order (heaviest first), all matrices of a bank in one run.
+// phase_run[p] receives the first run of phase p (phase_run[nphases] = nruns).
+void order_phase_major(CascadeParams* cp, int* phase_run) {
+    int items = 0, nr = 0;
+    for (int p = 0; p < cp->nphases; ++p) {
+        if (phase_run) phase_run[p] = nr;
+        for (int q = 0; q < cp->nbanks; ++q) {
+            const CascadeBank& b = cp->bank[q];
+            CascadeRun& r = cp->run[nr++];
+            r.begin = items;
+            r.phase = static_cast<uint8_t>(p);
+            r.bank = static_cast<uint8_t>(q);
+            r.mat0 = 0;
+            r.nmat = static_cast<uint32_t>(b.g);
+            items += b.g * phase_tiles(b, cp->phase[p].op);
+        }
+    }
+    if (phase_run) phase_run[cp->nphases] = nr;
+    cp->nruns = nr;
+    cp->run[nr].begin = items;
+}
+
+// Matrix by matrix in a staggered start: every bank releases its matrices at an even
+// rate over the step, and each (matrix, phase) is placed by its estimated ready time
+// (the matrix's release plus the latencies of the phases before it).  A matrix then runs
+// its phases close together, so the tiles one phase writes are mostly still in L2 when
+// the next phase reads them, while the matrices in flight together keep every CTA pair
+// busy.  Costs are in units of one 64-deep k-block of a 256x256 tile.
+void order_staggered(CascadeParams* cp, int npairs) {
+    const double kEpi = 6.0;    // epilogue of a tile that no product overlaps
+    const double kSync = 8.0;   // completion -> publish -> dependants see it
+    auto cost = [&](const CascadeBank& b, int op) -> double {
+        if (op == OP_NORMALIZE) return kEpi;
+        const int K = (op == OP_GRAM || op == OP_GRAM_NORM) ? b.L_pad : b.s_pad;
+        return K / 64.0;
+    };
+    double work = 0.0;
+    int total_mats = 0;
+    for (int q = 0; q < cp->nbanks; ++q) {
+        const CascadeBank& b = cp->bank[q];
+        total_mats += b.g;
+        for (int p = 0; p < cp->nphases; ++p)
+            work += static_cast<double>(b.g) * phase_tiles(b, cp->phase[p].op) * cost(b, cp->phase[p].op);
+    }
+    const double t_est = work / (npairs > 0 ? npairs : 1);
+    // matrices per run, so that the list fits
+    int chunk = 1;
+    while (((total_mats + chunk - 1) / chunk + cp->nbanks) * cp->nphases > MAX_RUNS) ++chunk;
+    struct Seg {
+        double ready;
+        int bank, mat0, nmat, phase;
+    };
+    std::vector<Seg> segs;
+    for (int q = 0; q < cp->nbanks; ++q) {
+        const CascadeBank& b = cp->bank[q];
+        double chain = 0.0;
+        for (int p = 0; p < cp->nphases; ++p) chain += cost(b, cp->phase[p].op) + kSync;
+        const double span = t_est > chain ? t_est - chain : 0.0;
+        for (int m0 = 0; m0 < b.g; m0 += chunk) {
+            const int nm = std::min(chunk, b.g - m0);
+            double t = span * m0 / b.g;
+            for (int p = 0; p < cp->nphases; ++p) {
+                segs.push_back({t, q, m0, nm, p});
+                t += cost(b, cp->phase[p].op) + kSync;
+            }
+        }
+    }
+    std::stable_sort(segs.begin(), segs.end(), [](const Seg& x, const Seg& y) {
+        if (x.ready != y.ready) return x.ready < y.ready;
+        if (x.phase != y.phase) return x.phase < y.phase;
+        return x.bank < y.bank;
+    });
+    int items = 0, nr = 0;
+    for (const Seg& sg : segs) {
+        const CascadeBank& b = cp->bank[sg.bank];
+        const int n = sg.nmat * phase_tiles(b, cp->phase[sg.phase].op);
+        if (nr > 0) {
+            CascadeRun& last = cp->run[nr - 1];
+            if (last.phase == sg.phase && last.bank == sg.bank &&
+                static_cast<int>(last.mat0 + last.nmat) == sg.mat0) {
+                last.nmat += static_cast<uint32_t>(sg.nmat);
+                items += n;
+                continue;
+            }
+        }
+        CascadeRun& r = cp->run[nr++];
+        r.begin = items;
+        r.phase = static_cast<uint8_t>(sg.phase);
+        r.bank = static_cast<uint8_t>(sg.bank);
+        r.mat0 = static_cast<uint16_t>(sg.mat0);
+        r.nmat = static_cast<uint32_t>(sg.nmat);
+        items += n;
+    }
+    cp->nruns = nr;
+    cp->run[nr].begin = items;
+}
+
+}  // namespace anvil
