@@ -414,6 +414,8 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         cb.a = B.a;
         cb.b = B.b;
         cb.out = banks[i].out;
+        cb.y0 = B.y[0];
+        cb.y1 = B.y[1];
         cb.d = B.d;
         cb.g = G.g;
         cb.s_pad = G.s_pad;

@@ -99,6 +99,7 @@ constexpr int SCONSUMERS = 3 + 2 * EPI_GROUPS;    // both producers, the MMA, ev
 struct SchedRing {
     uint64_t full[SDEPTH];   // slot written (this CTA)
     uint64_t empty[SDEPTH];  // slot read by every consumer (leader CTA)
+    uint64_t taken[SDEPTH];  // slot read by the leader's producer (leader CTA)
     int item[SDEPTH];
 };
 
@@ -201,24 +202,43 @@ __device__ __forceinline__ unsigned* tile_counter(const CascadeParams& p, const 
     return (p.phase[it.ph].op == OP_NORMALIZE ? p.norm : p.chain) + p.bank[it.bank].mat_begin + it.mat;
 }
 
+// bf16(RN(x / dd)) for four pairs of fp32 x, given rcp2 = (RN(1/dd), RN(1/dd)).  The
+// product q = RN(x * RN(1/dd)) is within 2.5 ulp of RN(x / dd), so both round to the same
+// bf16 unless a bf16 rounding boundary (low 16 bits 0x8000) lies within 8 ulps of q, or q
+// is tiny (exponent < 8), huge or not finite; a chunk with such an element (about one in
+// 1000) takes the correctly rounded division, out of line.
+__device__ __forceinline__ bool near_bf16_boundary(uint32_t b) {
+    return (((b + 8u) & 0xfff0u) == 0x8000u) | ((((b >> 23) + 1u) & 0xffu) < 9u);
+}
+__device__ __noinline__ uint4 div4_exact(uint64_t x0, uint64_t x1, uint64_t x2, uint64_t x3, float dd) {
+    const uint64_t x[4] = {x0, x1, x2, x3};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        o[e] = f2_to_bf2(f2_pack(__fdiv_rn(__uint_as_float(static_cast<uint32_t>(x[e])), dd),
+                                 __fdiv_rn(__uint_as_float(static_cast<uint32_t>(x[e] >> 32)), dd)));
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+__device__ __forceinline__ uint4 div4_to_bf2(uint64_t x0, uint64_t x1, uint64_t x2, uint64_t x3, uint64_t rcp2,
+                                             float dd) {
+    const uint64_t q0 = f2_mul(x0, rcp2), q1 = f2_mul(x1, rcp2), q2 = f2_mul(x2, rcp2), q3 = f2_mul(x3, rcp2);
+    const bool near = near_bf16_boundary(static_cast<uint32_t>(q0)) | near_bf16_boundary(static_cast<uint32_t>(q0 >> 32)) |
+                      near_bf16_boundary(static_cast<uint32_t>(q1)) | near_bf16_boundary(static_cast<uint32_t>(q1 >> 32)) |
+                      near_bf16_boundary(static_cast<uint32_t>(q2)) | near_bf16_boundary(static_cast<uint32_t>(q2 >> 32)) |
+                      near_bf16_boundary(static_cast<uint32_t>(q3)) | near_bf16_boundary(static_cast<uint32_t>(q3 >> 32));
+    if (__builtin_expect(near, 0)) return div4_exact(x0, x1, x2, x3, dd);
+    return make_uint4(f2_to_bf2(q0), f2_to_bf2(q1), f2_to_bf2(q2), f2_to_bf2(q3));
+}
+
 // The elementwise part of each op's epilogue on a pair: accumulator values v (packed fp32
 // pair) and input word xw (two bf16); returns two bf16.  Each product and sum is rounded
-// on its own (the page's fp32 tensor operations one at a time); divisions are correctly
-// rounded.
+// on its own (the page's fp32 tensor operations one at a time).  (The first Gram's
+// quotient is taken four pairs at a time, div4_to_bf2.)
 template <int OP>
 __device__ __forceinline__ uint32_t epi_pair(uint64_t v, uint32_t xw, uint64_t coef_x,
                                              uint64_t coef_v, float dd) {
-    if (OP == OP_GRAM) return f2_to_bf2(v);
-    if (OP == OP_GRAM_NORM) {  // bf16(bf16(acc) / d^2)
-        const float lo = __fdiv_rn(round_bf(__uint_as_float(static_cast<uint32_t>(v))), dd);
-        const float hi = __fdiv_rn(round_bf(__uint_as_float(static_cast<uint32_t>(v >> 32))), dd);
-        return f2_to_bf2(f2_pack(lo, hi));
-    }
-    if (OP == OP_NORMALIZE) {  // bf16(Y / d)
-        const float lo = __fdiv_rn(bf2f(static_cast<uint16_t>(xw & 0xffffu)), dd);
-        const float hi = __fdiv_rn(bf2f(static_cast<uint16_t>(xw >> 16)), dd);
-        return f2_to_bf2(f2_pack(lo, hi));
-    }
+    (void)dd;
+    if (OP == OP_GRAM || OP == OP_GRAM_NORM) return f2_to_bf2(v);
     const uint64_t t = f2_mul(coef_x, bf2_to_f2(xw));                     // b A  or  a Y
     if (OP == OP_SQPOLY) return f2_to_bf2(f2_add(t, f2_mul(coef_v, v)));  // + c acc
     return f2_to_bf2(f2_add(t, v));                                       // + acc
@@ -281,7 +301,7 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
     // take it (a tall bank's X = Y^T, or rows not 16-byte aligned)
     const bool tma_direct = OP != OP_XUPDATE_OUT || bk.out_tma;
     const bool mirror = sym && c.bi != c.bj;
-    const uint64_t coef_x = f2_pack(OP == OP_SQPOLY ? P.b : P.a, OP == OP_SQPOLY ? P.b : P.a);
+    uint64_t coef_x = f2_pack(OP == OP_SQPOLY ? P.b : P.a, OP == OP_SQPOLY ? P.b : P.a);
     const uint64_t coef_v = f2_pack(P.c, P.c);
     float dd = 0.f;
     if (OP == OP_GRAM_NORM) {
@@ -289,6 +309,10 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
         dd = __fmul_rn(d, d);
     } else if (OP == OP_NORMALIZE) {
         dd = bk.d[c.mat];
+    }
+    if (OP == OP_GRAM_NORM || OP == OP_NORMALIZE) {
+        const float rcp = __frcp_rn(dd);
+        coef_x = f2_pack(rcp, rcp);
     }
     uint16_t* const sym_dst = OP == OP_SQPOLY ? bk.b : bk.a;
     for (int q = 2 * x.grp; q < 2 * x.grp + 2; ++q) {
@@ -320,10 +344,18 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
                 const uint32_t xw[4] = {has_in ? xin[w].x : 0u, has_in ? xin[w].y : 0u, has_in ? xin[w].z : 0u,
                                         has_in ? xin[w].w : 0u};
                 uint32_t o[4];
+                if (OP == OP_GRAM_NORM) {  // bf16(bf16(acc) / d^2)
+                    const uint4 r4 = div4_to_bf2(bf2_to_f2(f2_to_bf2(f2_pack(v[8 * w + 0], v[8 * w + 1]))),
+                                                 bf2_to_f2(f2_to_bf2(f2_pack(v[8 * w + 2], v[8 * w + 3]))),
+                                                 bf2_to_f2(f2_to_bf2(f2_pack(v[8 * w + 4], v[8 * w + 5]))),
+                                                 bf2_to_f2(f2_to_bf2(f2_pack(v[8 * w + 6], v[8 * w + 7]))), coef_x, dd);
+                    o[0] = r4.x; o[1] = r4.y; o[2] = r4.z; o[3] = r4.w;
+                } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    o[e] = epi_pair<OP>(has_acc ? f2_pack(v[8 * w + 2 * e], v[8 * w + 2 * e + 1]) : 0ull,
-                                        xw[e], coef_x, coef_v, dd);
+                    for (int e = 0; e < 4; ++e)
+                        o[e] = epi_pair<OP>(has_acc ? f2_pack(v[8 * w + 2 * e], v[8 * w + 2 * e + 1]) : 0ull,
+                                            xw[e], coef_x, coef_v, dd);
+                }
                 if (tma_direct)
                     sts128(drow + static_cast<uint32_t>(((cc * 4 + w) ^ (r & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
                 const int c8 = cb + 8 * w;  // column of o[0]'s low half
@@ -374,6 +406,33 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
     }
 }
 
+// A normalisation tile: Y1 = bf16(Y0 / d) over this CTA's 128 rows and this group's 128
+// of the tile's 256 columns, streamed with coalesced 16-byte loads and stores (a warp
+// covers two 256-byte row segments per access), every load of the thread in flight at
+// once; no staging and no product.
+__device__ __forceinline__ void normalize_tile(const CascadeBank& bk, const Item& c, uint32_t rank, int grp,
+                                               int tid) {
+    const float d = bk.d[c.mat];
+    const float rcp = __frcp_rn(d);
+    const uint64_t rcp2 = f2_pack(rcp, rcp);
+    const size_t row0 = static_cast<size_t>(c.mat) * bk.s_pad + c.bi * PAIR + TILE * rank;
+    const int col0 = c.bj * PAIR + 128 * grp;
+    constexpr int N = 128 * 128 * 2 / 16 / 128;  // 16-byte chunks per thread
+    uint4 v[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const int ch = tid + 128 * i;  // chunk: row ch / 16, 8 columns (ch % 16) * 8
+        const uint4* src = reinterpret_cast<const uint4*>(bk.y0 + (row0 + ch / 16) * bk.L_pad + col0 + (ch % 16) * 8);
+        v[i] = ld_stream_v4(src);
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const int ch = tid + 128 * i;
+        *reinterpret_cast<uint4*>(bk.y1 + (row0 + ch / 16) * bk.L_pad + col0 + (ch % 16) * 8) =
+            div4_to_bf2(bf2_to_f2(v[i].x), bf2_to_f2(v[i].y), bf2_to_f2(v[i].z), bf2_to_f2(v[i].w), rcp2, d);
+    }
+}
+
 __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_constant__ CascadeParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -414,6 +473,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
         for (int s = 0; s < SDEPTH; ++s) {
             mbar_init(&sring.full[s], 1);
             mbar_init(&sring.empty[s], SCONSUMERS);
+            mbar_init(&sring.taken[s], 1);
         }
         mbar_init(&mma_done_bar, 1);
         fence_mbar_init();
@@ -440,6 +500,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
             for (int k = 0;; ++k) {
                 const int t = sched_take(sring, k, p.err);
                 if (t == 0x7fffffff) aborted = 1;
+                if (rank == 0) mbar_arrive_relaxed(&sring.taken[k % SDEPTH]);
                 if (t >= nitems) break;
                 const Item c = decode_item(p, item0 + t);
                 const CascadePhase& P = p.phase[c.ph];
@@ -548,6 +609,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
         if (lane == 0 && rank == 0) {
             // ---------------- scheduler (leader CTA)
             for (int k = 0;; ++k) {
+                // take a pair's next item only once its producer has started the one before:
+                // an item taken early would wait behind this pair's current work
+                if (k > 0 && !mbar_wait(&sring.taken[(k - 1) % SDEPTH], ((k - 1) / SDEPTH) & 1, p.err)) {
+                    aborted = 1;
+                    break;
+                }
                 const unsigned next = aborted ? static_cast<unsigned>(nitems) : atomicAdd(p.next_item, 1u);
                 const int t = next >= static_cast<unsigned>(nitems) ? nitems : static_cast<int>(next);
                 if (!sched_push(sring, k, t, p.err)) {
@@ -642,7 +709,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 if (!deps_wait(p, c)) x.fail = true;
             }
             const uint32_t in_phase = static_cast<uint32_t>(epi_tiles) & 1u;
-            if (!op_gram(op)) {
+            if (!op_gram(op) && op != OP_NORMALIZE) {
                 // the group's quarters of the tile's input, once the group's earlier TMA
                 // stores have finished reading the boxes
                 if (x.leader) {
@@ -673,12 +740,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 case OP_SQPOLY: epi_tile<OP_SQPOLY>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
                 case OP_XUPDATE: epi_tile<OP_XUPDATE>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
                 case OP_XUPDATE_OUT: epi_tile<OP_XUPDATE_OUT>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
-                default: epi_tile<OP_NORMALIZE>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
+                default: normalize_tile(bk, c, rank, x.grp, quad * 32 + lane); break;
             }
             // publish the group's previous tile: its stores are older than this tile's two
             // (one per quarter), so they have long completed
             if (x.leader && pending) {
-                if (op != OP_XUPDATE_OUT || bk.out_tma) bulk_wait_all_but_two();
+                if (op != OP_NORMALIZE && (op != OP_XUPDATE_OUT || bk.out_tma)) bulk_wait_all_but_two();
                 else bulk_wait_all();
                 send_done(mbox, x, tile_counter(p, pend), p.err);
             }

@@ -120,6 +120,8 @@ struct CascadeBank {
     uint16_t* a;        // A [g, s_pad, s_pad]
     uint16_t* b;        // B [g, s_pad, s_pad]
     uint16_t* out;      // out [g, m, n]
+    const uint16_t* y0; // X_raw [g, s_pad, L_pad] (the normalisation's input)
+    uint16_t* y1;       // normalised X (its output)
     const float* d;     // [g] normaliser of this bank's matrices
     int g, s_pad, L_pad, m, n, tall;
     int out_tma;        // out is written through TM_OUT (wide bank, rows 16-byte aligned)
