@@ -306,6 +306,8 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         }
         if ((st = encode_map(&B.tm[TM_A], B.a, G.g, G.s_pad, G.s_pad, BK, TILE))) return st;
         if ((st = encode_map(&B.tm[TM_B], B.b, G.g, G.s_pad, G.s_pad, BK, TILE))) return st;
+        if ((st = encode_map(&B.tm[TM_AN], B.a, G.g, G.s_pad, G.s_pad, BK, BK))) return st;
+        if ((st = encode_map(&B.tm[TM_BN], B.b, G.g, G.s_pad, G.s_pad, BK, BK))) return st;
         // the last X-update of a wide bank stores `out` [g, m, n] by TMA (boxes of Y) when
         // its rows are 16-byte aligned; tall banks (out = Y^T) and the rest take plain stores
         memset(&B.tm[TM_OUT], 0, sizeof(CUtensorMap));

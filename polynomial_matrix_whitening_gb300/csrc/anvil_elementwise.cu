@@ -232,9 +232,14 @@ __global__ void extract_sq_kernel(const uint16_t* __restrict__ src, uint16_t* __
     const long long total = static_cast<long long>(g) * s * s;
     for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
          e += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int j = static_cast<int>(e % s);
-        const int i = static_cast<int>((e / s) % s);
+        int j = static_cast<int>(e % s);
+        int i = static_cast<int>((e / s) % s);
         const int mat = static_cast<int>(e / (static_cast<long long>(s) * s));
+        if (i / 256 > j / 256) {  // only the diagonal and upper 256-blocks are stored
+            const int t = i;
+            i = j;
+            j = t;
+        }
         dst[e] = src[(static_cast<size_t>(mat) * s_pad + i) * s_pad + j];
     }
 }

@@ -293,14 +293,12 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
                                          EpiCtx& x, uint32_t tbase, uint32_t tempty, uint32_t in_phase) {
     constexpr bool has_acc = OP != OP_NORMALIZE;
     constexpr bool has_in = !op_gram(OP);
-    constexpr bool sym = op_sym(OP);
     const int row0 = c.bi * PAIR + TILE * static_cast<int>(rank);  // this CTA's first row
     const int col0 = c.bj * PAIR;
     const int r = x.r;
     // the direct tile leaves by TMA except the last X-update into an `out` that cannot
     // take it (a tall bank's X = Y^T, or rows not 16-byte aligned)
     const bool tma_direct = OP != OP_XUPDATE_OUT || bk.out_tma;
-    const bool mirror = sym && c.bi != c.bj;
     uint64_t coef_x = f2_pack(OP == OP_SQPOLY ? P.b : P.a, OP == OP_SQPOLY ? P.b : P.a);
     const uint64_t coef_v = f2_pack(P.c, P.c);
     float dd = 0.f;
@@ -314,7 +312,6 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
         const float rcp = __frcp_rn(dd);
         coef_x = f2_pack(rcp, rcp);
     }
-    uint16_t* const sym_dst = OP == OP_SQPOLY ? bk.b : bk.a;
     for (int q = 2 * x.grp; q < 2 * x.grp + 2; ++q) {
         int box = q;
         if (!has_in) {
@@ -359,17 +356,7 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
                 if (tma_direct)
                     sts128(drow + static_cast<uint32_t>(((cc * 4 + w) ^ (r & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
                 const int c8 = cb + 8 * w;  // column of o[0]'s low half
-                if (sym) {
-                    if (mirror) {
-                        // element (row0 + r, c8 + e) -> (c8 + e, row0 + r): the 32 lanes of a
-                        // warp write 64 contiguous bytes per element
-                        uint16_t* base = sym_dst + static_cast<size_t>(c.mat) * bk.s_pad * bk.s_pad +
-                                         row0 + r;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            base[static_cast<size_t>(c8 + e) * bk.s_pad] = half_of(o, e);
-                    }
-                } else if (OP == OP_XUPDATE_OUT && !tma_direct) {
+                if (OP == OP_XUPDATE_OUT && !tma_direct) {
                     uint16_t* out = bk.out + static_cast<size_t>(c.mat) * bk.m * bk.n;
                     if (bk.tall) {
                         // X = Y^T: element (row0 + r, c8 + e) -> out row c8 + e, column row0 + r
@@ -529,12 +516,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                     // both CTAs' bytes complete on the leader's barrier of this stage
                     const uint32_t fb = map_to_rank(&full_bar[s], 0);
                     if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * STAGE);
-                    tma_load_3d_pair(sa, tma, fb, kb * BK, arow, c.mat);
+                    // a k-block left of the operand's diagonal block comes from the upper block
+                    // it mirrors, read MN-major: two 64 x 64 boxes (k rows, operand rows)
+                    if (P.map_a_t >= 0 && kb * BK < c.bi * PAIR) {
+                        tma_load_3d_pair(sa, &bk.tm[P.map_a_t], fb, arow, kb * BK, c.mat);
+                        tma_load_3d_pair(sa + 8192, &bk.tm[P.map_a_t], fb, arow + 64, kb * BK, c.mat);
+                    } else {
+                        tma_load_3d_pair(sa, tma, fb, kb * BK, arow, c.mat);
+                    }
                     if (xu) {
                         // Y rows kb*64 .. +63 (the contraction index), this CTA's 128 of the
                         // tile's columns in two 64-column boxes: MN-major chunks 8 KB apart.
                         tma_load_3d_pair(sb, tmb, fb, bofs, kb * BK, c.mat);
                         tma_load_3d_pair(sb + 8192, tmb, fb, bofs + 64, kb * BK, c.mat);
+                    } else if (P.map_b_t >= 0 && kb * BK < c.bj * PAIR) {
+                        tma_load_3d_pair(sb, &bk.tm[P.map_b_t], fb, bofs, kb * BK, c.mat);
+                        tma_load_3d_pair(sb + 8192, &bk.tm[P.map_b_t], fb, bofs + 64, kb * BK, c.mat);
                     } else {
                         tma_load_3d_pair(sb, tmb, fb, kb * BK, bofs, c.mat);
                     }
@@ -549,8 +546,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             // ---------------- MMA issuer (leader CTA)
-            constexpr uint32_t idesc_kk = idesc_bf16_f32(PAIR, PAIR, false, false);
-            constexpr uint32_t idesc_kn = idesc_bf16_f32(PAIR, PAIR, false, true);
             int it = 0, mt = 0;
             for (int lt = 0;; ++lt) {
                 const int t = sched_take(sring, lt, p.err);
@@ -571,7 +566,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 }
                 tc_fence_after();
                 const uint32_t dacc = tmem + static_cast<uint32_t>(ab * BN);
-                const uint32_t idesc = xu ? idesc_kn : idesc_kk;
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % STAGES;
@@ -583,11 +577,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(smem + s * STAGE);
                     const uint32_t b0 = a0 + A_STAGE;
+                    // operands staged MN-major: Y in the X-update, and k-blocks read from the
+                    // transposed upper block of a symmetric operand (as the producer loaded them)
+                    const bool a_mn = P.map_a_t >= 0 && kb * BK < c.bi * PAIR;
+                    const bool b_mn = xu || (P.map_b_t >= 0 && kb * BK < c.bj * PAIR);
+                    const uint32_t idesc = idesc_bf16_f32(PAIR, PAIR, a_mn, b_mn);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                        const uint64_t bd = xu ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
-                                               : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+                        const uint64_t ad = a_mn ? smem_desc_sw128(a0 + kk * 2048, 8192, 1024)
+                                                 : smem_desc_sw128(a0 + kk * 32, 16, 1024);
+                        const uint64_t bd = b_mn ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
+                                                 : smem_desc_sw128(b0 + kk * 32, 16, 1024);
                         umma_bf16_pair(dacc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     umma_commit_pair(&empty_bar[s], 3);  // frees stage s in both CTAs

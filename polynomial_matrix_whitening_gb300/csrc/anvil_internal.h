@@ -109,7 +109,9 @@ enum MapSlot : int {
     TM_A = 4,    // A [g][s_pad][s_pad], box {64, 128}
     TM_B = 5,    // B, the same
     TM_OUT = 6,  // out [g][m][n], box {64, 128} (wide banks whose rows are 16-byte aligned)
-    TM_COUNT = 7
+    TM_AN = 7,   // A, box {64, 64}: an upper block read as the transpose of a lower one
+    TM_BN = 8,   // B, the same
+    TM_COUNT = 9
 };
 
 constexpr int MAX_CASCADE_MAPS = 16;                      // spectral maps per call
@@ -129,10 +131,15 @@ struct CascadeBank {
     int mat_begin;      // first matrix of this bank among all matrices of the call
 };
 
-// A phase: one op of the cascade (over every matrix of every bank).
+// A phase: one op of the cascade (over every matrix of every bank).  A = Y Y^T and B are
+// symmetric; the kernel writes their diagonal and upper 256x256 blocks only.
 struct CascadePhase {
     int op;
     int map_a, map_b, map_in, map_out;  // MapSlot of each operand (-1: none)
+    // A and B are stored as their upper-triangle 256-blocks only: a k-block of a product
+    // operand that falls below the diagonal is read, MN-major, from the transposed upper
+    // block through these maps (-1: the operand is not symmetric)
+    int map_a_t, map_b_t;
     float a, b, c;                      // the map's coefficients
     // before an item of matrix i of bank q loads anything: chain[i] >= need_chain[q]
     // and norm[i] >= need_norm[q] (0: no wait)
@@ -181,7 +188,8 @@ cudaError_t gemm_prepare();  // sets the cascade kernel's shared-memory limit on
 // dst [g, m, n] (natural layout) <- Y [g, s_pad, L_pad] (small-side-major), bf16.
 cudaError_t launch_extract_x(const uint16_t* y, uint16_t* dst, int g, int m, int n, int tall,
                              int s_pad, int L_pad, cudaStream_t stream);
-// dst [g, s, s] <- src [g, s_pad, s_pad], bf16.
+// dst [g, s, s] <- src [g, s_pad, s_pad], bf16, from the diagonal and upper 256-blocks of a
+// symmetric src (a lower block is the transpose of the upper one).
 cudaError_t launch_extract_sq(const uint16_t* src, uint16_t* dst, int g, int s, int s_pad,
                               cudaStream_t stream);
 cudaError_t launch_wait_selftest(unsigned timeout_us, unsigned* err, cudaStream_t stream);

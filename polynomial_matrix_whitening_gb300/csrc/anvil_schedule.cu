@@ -30,6 +30,9 @@ void build_phases(CascadeParams* cp, const anvil_map_coef* maps, int nmaps) {
         ph.map_b = mb;
         ph.map_in = min;
         ph.map_out = mout;
+        // the symmetric operands: A (both operands of A A) and B (the X-update's left factor)
+        ph.map_a_t = ma == TM_A ? TM_AN : ma == TM_B ? TM_BN : -1;
+        ph.map_b_t = mb == TM_A ? TM_AN : -1;
         ph.a = a;
         ph.b = b;
         ph.c = c;
