@@ -46,7 +46,10 @@ GEMM_KINDS = ("gram", "gram_norm", "sqpoly", "xupdate", "xupdate_out", "cascade"
 # ncu DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
 # kernel kind on this workload, from the capture summarised under profiles/; valid only
 # while the kernel source hashes to the recorded value.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/cascade_full_step.md: the cascade launch of the full three-bank step
+    "cascade": {"bytes_per_launch": 3346.6e6, "source_hash": "73bfc9af4843b0d0"},
+}
 
 
 def kernel_source_hash(kind):

@@ -241,10 +241,12 @@ anvil_status anvil_selftest_wait_timeout(unsigned timeout_us, void* stream);
  * with profiling on, while a stream is capturing).  end synchronises, writes up
  * to cap records in launch order, destroys the events and returns how many
  * launches were timed (negative on a CUDA error). */
+/* Kinds 2-7 are the cascade's phases, each its own launch in traced steps only; an
+ * untraced step runs them all in one ANVIL_KERNEL_CASCADE launch. */
 typedef enum {
     ANVIL_KERNEL_MOMENTUM = 0,     /* momentum + cast + diagonal partials */
     ANVIL_KERNEL_NORM_D = 1,       /* d per matrix */
-    ANVIL_KERNEL_NORMALIZE = 2,    /* X <- bf16(X / d) (traced runs: one launch per phase) */
+    ANVIL_KERNEL_NORMALIZE = 2,    /* X <- bf16(X / d) */
     ANVIL_KERNEL_GRAM_NORM = 3,    /* first Gram, A = bf16(bf16(X X^T) / d^2) */
     ANVIL_KERNEL_GRAM = 4,         /* A = bf16(X X^T) */
     ANVIL_KERNEL_SQPOLY = 5,       /* B = bf16(b A + c A A) */
@@ -254,7 +256,7 @@ typedef enum {
     ANVIL_KERNEL_TAIL_SCALE = 9,   /* update tail: lane energies and scales */
     ANVIL_KERNEL_TAIL_APPLY = 10,  /* update tail: equalise + sign-aligned decay update */
     ANVIL_KERNEL_ADAM = 11,        /* Adam step */
-    ANVIL_KERNEL_CASCADE = 12      /* every product phase of every map, one persistent launch */
+    ANVIL_KERNEL_CASCADE = 12      /* the whole cascade (normalisation, every product of every map) */
 } anvil_kernel_kind;
 
 typedef struct { int kind; float ms; } anvil_profile_record;

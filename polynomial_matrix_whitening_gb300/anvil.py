@@ -203,7 +203,7 @@ class Bank:
 
 def multi_bank_step(banks, workspace, maps=None, margin=1.05, eps=1e-6, d_scalars=None,
                     stream=None):
-    """One ANVIL step over several banks (one grouped launch per phase).
+    """One ANVIL step over several banks (three launches: momentum, d, the cascade).
 
     d_scalars: optional fp32 CUDA tensor [nbanks, 4] (momentum, fast_beta, fast_weight,
     slow_beta) read on the device when the step runs (for CUDA-graph replays).

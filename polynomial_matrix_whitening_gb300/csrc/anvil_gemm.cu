@@ -235,10 +235,8 @@ __device__ __forceinline__ uint4 div4_to_bf2(uint64_t x0, uint64_t x1, uint64_t 
 // on its own (the page's fp32 tensor operations one at a time).  (The first Gram's
 // quotient is taken four pairs at a time, div4_to_bf2.)
 template <int OP>
-__device__ __forceinline__ uint32_t epi_pair(uint64_t v, uint32_t xw, uint64_t coef_x,
-                                             uint64_t coef_v, float dd) {
-    (void)dd;
-    if (OP == OP_GRAM || OP == OP_GRAM_NORM) return f2_to_bf2(v);
+__device__ __forceinline__ uint32_t epi_pair(uint64_t v, uint32_t xw, uint64_t coef_x, uint64_t coef_v) {
+    if (OP == OP_GRAM) return f2_to_bf2(v);
     const uint64_t t = f2_mul(coef_x, bf2_to_f2(xw));                     // b A  or  a Y
     if (OP == OP_SQPOLY) return f2_to_bf2(f2_add(t, f2_mul(coef_v, v)));  // + c acc
     return f2_to_bf2(f2_add(t, v));                                       // + acc
@@ -281,9 +279,9 @@ __device__ __forceinline__ void send_done(Mailbox& mb, EpiCtx& x, unsigned* cnt,
     mbar_arrive_cta(&mb.full[x.grp][s]);
 }
 
-// The quarters of one tile that this thread's group owns: read the accumulator (tbase:
-// TMEM address of the thread's lane quadrant in the accumulator; unused by NORMALIZE),
-// combine with the input box, store.  tempty: the leader CTA's barrier for this
+// The quarters of one product tile that this thread's group owns: read the accumulator
+// (tbase: TMEM address of the thread's lane quadrant in the accumulator), combine with
+// the input box, store.  tempty: the leader CTA's barrier for this
 // accumulator.  A wait that gives up sets x.fail and the tile runs to its end all the
 // same (its values are then meaningless), so every thread of the group reaches every
 // group barrier.
@@ -291,7 +289,6 @@ template <int OP>
 __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBank& bk,
                                          const CascadePhase& P, const Item& c, uint32_t rank,
                                          EpiCtx& x, uint32_t tbase, uint32_t tempty, uint32_t in_phase) {
-    constexpr bool has_acc = OP != OP_NORMALIZE;
     constexpr bool has_in = !op_gram(OP);
     const int row0 = c.bi * PAIR + TILE * static_cast<int>(rank);  // this CTA's first row
     const int col0 = c.bj * PAIR;
@@ -302,13 +299,9 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
     uint64_t coef_x = f2_pack(OP == OP_SQPOLY ? P.b : P.a, OP == OP_SQPOLY ? P.b : P.a);
     const uint64_t coef_v = f2_pack(P.c, P.c);
     float dd = 0.f;
-    if (OP == OP_GRAM_NORM) {
+    if (OP == OP_GRAM_NORM) {  // coef_x: the reciprocal of d^2 for div4_to_bf2
         const float d = bk.d[c.mat];
         dd = __fmul_rn(d, d);
-    } else if (OP == OP_NORMALIZE) {
-        dd = bk.d[c.mat];
-    }
-    if (OP == OP_GRAM_NORM || OP == OP_NORMALIZE) {
         const float rcp = __frcp_rn(dd);
         coef_x = f2_pack(rcp, rcp);
     }
@@ -334,7 +327,7 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
                 for (int w = 0; w < 4; ++w) xin[w] = lds128(drow + static_cast<uint32_t>(((cc * 4 + w) ^ (r & 7)) << 4));
             }
             float v[32];
-            if (has_acc) tmem_ld_32x32b_x32(tbase + q * 64 + cc * 32, v);
+            tmem_ld_32x32b_x32(tbase + q * 64 + cc * 32, v);
             const int cb = col0 + q * 64 + cc * 32;  // first column of this chunk
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
@@ -350,8 +343,7 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        o[e] = epi_pair<OP>(has_acc ? f2_pack(v[8 * w + 2 * e], v[8 * w + 2 * e + 1]) : 0ull,
-                                            xw[e], coef_x, coef_v, dd);
+                        o[e] = epi_pair<OP>(f2_pack(v[8 * w + 2 * e], v[8 * w + 2 * e + 1]), xw[e], coef_x, coef_v);
                 }
                 if (tma_direct)
                     sts128(drow + static_cast<uint32_t>(((cc * 4 + w) ^ (r & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
@@ -375,7 +367,7 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
                 }
             }
         }
-        if (has_acc && q == 2 * x.grp + 1) {
+        if (q == 2 * x.grp + 1) {
             // the accumulator is free once every epilogue warp of both CTAs has read it
             tc_fence_before();
             __syncwarp();
