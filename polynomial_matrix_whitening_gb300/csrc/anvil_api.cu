@@ -440,7 +440,10 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         cudaError_t ee = profiled(kind, stream, [&] { return launch_cascade(*cp, stream); });
         return ee ? cuda_fail(ee, "cascade launch") : ANVIL_OK;
     };
-    if (!trace) return run_range(0, cp->nruns, ANVIL_KERNEL_CASCADE, 0);
+    if (!trace) {
+        order_normalize_interleaved(cp);
+        return run_range(0, cp->nruns, ANVIL_KERNEL_CASCADE, 0);
+    }
 
     static const int kinds[6] = {ANVIL_KERNEL_GRAM, ANVIL_KERNEL_GRAM_NORM, ANVIL_KERNEL_SQPOLY,
                                  ANVIL_KERNEL_XUPDATE, ANVIL_KERNEL_XUPDATE_OUT, ANVIL_KERNEL_NORMALIZE};

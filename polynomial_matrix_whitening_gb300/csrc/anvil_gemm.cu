@@ -10,24 +10,27 @@
 //   OP_XUPDATE   : Y' = bf16(a Y + B Y)             (OP_XUPDATE_OUT: the last, into out)
 //
 // in the small-side-major layout of anvil_internal.h.  A and B are symmetric: the Gram
-// and A A compute only the upper-triangle 256x256 blocks and store each off-diagonal
-// block twice (itself, and its mirror).  A A contracts A's rows with A's rows (A A =
-// A A^T), so every operand is K-major except Y in the X-update, read MN-major.
+// and A A compute and store only the diagonal and upper 256x256 blocks, and a product
+// operand's k-block left of its diagonal block is read, MN-major, from the transposed
+// upper block.  A A contracts A's rows with A's rows (A A = A A^T), so every operand is
+// K-major except those mirrored k-blocks and Y in the X-update.
 //
 // Work items.  An item is one 256x256 output tile of one matrix in one phase.  The host
 // numbers the items by a list of runs (each: one phase of a range of matrices of one
-// bank) and the persistent grid of CTA pairs takes them in list order: a pair ready for
-// work takes the next item from a global counter, so each pair's items increase.  An item loads nothing before
-// the phases it reads are complete for its matrix: every finished tile adds to a
-// per-matrix completion counter in global memory (a release add once the tile's stores
-// have landed) and an item's loads wait (acquire) until its matrix's counters reach the
-// totals its phase needs (the adds come from a publisher warp, so that no epilogue
-// thread waits for its own stores to drain).  A pair therefore moves on to the next
-// phase of one matrix while other matrices are still in the previous one, with no kernel
-// boundary between the phases.  Each phase of a matrix reads only what the phases before it wrote and
-// waits for all of them, which also orders every reuse of the A, B and Y buffers.
-// An epilogue never blocks on another pair's tile while its own last tile is still
-// unpublished, and the lowest-numbered unfinished item never waits, so the walk always
+// bank) and the persistent grid of CTA pairs takes them in list order: a pair's scheduler
+// warp takes the next item from a global counter, so each pair's items increase.  Every
+// finished tile adds to a per-matrix completion counter in global memory (a release add,
+// once the tile's stores have landed, from a publisher warp, so that no epilogue thread
+// waits for its own stores to drain).  The scheduler hands an item to the pair's other
+// roles only once its matrix's counters reach the totals its phase needs (acquire), as a
+// resolved entry (phase, matrix, block, k-blocks, operand maps) in shared memory: the
+// producer and the MMA issuer, whose work is the critical path, read nothing else at an
+// item boundary.  A pair therefore moves on to the next phase of one matrix while other
+// matrices are still in the previous one, with no kernel boundary between the phases.
+// Each phase of a matrix reads only what the phases before it wrote and waits for all of
+// them, which also orders every reuse of the A, B and Y buffers.  Every entry in a ring
+// can complete without another pair, an epilogue publishes its last tile before it waits
+// for an entry, and the lowest-numbered unfinished item never waits, so the walk always
 // progresses (every pair of the grid is co-resident: one CTA per SM).
 //
 // CTA pairs.  Clusters of two CTAs on two SMs compute a tile with tcgen05.mma.cta_group::2
@@ -37,10 +40,11 @@
 // 5-stage ring; warp 1 allocates 512 TMEM columns in both CTAs and, in the leader only,
 // issues the MMAs into one of two 256-column accumulators, committing to both CTAs'
 // barriers; warps 2-9 (two groups of four, one per column half) run the fused epilogue on
-// the other accumulator; warp 10 publishes finished tiles.  The epilogue input tile (A for B = bA + cAA, Y for the X-update
-// and the normalisation) arrives by TMA into 128x64 boxes (128-byte swizzle), is updated
-// in place with packed f32x2 arithmetic and leaves by TMA store; mirror tiles (and the
-// X^T output of tall banks) leave as plain stores, 64 contiguous bytes per warp.
+// the other accumulator; warp 10 publishes finished tiles; warp 11 (leader CTA) is the
+// pair's scheduler.  The epilogue input tile (A for B = bA + cAA, Y for the X-update)
+// arrives by TMA into 128x64 boxes (128-byte swizzle), is updated
+// in place with packed f32x2 arithmetic and leaves by TMA store; the X^T output of tall
+// banks leaves as plain stores, 64 contiguous bytes per warp.
 //
 // Every wait is bounded (anvil_device.cuh): a wait that gives up sets the device error
 // word and an abort flag; all roles stop, in-flight copies and MMAs are waited for
@@ -86,45 +90,79 @@ struct Item {
 };
 
 // Item schedule of a CTA pair: the leader's scheduler warp takes the pair's next item
-// from the launch's global counter (an atomic add) and writes it into a ring in both
-// CTAs' shared memory; every role of both CTAs reads the ring in order and frees each
-// slot on the leader's barrier.  Items thus go to whichever pair is ready for work, in
-// list order, and each pair's items increase.  The writes need release semantics, which
-// make a thread wait for its own asynchronous copies; the scheduler has none, and the
-// readers free slots with relaxed arrivals (ordered after their read of the slot by a
-// data dependency).
-constexpr int SDEPTH = 4;                         // ring slots
+// from the launch's global counter (an atomic add), decodes it, waits until the phases
+// it reads are complete for its matrix, and writes the resolved entry (a Work) into a
+// ring in both CTAs' shared memory; every role of both CTAs reads the ring in order and
+// frees each slot on the leader's barrier.  Items thus go to whichever pair is ready for
+// work, in list order, and each pair's items increase; no role but the scheduler reads
+// the kernel parameters or the completion counters at an item boundary.  The writes need
+// release semantics, which make a thread wait for its own asynchronous copies; the
+// scheduler has none, and the readers free slots with relaxed arrivals (ordered after
+// their reads of the slot by a data dependency).
+constexpr int SDEPTH = 6;                         // ring slots
+constexpr int SAHEAD = 2;                         // entries the scheduler may run ahead of the producer
 constexpr int SCONSUMERS = 3 + 2 * EPI_GROUPS;    // both producers, the MMA, every epilogue group
 
-struct SchedRing {
+// A resolved item: two 16-byte words.
+//   w0 = {t, op | bank << 8 | ph << 16, mat, nkb}    (t >= the item count: no more work)
+//   w1 = {bi, bj, the operand map slots (map_a, map_a_t, map_b, map_b_t: one byte each), check}
+// where check = ~(the XOR of the other seven words), so that the XOR of all eight is
+// 0xffffffff: a reader derives its arrival count from it, which makes the arrival depend
+// on every word it read (see sched_take).
+struct Work {
+    uint4 w0, w1;
+    __device__ int t() const { return static_cast<int>(w0.x); }
+    __device__ int op() const { return static_cast<int>(w0.y & 0xffu); }
+    __device__ int bank() const { return static_cast<int>((w0.y >> 8) & 0xffu); }
+    __device__ int ph() const { return static_cast<int>(w0.y >> 16); }
+    __device__ int mat() const { return static_cast<int>(w0.z); }
+    __device__ int nkb() const { return static_cast<int>(w0.w); }
+    __device__ int bi() const { return static_cast<int>(w1.x); }
+    __device__ int bj() const { return static_cast<int>(w1.y); }
+    __device__ int map(int k) const { return static_cast<int>(static_cast<int8_t>((w1.z >> (8 * k)) & 0xffu)); }
+};
+
+struct alignas(16) SchedRing {
+    uint4 work[SDEPTH][2];   // read and written as 16-byte words: 16-byte aligned
     uint64_t full[SDEPTH];   // slot written (this CTA)
     uint64_t empty[SDEPTH];  // slot read by every consumer (leader CTA)
     uint64_t taken[SDEPTH];  // slot read by the leader's producer (leader CTA)
-    int item[SDEPTH];
 };
 
-// Scheduler: publishes item t (>= the item count: no more work) as the k-th entry.
-__device__ __forceinline__ bool sched_push(SchedRing& q, int k, int t, unsigned* err) {
+static_assert(offsetof(SchedRing, work) == 0 && alignof(SchedRing) == 16, "ring words need 16-byte alignment");
+
+// Scheduler: publishes w as the k-th entry.
+__device__ __forceinline__ bool sched_push(SchedRing& q, int k, const Work& w, unsigned* err) {
     const int s = k % SDEPTH;
     if (!mbar_wait_cluster(&q.empty[s], ((k / SDEPTH) & 1) ^ 1, err)) return false;
-    q.item[s] = t;
-    st_cluster_u32(map_to_rank(&q.item[s], 1), static_cast<uint32_t>(t));
+    sts128(smem_u32(&q.work[s][0]), w.w0);
+    sts128(smem_u32(&q.work[s][1]), w.w1);
+    st_cluster_v4(map_to_rank(&q.work[s][0], 1), w.w0);
+    st_cluster_v4(map_to_rank(&q.work[s][1], 1), w.w1);
     mbar_arrive_cta(&q.full[s]);
     mbar_arrive_cluster(map_to_rank(&q.full[s], 1));
     return true;
 }
 
-// Any other role: the k-th entry (INT_MAX if the wait gave up).
-__device__ __forceinline__ int sched_take(SchedRing& q, int k, unsigned* err) {
+// Any other role: the k-th entry (t = INT_MAX if the wait gave up).
+__device__ __forceinline__ Work sched_take(SchedRing& q, int k, unsigned* err) {
     const int s = k % SDEPTH;
-    if (!mbar_wait_cluster(&q.full[s], (k / SDEPTH) & 1, err)) return 0x7fffffff;
-    const int t = *reinterpret_cast<volatile int*>(&q.item[s]);
-    const uint32_t one = (static_cast<uint32_t>(t) >> 31) + 1u;  // 1, once t has been read
+    Work w;
+    if (!mbar_wait_cluster(&q.full[s], (k / SDEPTH) & 1, err)) {
+        w.w0 = make_uint4(0x7fffffffu, 0u, 0u, 0u);
+        w.w1 = make_uint4(0u, 0u, 0u, 0u);
+        return w;
+    }
+    w.w0 = lds128(smem_u32(&q.work[s][0]));
+    w.w1 = lds128(smem_u32(&q.work[s][1]));
+    // the arrival count, 1, is computed from every word read (their XOR is 0xffffffff), so
+    // the relaxed arrival cannot overtake the reads of the slot it frees
+    const uint32_t all = w.w0.x ^ w.w0.y ^ w.w0.z ^ w.w0.w ^ w.w1.x ^ w.w1.y ^ w.w1.z ^ w.w1.w;
     asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
                      map_to_rank(&q.empty[s], 0)),
-                 "r"(one)
+                 "r"(all >> 31)
                  : "memory");
-    return t;
+    return w;
 }
 
 // Item t (an index into the call's item list) -> phase, bank, matrix, block row and
@@ -164,6 +202,43 @@ __device__ __forceinline__ Item decode_item(const CascadeParams& p, int t) {
     return it;
 }
 
+__device__ __forceinline__ void work_seal(Work& w) {
+    w.w1.w = ~(w.w0.x ^ w.w0.y ^ w.w0.z ^ w.w0.w ^ w.w1.x ^ w.w1.y ^ w.w1.z);
+}
+
+// The resolved entry of item t of this launch (t >= nitems: the end marker).
+__device__ __forceinline__ Work make_work(const CascadeParams& p, int item0, int nitems, int t) {
+    Work w;
+    w.w0 = make_uint4(static_cast<uint32_t>(t), 0u, 0u, 0u);
+    w.w1 = make_uint4(0u, 0u, 0u, 0u);
+    if (t >= nitems) {
+        work_seal(w);
+        return w;
+    }
+    const Item c = decode_item(p, item0 + t);
+    const CascadePhase& P = p.phase[c.ph];
+    const CascadeBank& bk = p.bank[c.bank];
+    const int nkb = P.op == OP_NORMALIZE ? 0 : (op_gram(P.op) ? bk.L_pad : bk.s_pad) / BK;
+    w.w0 = make_uint4(static_cast<uint32_t>(t), static_cast<uint32_t>(P.op | (c.bank << 8) | (c.ph << 16)),
+                      static_cast<uint32_t>(c.mat), static_cast<uint32_t>(nkb));
+    const uint32_t maps = (static_cast<uint32_t>(P.map_a) & 0xffu) | ((static_cast<uint32_t>(P.map_a_t) & 0xffu) << 8) |
+                          ((static_cast<uint32_t>(P.map_b) & 0xffu) << 16) |
+                          ((static_cast<uint32_t>(P.map_b_t) & 0xffu) << 24);
+    w.w1 = make_uint4(static_cast<uint32_t>(c.bi), static_cast<uint32_t>(c.bj), maps, 0u);
+    work_seal(w);
+    return w;
+}
+
+__device__ __forceinline__ Item work_item(const Work& w) {
+    Item c;
+    c.ph = w.ph();
+    c.bank = w.bank();
+    c.mat = w.mat();
+    c.bi = w.bi();
+    c.bj = w.bj();
+    return c;
+}
+
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -195,6 +270,36 @@ __device__ __forceinline__ bool deps_wait(const CascadeParams& p, const Item& it
     }
     asm volatile("fence.proxy.async.global;" ::: "memory");
     return true;
+}
+
+// This CTA's operand boxes of k-block kb of entry w, loaded by TMA into the stage at `sa`
+// (both CTAs' bytes complete on the leader's barrier `fb`).  CTA rank r holds rows 128r..
+// of the tile's A operand and columns 128r.. of its B operand.  A k-block left of a
+// symmetric operand's diagonal block comes from the upper block it mirrors, read MN-major
+// as two 64 x 64 boxes (k rows, operand rows); the X-update's Y is MN-major too: Y rows
+// kb*64 .. +63, this CTA's 128 columns in two 64-column boxes, 8 KB apart.
+__device__ __forceinline__ void load_kblock(const CascadeParams& p, const Work& w, int kb, uint32_t rank,
+                                            uint8_t* sa, uint32_t fb) {
+    const CUtensorMap* tm = p.bank[w.bank()].tm;
+    const int bi = w.bi(), bj = w.bj(), mat = w.mat();
+    const int arow = bi * PAIR + TILE * static_cast<int>(rank);
+    const int bofs = bj * PAIR + TILE * static_cast<int>(rank);
+    const int map_a = w.map(0), map_a_t = w.map(1), map_b = w.map(2), map_b_t = w.map(3);
+    uint8_t* sb = sa + A_STAGE;
+    if (map_a_t >= 0 && kb * BK < bi * PAIR) {
+        tma_load_3d_pair(sa, &tm[map_a_t], fb, arow, kb * BK, mat);
+        tma_load_3d_pair(sa + 8192, &tm[map_a_t], fb, arow + 64, kb * BK, mat);
+    } else {
+        tma_load_3d_pair(sa, &tm[map_a], fb, kb * BK, arow, mat);
+    }
+    const bool xu = op_xupdate(w.op());
+    if (xu || (map_b_t >= 0 && kb * BK < bj * PAIR)) {
+        const CUtensorMap* tb = &tm[xu ? map_b : map_b_t];
+        tma_load_3d_pair(sb, tb, fb, bofs, kb * BK, mat);
+        tma_load_3d_pair(sb + 8192, tb, fb, bofs + 64, kb * BK, mat);
+    } else {
+        tma_load_3d_pair(sb, &tm[map_b], fb, kb * BK, bofs, mat);
+    }
 }
 
 // The completion counter a finished tile adds to.
@@ -421,8 +526,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
     __shared__ __align__(8) uint64_t mma_done_bar;
     __shared__ __align__(8) uint64_t epi_bar[NQ];  // epilogue input loads, one per quarter
     __shared__ __align__(8) Mailbox mbox;
-    __shared__ __align__(8) SchedRing sring;
-    __shared__ volatile int grp_item[EPI_GROUPS];
+    __shared__ __align__(16) SchedRing sring;
+    // each group's current entry, by iteration parity: the leader writes the next one
+    // while the group may still read this one
+    __shared__ uint4 grp_work[EPI_GROUPS][2][2];
     __shared__ uint32_t tmem_slot;
     __shared__ volatile int aborted;
 
@@ -477,24 +584,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
             // ---------------- TMA producer
             int it = 0;
             for (int k = 0;; ++k) {
-                const int t = sched_take(sring, k, p.err);
-                if (t == 0x7fffffff) aborted = 1;
+                const Work w = sched_take(sring, k, p.err);
+                if (w.t() == 0x7fffffff) aborted = 1;
                 if (rank == 0) mbar_arrive_relaxed(&sring.taken[k % SDEPTH]);
-                if (t >= nitems) break;
-                const Item c = decode_item(p, item0 + t);
-                const CascadePhase& P = p.phase[c.ph];
-                if (P.op == OP_NORMALIZE) continue;
-                const CascadeBank& bk = p.bank[c.bank];
-                if (!deps_wait(p, c)) {
-                    aborted = 1;
-                    break;
-                }
-                const bool xu = op_xupdate(P.op);
-                const CUtensorMap* tma = &bk.tm[P.map_a];
-                const CUtensorMap* tmb = &bk.tm[P.map_b];
-                const int nkb = (op_gram(P.op) ? bk.L_pad : bk.s_pad) / BK;
-                const int arow = c.bi * PAIR + TILE * static_cast<int>(rank);  // this CTA's A rows
-                const int bofs = c.bj * PAIR + TILE * static_cast<int>(rank);  // its B rows / Y columns
+                if (w.t() >= nitems) break;
+                if (w.op() == OP_NORMALIZE) continue;
+                // the scheduler saw the item's inputs complete (acquire); these TMA reads follow
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                const int nkb = w.nkb();
                 bool ok = true;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % STAGES;
@@ -503,30 +600,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                         ok = false;
                         break;
                     }
-                    uint8_t* sa = smem + s * STAGE;
-                    uint8_t* sb = sa + A_STAGE;
-                    // both CTAs' bytes complete on the leader's barrier of this stage
-                    const uint32_t fb = map_to_rank(&full_bar[s], 0);
                     if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * STAGE);
-                    // a k-block left of the operand's diagonal block comes from the upper block
-                    // it mirrors, read MN-major: two 64 x 64 boxes (k rows, operand rows)
-                    if (P.map_a_t >= 0 && kb * BK < c.bi * PAIR) {
-                        tma_load_3d_pair(sa, &bk.tm[P.map_a_t], fb, arow, kb * BK, c.mat);
-                        tma_load_3d_pair(sa + 8192, &bk.tm[P.map_a_t], fb, arow + 64, kb * BK, c.mat);
-                    } else {
-                        tma_load_3d_pair(sa, tma, fb, kb * BK, arow, c.mat);
-                    }
-                    if (xu) {
-                        // Y rows kb*64 .. +63 (the contraction index), this CTA's 128 of the
-                        // tile's columns in two 64-column boxes: MN-major chunks 8 KB apart.
-                        tma_load_3d_pair(sb, tmb, fb, bofs, kb * BK, c.mat);
-                        tma_load_3d_pair(sb + 8192, tmb, fb, bofs + 64, kb * BK, c.mat);
-                    } else if (P.map_b_t >= 0 && kb * BK < c.bj * PAIR) {
-                        tma_load_3d_pair(sb, &bk.tm[P.map_b_t], fb, bofs, kb * BK, c.mat);
-                        tma_load_3d_pair(sb + 8192, &bk.tm[P.map_b_t], fb, bofs + 64, kb * BK, c.mat);
-                    } else {
-                        tma_load_3d_pair(sb, tmb, fb, kb * BK, bofs, c.mat);
-                    }
+                    load_kblock(p, w, kb, rank, smem + s * STAGE, map_to_rank(&full_bar[s], 0));
                     issued = it + 1;
                 }
                 if (!ok) {
@@ -540,15 +615,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
             // ---------------- MMA issuer (leader CTA)
             int it = 0, mt = 0;
             for (int lt = 0;; ++lt) {
-                const int t = sched_take(sring, lt, p.err);
-                if (t == 0x7fffffff) aborted = 1;
-                if (t >= nitems) break;
-                const Item c = decode_item(p, item0 + t);
-                const CascadePhase& P = p.phase[c.ph];
-                if (P.op == OP_NORMALIZE) continue;
-                const CascadeBank& bk = p.bank[c.bank];
-                const bool xu = op_xupdate(P.op);
-                const int nkb = (op_gram(P.op) ? bk.L_pad : bk.s_pad) / BK;
+                const Work w = sched_take(sring, lt, p.err);
+                if (w.t() == 0x7fffffff) aborted = 1;
+                if (w.t() >= nitems) break;
+                if (w.op() == OP_NORMALIZE) continue;
+                const bool xu = op_xupdate(w.op());
+                const int nkb = w.nkb();
+                const int bi = w.bi(), bj = w.bj();
+                const bool a_sym = w.map(1) >= 0, b_sym = w.map(3) >= 0;
                 const int ab = mt & 1;
                 const uint32_t u = static_cast<uint32_t>(mt >> 1);
                 ++mt;
@@ -571,8 +645,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                     const uint32_t b0 = a0 + A_STAGE;
                     // operands staged MN-major: Y in the X-update, and k-blocks read from the
                     // transposed upper block of a symmetric operand (as the producer loaded them)
-                    const bool a_mn = P.map_a_t >= 0 && kb * BK < c.bi * PAIR;
-                    const bool b_mn = xu || (P.map_b_t >= 0 && kb * BK < c.bj * PAIR);
+                    const bool a_mn = a_sym && kb * BK < bi * PAIR;
+                    const bool b_mn = xu || (b_sym && kb * BK < bj * PAIR);
                     const uint32_t idesc = idesc_bf16_f32(PAIR, PAIR, a_mn, b_mn);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
@@ -601,15 +675,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
         if (lane == 0 && rank == 0) {
             // ---------------- scheduler (leader CTA)
             for (int k = 0;; ++k) {
-                // take a pair's next item only once its producer has started the one before:
-                // an item taken early would wait behind this pair's current work
-                if (k > 0 && !mbar_wait(&sring.taken[(k - 1) % SDEPTH], ((k - 1) / SDEPTH) & 1, p.err)) {
+                // take a pair's next item only once its producer has started the one SAHEAD
+                // entries before: an item taken much earlier would wait behind this pair's work
+                if (k >= SAHEAD &&
+                    !mbar_wait(&sring.taken[(k - SAHEAD) % SDEPTH], ((k - SAHEAD) / SDEPTH) & 1, p.err)) {
                     aborted = 1;
                     break;
                 }
                 const unsigned next = aborted ? static_cast<unsigned>(nitems) : atomicAdd(p.next_item, 1u);
-                const int t = next >= static_cast<unsigned>(nitems) ? nitems : static_cast<int>(next);
-                if (!sched_push(sring, k, t, p.err)) {
+                int t = next >= static_cast<unsigned>(nitems) ? nitems : static_cast<int>(next);
+                Work w = make_work(p, item0, nitems, t);
+                // the entry goes out once the phases the item reads are complete for its
+                // matrix, so no role of the pair waits on another pair after taking it
+                if (t < nitems && !deps_wait(p, work_item(w))) {
+                    aborted = 1;
+                    t = nitems;
+                    w = make_work(p, item0, nitems, t);
+                }
+                if (!sched_push(sring, k, w, p.err)) {
                     aborted = 1;
                     break;
                 }
@@ -674,9 +757,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                     send_done(mbox, x, tile_counter(p, pend), p.err);
                     pending = false;
                 }
-                const int tn = sched_take(sring, lt, p.err);
-                if (tn == 0x7fffffff) x.fail = true;
-                grp_item[x.grp] = tn;
+                const Work wn = sched_take(sring, lt, p.err);
+                if (wn.t() == 0x7fffffff) x.fail = true;
+                grp_work[x.grp][lt & 1][0] = wn.w0;
+                grp_work[x.grp][lt & 1][1] = wn.w1;
             }
             // the group stops together: at its last item, or once any wait of any role
             // (or of any thread of the group) gave up
@@ -684,22 +768,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 aborted = 1;
                 break;
             }
-            const int t = grp_item[x.grp];
-            if (t >= nitems) break;
-            const Item c = decode_item(p, item0 + t);
+            Work w;
+            w.w0 = grp_work[x.grp][lt & 1][0];
+            w.w1 = grp_work[x.grp][lt & 1][1];
+            if (w.t() >= nitems) break;
+            const Item c = work_item(w);
             const CascadePhase& P = p.phase[c.ph];
             const CascadeBank& bk = p.bank[c.bank];
-            const int op = P.op;
-            // what the tile reads must be complete; never block on other pairs while this
-            // group's last tile is unpublished
-            if (x.leader && !deps_ready(p, c)) {
-                if (pending) {
-                    bulk_wait_all();
-                    send_done(mbox, x, tile_counter(p, pend), p.err);
-                    pending = false;
-                }
-                if (!deps_wait(p, c)) x.fail = true;
-            }
+            const int op = w.op();
             const uint32_t in_phase = static_cast<uint32_t>(epi_tiles) & 1u;
             if (!op_gram(op) && op != OP_NORMALIZE) {
                 // the group's quarters of the tile's input, once the group's earlier TMA
