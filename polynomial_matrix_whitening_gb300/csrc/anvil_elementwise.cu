@@ -169,10 +169,14 @@ cudaError_t launch_momentum(const MomentumParams& p, cudaStream_t stream) {
 static_assert(SCHED_COUNTERS <= 256, "norm_d_kernel zeroes the item counters with one block");
 
 // One block per matrix.  Diagonal entry i of the first Gram is the fp32 sum of the
-// squares of row i of Y, rounded to bf16 as the page stores the Gram; the trace sums
-// those in fp32.
-__global__ void __launch_bounds__(256) norm_d_kernel(const __grid_constant__ NormParams p) {
-    __shared__ float red[256];
+// squares of row i of Y (the momentum kernel's per-64-column partials, summed here in
+// column-block order), rounded to bf16 as the page stores the Gram; the trace sums those
+// in fp32 (a fixed order: per thread, then per warp by shuffles, then over the warps).
+// A thread's partial loads go out eight at a time, so a row costs a few memory round
+// trips rather than one per column block.
+constexpr int NORM_THREADS = 1024;
+__global__ void __launch_bounds__(NORM_THREADS) norm_d_kernel(const __grid_constant__ NormParams p) {
+    __shared__ float red[NORM_THREADS / 32];
     pdl_allow_next();
     pdl_wait_previous();
     const int gm = blockIdx.x;
@@ -186,25 +190,34 @@ __global__ void __launch_bounds__(256) norm_d_kernel(const __grid_constant__ Nor
     if (gm == 0 && threadIdx.x < SCHED_COUNTERS) p.counters[2 * p.total_mats + threadIdx.x] = 0u;
     const float* part = B.part + static_cast<size_t>(lm) * B.nlb * B.s_pad;  // [nlb][s_pad]
     float acc = 0.f;
-    for (int i = threadIdx.x; i < B.s_pad; i += blockDim.x) {
+    for (int i = threadIdx.x; i < B.s_pad; i += NORM_THREADS) {
+        const float* col = part + i;
         float s = 0.f;
-        for (int lb = 0; lb < B.nlb; ++lb) s = __fadd_rn(s, part[static_cast<size_t>(lb) * B.s_pad + i]);
+        int lb = 0;
+        for (; lb + 8 <= B.nlb; lb += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = col[static_cast<size_t>(lb + u) * B.s_pad];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s = __fadd_rn(s, v[u]);
+        }
+        for (; lb < B.nlb; ++lb) s = __fadd_rn(s, col[static_cast<size_t>(lb) * B.s_pad]);
         acc = __fadd_rn(acc, round_bf(s));
     }
-    red[threadIdx.x] = acc;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
     __syncthreads();
-    for (int w = 128; w > 0; w >>= 1) {
-        if (threadIdx.x < w) red[threadIdx.x] = __fadd_rn(red[threadIdx.x], red[threadIdx.x + w]);
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-        const float tr = red[0];
-        p.d[gm] = __fadd_rn(__fmul_rn(__fsqrt_rn(tr), p.margin), p.eps);
+    if (threadIdx.x < 32) {
+        float w = red[threadIdx.x];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) w = __fadd_rn(w, __shfl_xor_sync(0xffffffffu, w, o));
+        if (threadIdx.x == 0) p.d[gm] = __fadd_rn(__fmul_rn(__fsqrt_rn(w), p.margin), p.eps);
     }
 }
 
 cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream) {
-    return launch_pdl(norm_d_kernel, dim3(p.total_mats), dim3(256), 0, stream, p);
+    return launch_pdl(norm_d_kernel, dim3(p.total_mats), dim3(NORM_THREADS), 0, stream, p);
 }
 
 // ---------------------------------------------------------------- tracing
