@@ -17,16 +17,32 @@
 
 #include "../../include/anvil.h"
 #include "anvil_device.cuh"
+#include "anvil_internal.h"
 #include "anvil_tail.h"
 
 namespace anvil {
 
 // ---------------------------------------------------------------- lane powers
-// Lanes along rows (m >= n): one warp per (matrix, row), lanes of the warp stride the
-// columns; a fixed shuffle tree adds the 32 partial sums.
-// Lanes along columns (m < n): a block covers 32 columns of one matrix with 8 row
-// slices; slice k sums rows k, k+8, ...; the 8 slice sums are added in order.
+// Lanes along rows (m >= n): one warp per (matrix, row).  With the vector layout (n % 8
+// == 0, 16-byte aligned) lane k of the warp takes 8-element chunks k, k + 32, ... (one
+// 16-byte load each), otherwise single elements k, k + 32, ...; a fixed shuffle tree adds
+// the 32 partial sums.
+// Lanes along columns (m < n): a block covers 256 columns of one matrix (8 per thread with
+// the vector layout, else 32 columns) with 8 row slices; slice k sums rows k, k + 8, ...;
+// the slice sums of a column are added in slice order.
+constexpr int POWER_COLS = 256;  // columns per block, lanes along columns, vector layout
+__device__ __forceinline__ float sumsq8(uint4 q, float s) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float x = bf2f(static_cast<uint16_t>((k & 1) ? w[k >> 1] >> 16 : w[k >> 1] & 0xffffu));
+        s = __fadd_rn(s, __fmul_rn(x, x));
+    }
+    return s;
+}
 __global__ void __launch_bounds__(256) lane_power_kernel(const __grid_constant__ TailParams p) {
+    pdl_allow_next();
+    pdl_wait_previous();
     const int b = blockIdx.y;
     const TailBank& B = p.bank[b];
     const int mn = B.m * B.n;
@@ -37,40 +53,79 @@ __global__ void __launch_bounds__(256) lane_power_kernel(const __grid_constant__
         const int mat = static_cast<int>(warp_id / B.m), row = static_cast<int>(warp_id % B.m);
         const uint16_t* v = B.update + static_cast<size_t>(mat) * mn + static_cast<size_t>(row) * B.n;
         float s = 0.f;
-        for (int j = lane; j < B.n; j += 32) {
-            const float x = bf2f(v[j]);
-            s = __fadd_rn(s, __fmul_rn(x, x));
+        if (B.vec8) {
+            const uint4* v4 = reinterpret_cast<const uint4*>(v);
+            const int nc = B.n / 8;
+#pragma unroll 4
+            for (int j = lane; j < nc; j += 32) s = sumsq8(__ldcs(v4 + j), s);
+        } else {
+            for (int j = lane; j < B.n; j += 32) {
+                const float x = bf2f(v[j]);
+                s = __fadd_rn(s, __fmul_rn(x, x));
+            }
         }
 #pragma unroll
         for (int off = 16; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
         if (lane == 0) B.power[static_cast<size_t>(mat) * B.m + row] = __fdiv_rn(s, static_cast<float>(B.n));
     } else {
-        __shared__ float part[8][33];
-        const int cblocks = (B.n + 31) / 32;
+        __shared__ float part[8][POWER_COLS + 1];
+        const int span = B.vec8 ? POWER_COLS : 32;  // columns per block
+        const int cblocks = (B.n + span - 1) / span;
         if (blockIdx.x >= static_cast<unsigned>(B.g * cblocks)) return;
-        const int mat = blockIdx.x / cblocks, c0 = (blockIdx.x % cblocks) * 32;
+        const int mat = blockIdx.x / cblocks, c0 = (blockIdx.x % cblocks) * span;
         const int cx = threadIdx.x & 31, slice = threadIdx.x >> 5;
-        const int col = c0 + cx;
         const uint16_t* v = B.update + static_cast<size_t>(mat) * mn;
-        float s = 0.f;
-        if (col < B.n)
-            for (int i = slice; i < B.m; i += 8) {
-                const float x = bf2f(v[static_cast<size_t>(i) * B.n + col]);
-                s = __fadd_rn(s, __fmul_rn(x, x));
+        if (B.vec8) {
+            // thread: columns c0 + 8 cx .. +7 (n % 8 == 0, so a chunk is in or out whole)
+            const int col = c0 + 8 * cx;
+            float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (col < B.n)
+                for (int i = slice; i < B.m; i += 8) {
+                    const uint4 q = __ldcs(reinterpret_cast<const uint4*>(v + static_cast<size_t>(i) * B.n + col));
+                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float x = bf2f(static_cast<uint16_t>((k & 1) ? w[k >> 1] >> 16 : w[k >> 1] & 0xffffu));
+                        s[k] = __fadd_rn(s[k], __fmul_rn(x, x));
+                    }
+                }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) part[slice][8 * cx + k] = s[k];
+            __syncthreads();
+            const int c = c0 + threadIdx.x;  // one column per thread
+            if (c < B.n) {
+                float t = part[0][threadIdx.x];
+                for (int k = 1; k < 8; ++k) t = __fadd_rn(t, part[k][threadIdx.x]);
+                B.power[static_cast<size_t>(mat) * B.n + c] = __fdiv_rn(t, static_cast<float>(B.m));
             }
-        part[slice][cx] = s;
-        __syncthreads();
-        if (slice == 0 && col < B.n) {
-            float t = part[0][cx];
-            for (int k = 1; k < 8; ++k) t = __fadd_rn(t, part[k][cx]);
-            B.power[static_cast<size_t>(mat) * B.n + col] = __fdiv_rn(t, static_cast<float>(B.m));
+        } else {
+            const int col = c0 + cx;
+            float s = 0.f;
+            if (col < B.n)
+                for (int i = slice; i < B.m; i += 8) {
+                    const float x = bf2f(v[static_cast<size_t>(i) * B.n + col]);
+                    s = __fadd_rn(s, __fmul_rn(x, x));
+                }
+            part[slice][cx] = s;
+            __syncthreads();
+            if (slice == 0 && col < B.n) {
+                float t = part[0][cx];
+                for (int k = 1; k < 8; ++k) t = __fadd_rn(t, part[k][cx]);
+                B.power[static_cast<size_t>(mat) * B.n + col] = __fdiv_rn(t, static_cast<float>(B.m));
+            }
         }
     }
 }
 
 // ---------------------------------------------------------------- lane scales
-__global__ void __launch_bounds__(256) lane_scale_kernel(const __grid_constant__ TailParams p) {
-    __shared__ float red_p[256], red_q[256];
+// One block per matrix; sums in a fixed order (per thread, per warp by shuffles, then
+// over the warps).
+constexpr int SCALE_THREADS = 1024;
+__global__ void __launch_bounds__(SCALE_THREADS) lane_scale_kernel(const __grid_constant__ TailParams p) {
+    __shared__ float red_p[SCALE_THREADS / 32], red_q[SCALE_THREADS / 32];
+    __shared__ float ratio_s;
+    pdl_allow_next();
+    pdl_wait_previous();
     const int gm = blockIdx.x;
     int bi = 0;
 #pragma unroll 1
@@ -85,30 +140,43 @@ __global__ void __launch_bounds__(256) lane_scale_kernel(const __grid_constant__
     float* E = B.lane_energy + static_cast<size_t>(mat) * nl;
     float* S = B.scale + static_cast<size_t>(mat) * nl;
     float sp = 0.f, sq = 0.f;
-    for (int l = threadIdx.x; l < nl; l += blockDim.x) {
+    for (int l = threadIdx.x; l < nl; l += SCALE_THREADS) {
         const float pw = P[l];
-        const float e = __fadd_rn(E[l], __fmul_rn(w, __fsub_rn(pw, E[l])));
+        const float e0 = E[l];
+        const float e = __fadd_rn(e0, __fmul_rn(w, __fsub_rn(pw, e0)));
         E[l] = e;
         const float gain = __frsqrt_rn(e > 1e-10f ? e : 1e-10f);
         S[l] = gain;
         sp = __fadd_rn(sp, pw);
         sq = __fadd_rn(sq, __fmul_rn(__fmul_rn(pw, len), __fmul_rn(gain, gain)));
     }
-    red_p[threadIdx.x] = sp;
-    red_q[threadIdx.x] = sq;
-    __syncthreads();
-    for (int k = blockDim.x / 2; k > 0; k >>= 1) {
-        if (threadIdx.x < k) {
-            red_p[threadIdx.x] = __fadd_rn(red_p[threadIdx.x], red_p[threadIdx.x + k]);
-            red_q[threadIdx.x] = __fadd_rn(red_q[threadIdx.x], red_q[threadIdx.x + k]);
-        }
-        __syncthreads();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        sp = __fadd_rn(sp, __shfl_xor_sync(0xffffffffu, sp, o));
+        sq = __fadd_rn(sq, __shfl_xor_sync(0xffffffffu, sq, o));
     }
-    const float pre = __fsqrt_rn(__fmul_rn(red_p[0], len));
-    float post = __fsqrt_rn(red_q[0]);
-    if (post < 1e-10f) post = 1e-10f;
-    const float ratio = __fdiv_rn(pre, post);
-    for (int l = threadIdx.x; l < nl; l += blockDim.x) S[l] = round_bf(__fmul_rn(S[l], ratio));
+    if ((threadIdx.x & 31) == 0) {
+        red_p[threadIdx.x >> 5] = sp;
+        red_q[threadIdx.x >> 5] = sq;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float a = red_p[threadIdx.x], c = red_q[threadIdx.x];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, o));
+            c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, c, o));
+        }
+        if (threadIdx.x == 0) {
+            const float pre = __fsqrt_rn(__fmul_rn(a, len));
+            float post = __fsqrt_rn(c);
+            if (post < 1e-10f) post = 1e-10f;
+            ratio_s = __fdiv_rn(pre, post);
+        }
+    }
+    __syncthreads();
+    const float ratio = ratio_s;
+    for (int l = threadIdx.x; l < nl; l += SCALE_THREADS) S[l] = round_bf(__fmul_rn(S[l], ratio));
 }
 
 // ---------------------------------------------------------------- equalise + decay update
@@ -126,6 +194,8 @@ __device__ __forceinline__ void tail_element(float v, float scale, float gate, f
 
 // Eight consecutive elements of one row per thread, grid-stride over all banks.
 __global__ void __launch_bounds__(256) tail_apply_kernel(const __grid_constant__ TailParams p) {
+    pdl_allow_next();
+    pdl_wait_previous();
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < p.total_chunks;
          t += stride) {
@@ -186,26 +256,24 @@ cudaError_t launch_tail_power(const TailParams& p, cudaStream_t stream) {
     unsigned gx = 1;
     for (int i = 0; i < p.nbanks; ++i) {
         const TailBank& B = p.bank[i];
+        const int span = B.vec8 ? POWER_COLS : 32;
         const unsigned need = B.m >= B.n
                                   ? static_cast<unsigned>((static_cast<long long>(B.g) * B.m * 32 + 255) / 256)
-                                  : static_cast<unsigned>(B.g * ((B.n + 31) / 32));
+                                  : static_cast<unsigned>(B.g * ((B.n + span - 1) / span));
         if (need > gx) gx = need;
     }
-    lane_power_kernel<<<dim3(gx, p.nbanks), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(lane_power_kernel, dim3(gx, p.nbanks), dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_tail_scale(const TailParams& p, cudaStream_t stream) {
-    lane_scale_kernel<<<p.total_mats, 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(lane_scale_kernel, dim3(p.total_mats), dim3(SCALE_THREADS), 0, stream, p);
 }
 
 cudaError_t launch_tail_apply(const TailParams& p, cudaStream_t stream) {
     long long blocks = (p.total_chunks + 255) / 256;
     if (blocks > 152 * 8) blocks = 152 * 8;
     if (blocks < 1) blocks = 1;
-    tail_apply_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(tail_apply_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
 }
 
 }  // namespace anvil
