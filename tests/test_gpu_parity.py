@@ -283,6 +283,43 @@ def test_grouped_banks_equal_separate_calls(A):
         assert torch.equal(o.view(torch.int16), banks[2].out[i:i + 1].view(torch.int16))
 
 
+@pytest.mark.parametrize("shapes", [
+    # 400 matrices: the normalisation interleaved with the first products, one run per
+    # matrix and phase before the first X-update (about 1260 runs)
+    [(200, 24, 16), (120, 8, 40), (80, 20, 20)],
+    # 1000 matrices: past the run table, the plain phase-major order
+    [(500, 24, 16), (300, 8, 40), (200, 20, 20)],
+], ids=["400_matrices", "1000_matrices"])
+def test_many_matrices_item_order(A, shapes):
+    """The item order of a call with hundreds of matrices (one run per matrix near the
+    run table's capacity, and the fallback past it): the grouped call equals one call per
+    bank bit for bit, and sampled matrices match the oracle."""
+    banks, solo, cases = [], [], []
+    for j, (g, m, n) in enumerate(shapes):
+        grad, vel = W.random_case(900 + j, g, m, n)
+        sc = dict(momentum=0.95, fast_beta=0.85, fast_weight=0.4385, slow_beta=0.98)
+        banks.append(gpu_bank(A, grad, vel, sc))
+        solo.append(gpu_bank(A, grad, vel, sc))
+        cases.append((grad, vel, sc))
+    A.multi_bank_step(banks, A.alloc_workspace(shapes))
+    for b, s in zip(solo, shapes):
+        A.multi_bank_step([b], A.alloc_workspace([s]))
+    torch.cuda.synchronize()
+    assert A.device_error() == A.OK
+    for j, (b, s) in enumerate(zip(banks, solo)):
+        assert torch.equal(b.out.view(torch.int16), s.out.view(torch.int16))
+        assert torch.equal(b.velocity, s.velocity)
+        grad, vel, sc = cases[j]
+        g = grad.shape[0]
+        pick = [0, g // 2, g - 1]
+        out_or, vel_or = oracle.bank_step(grad[pick], vel[:, pick], sc["momentum"], sc["fast_beta"],
+                                          sc["fast_weight"], sc["slow_beta"])
+        got = bits(b.out)[pick]
+        np.testing.assert_array_equal(b.velocity[:, pick].cpu().numpy(), vel_or)
+        for k in range(len(pick)):
+            assert rel(f64(got[k]), f64(out_or[k])) <= OUT_RTOL
+
+
 def test_cuda_graph_with_device_scalars(A):
     """A captured step reads the device scalar block when it runs: replays with new
     scalars equal eager calls with those scalars as host values."""
