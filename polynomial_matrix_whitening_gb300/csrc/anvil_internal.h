@@ -92,9 +92,9 @@ cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream);
 // ---------------------------------------------------------------- the cascade kernel
 // One persistent tcgen05 kernel walks every phase of the cascade (anvil_gemm.cu).
 enum PhaseOp : int {
-    OP_GRAM = 0,        // A = bf16(Y Y^T)                    (upper tiles, mirrored)
+    OP_GRAM = 0,        // A = bf16(Y Y^T)                    (diagonal and upper 256-blocks)
     OP_GRAM_NORM = 1,   // A = bf16(bf16(Y Y^T) / d^2)        (the first Gram, on X_raw)
-    OP_SQPOLY = 2,      // B = bf16(b A + c A A)              (upper tiles, mirrored)
+    OP_SQPOLY = 2,      // B = bf16(b A + c A A)              (diagonal and upper 256-blocks)
     OP_XUPDATE = 3,     // Y' = bf16(a Y + B Y)
     OP_XUPDATE_OUT = 4, // the same, written to out in the natural [m, n] layout
     OP_NORMALIZE = 5    // Y1 = bf16(Y0 / d)                  (no product)
