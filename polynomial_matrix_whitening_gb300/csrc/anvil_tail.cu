@@ -23,14 +23,17 @@
 namespace anvil {
 
 // ---------------------------------------------------------------- lane powers
-// Lanes along rows (m >= n): one warp per (matrix, row).  With the vector layout (n % 8
-// == 0, 16-byte aligned) lane k of the warp takes 8-element chunks k, k + 32, ... (one
-// 16-byte load each), otherwise single elements k, k + 32, ...; a fixed shuffle tree adds
-// the 32 partial sums.
+// One grid over every bank (a block finds its bank from power_begin).
+// Lanes along rows (m >= n): each warp sums POWER_ROWS consecutive rows of the bank (rows
+// of consecutive matrices are contiguous); with the vector layout (n % 8 == 0, 16-byte
+// aligned) lane k takes 8-element chunks k, k + 32, ... of every row, the rows' loads in
+// flight together, otherwise single elements; a fixed shuffle tree adds each row's 32
+// partial sums.
 // Lanes along columns (m < n): a block covers 256 columns of one matrix (8 per thread with
 // the vector layout, else 32 columns) with 8 row slices; slice k sums rows k, k + 8, ...;
 // the slice sums of a column are added in slice order.
 constexpr int POWER_COLS = 256;  // columns per block, lanes along columns, vector layout
+constexpr int POWER_ROWS = 4;    // rows per warp, lanes along rows
 __device__ __forceinline__ float sumsq8(uint4 q, float s) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -40,41 +43,65 @@ __device__ __forceinline__ float sumsq8(uint4 q, float s) {
     }
     return s;
 }
+__host__ __device__ inline long long power_blocks(const TailBank& B) {
+    if (B.m >= B.n) return (static_cast<long long>(B.g) * B.m + 8 * POWER_ROWS - 1) / (8 * POWER_ROWS);
+    const int span = B.vec8 ? POWER_COLS : 32;
+    return static_cast<long long>(B.g) * ((B.n + span - 1) / span);
+}
 __global__ void __launch_bounds__(256) lane_power_kernel(const __grid_constant__ TailParams p) {
     pdl_allow_next();
     pdl_wait_previous();
-    const int b = blockIdx.y;
+    const long long blk = blockIdx.x;
+    int b = 0;
+#pragma unroll 1
+    for (int i = 1; i < p.nbanks; ++i)
+        if (blk >= p.bank[i].power_begin) b = i;
     const TailBank& B = p.bank[b];
-    const int mn = B.m * B.n;
+    const long long lb = blk - B.power_begin;
     if (B.m >= B.n) {
-        const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-        const int lane = threadIdx.x & 31;
-        if (warp_id >= static_cast<long long>(B.g) * B.m) return;
-        const int mat = static_cast<int>(warp_id / B.m), row = static_cast<int>(warp_id % B.m);
-        const uint16_t* v = B.update + static_cast<size_t>(mat) * mn + static_cast<size_t>(row) * B.n;
-        float s = 0.f;
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const long long nrows = static_cast<long long>(B.g) * B.m;
+        const long long row0 = (lb * 8 + warp) * POWER_ROWS;  // row (mat * m + row) of the bank
+        if (row0 >= nrows) return;  // whole warp
+        float s[POWER_ROWS];
+#pragma unroll
+        for (int k = 0; k < POWER_ROWS; ++k) s[k] = 0.f;
         if (B.vec8) {
-            const uint4* v4 = reinterpret_cast<const uint4*>(v);
             const int nc = B.n / 8;
-#pragma unroll 4
-            for (int j = lane; j < nc; j += 32) s = sumsq8(__ldcs(v4 + j), s);
+            for (int j = lane; j < nc; j += 32) {
+                uint4 q[POWER_ROWS];
+#pragma unroll
+                for (int k = 0; k < POWER_ROWS; ++k)
+                    q[k] = row0 + k < nrows
+                               ? __ldcs(reinterpret_cast<const uint4*>(B.update + static_cast<size_t>(row0 + k) * B.n) + j)
+                               : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int k = 0; k < POWER_ROWS; ++k) s[k] = sumsq8(q[k], s[k]);
+            }
         } else {
-            for (int j = lane; j < B.n; j += 32) {
-                const float x = bf2f(v[j]);
-                s = __fadd_rn(s, __fmul_rn(x, x));
+#pragma unroll
+            for (int k = 0; k < POWER_ROWS; ++k) {
+                if (row0 + k >= nrows) break;
+                const uint16_t* v = B.update + static_cast<size_t>(row0 + k) * B.n;
+                for (int j = lane; j < B.n; j += 32) {
+                    const float x = bf2f(v[j]);
+                    s[k] = __fadd_rn(s[k], __fmul_rn(x, x));
+                }
             }
         }
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xffffffffu, s, off));
-        if (lane == 0) B.power[static_cast<size_t>(mat) * B.m + row] = __fdiv_rn(s, static_cast<float>(B.n));
+        for (int k = 0; k < POWER_ROWS; ++k) {
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) s[k] = __fadd_rn(s[k], __shfl_xor_sync(0xffffffffu, s[k], off));
+            if (lane == 0 && row0 + k < nrows) B.power[row0 + k] = __fdiv_rn(s[k], static_cast<float>(B.n));
+        }
     } else {
         __shared__ float part[8][POWER_COLS + 1];
         const int span = B.vec8 ? POWER_COLS : 32;  // columns per block
         const int cblocks = (B.n + span - 1) / span;
-        if (blockIdx.x >= static_cast<unsigned>(B.g * cblocks)) return;
-        const int mat = blockIdx.x / cblocks, c0 = (blockIdx.x % cblocks) * span;
+        const int mat = static_cast<int>(lb / cblocks), c0 = static_cast<int>(lb % cblocks) * span;
         const int cx = threadIdx.x & 31, slice = threadIdx.x >> 5;
-        const uint16_t* v = B.update + static_cast<size_t>(mat) * mn;
+        const uint16_t* v = B.update + static_cast<size_t>(mat) * B.m * B.n;
         if (B.vec8) {
             // thread: columns c0 + 8 cx .. +7 (n % 8 == 0, so a chunk is in or out whole)
             const int col = c0 + 8 * cx;
@@ -252,17 +279,15 @@ __global__ void __launch_bounds__(256) tail_apply_kernel(const __grid_constant__
 }
 
 cudaError_t launch_tail_power(const TailParams& p, cudaStream_t stream) {
-    // grid.x covers the largest bank, grid.y the banks
-    unsigned gx = 1;
-    for (int i = 0; i < p.nbanks; ++i) {
-        const TailBank& B = p.bank[i];
-        const int span = B.vec8 ? POWER_COLS : 32;
-        const unsigned need = B.m >= B.n
-                                  ? static_cast<unsigned>((static_cast<long long>(B.g) * B.m * 32 + 255) / 256)
-                                  : static_cast<unsigned>(B.g * ((B.n + span - 1) / span));
-        if (need > gx) gx = need;
+    TailParams q = p;
+    long long blocks = 0;
+    for (int i = 0; i < q.nbanks; ++i) {
+        q.bank[i].power_begin = blocks;
+        blocks += power_blocks(q.bank[i]);
     }
-    return launch_pdl(lane_power_kernel, dim3(gx, p.nbanks), dim3(256), 0, stream, p);
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    return launch_pdl(lane_power_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, q);
 }
 
 cudaError_t launch_tail_scale(const TailParams& p, cudaStream_t stream) {
