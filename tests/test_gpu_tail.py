@@ -84,6 +84,31 @@ def test_tail_matches_oracle(A, shape):
     assert A.device_error() == A.OK
 
 
+def test_grouped_tail_over_mixed_banks(A):
+    """One tail call over four banks (lanes along rows and along columns, the 16-byte and
+    the element path, a tiny bank) matches the oracle bank by bank, and equals one call
+    per bank bit for bit."""
+    shapes = [(5, 300, 136), (4, 72, 264), (3, 130, 99), (2, 3, 5)]
+    wd, beta2 = 0.1, 0.95
+    ins = [tail_inputs(700 + j, *s) for j, s in enumerate(shapes)]
+    def tails():
+        return [A.Tail(to_dev(u), to_dev(v), to_dev(le), to_dev(p), torch.from_numpy(mt.view(np.int16)).cuda(),
+                       to_dev(lr), wd, beta2) for (u, v, le, p, mt, lr) in ins]
+    grouped, solo = tails(), tails()
+    A.update_tail(grouped, torch.empty(A.tail_workspace_bytes(shapes), dtype=torch.uint8, device="cuda"))
+    for t, s in zip(solo, shapes):
+        A.update_tail([t], torch.empty(A.tail_workspace_bytes([s]), dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert A.device_error() == A.OK
+    for t, u, (upd, vel, le, p, mt, lr) in zip(grouped, solo, ins):
+        assert torch.equal(t.param.view(torch.int16), u.param.view(torch.int16))
+        assert torch.equal(t.mantissa, u.mantissa)
+        assert torch.equal(t.lane_energy, u.lane_energy)
+        p_o, mt_o, le_o, _ = oracle.update_tail(upd, le, beta2, p, mt, vel[1], wd, lr)
+        check(t.param.view(torch.int16).cpu().numpy().view(np.uint16), t.mantissa.cpu().numpy().view(np.uint16),
+              t.lane_energy.cpu().numpy(), p_o, mt_o, le_o, upd, lr)
+
+
 def test_tail_twice_accumulates_lane_energy(A):
     shape = (3, 96, 160)
     upd, vel, le, p, mt, lr = tail_inputs(11, *shape)
