@@ -264,6 +264,24 @@ typedef struct { int kind; float ms; } anvil_profile_record;
 anvil_status anvil_profile_begin(int max_records);
 int anvil_profile_end(anvil_profile_record* records, int cap);
 
+/* Diagnostic, host only (no CUDA call, no GPU needed): the order in which the cascade
+ * kernel of anvil_multi_bank_step walks its work items for these banks and nmaps maps.
+ * Items are 256 x 256 output tiles; the kernel's phases are the first Gram, the
+ * normalisation, then per map the Gram (after the first map), B = bA + cA^2 and the
+ * X-update.  The order is a list of runs, each one phase of a range of matrices of one
+ * bank, matrix by matrix; every phase of a matrix comes after the phases it reads.
+ * Writes up to cap runs and returns how many there are (-1 on invalid arguments). */
+typedef struct {
+    int phase;  /* phase index, 0 = the first Gram */
+    int op;     /* 0 Gram, 1 first Gram, 2 B = bA + cA^2, 3 X-update, 4 last X-update, 5 normalisation */
+    int bank;   /* index of the bank in the call */
+    int mat0;   /* first matrix of the run */
+    int nmat;   /* matrices in the run */
+    int begin;  /* index of the run's first item in the walk */
+    int tiles;  /* items per matrix in this phase */
+} anvil_schedule_run;
+int anvil_schedule_runs(const anvil_bank_desc* banks, int nbanks, int nmaps, anvil_schedule_run* runs, int cap);
+
 /* Human-readable name of a status. */
 const char* anvil_status_string(anvil_status status);
 

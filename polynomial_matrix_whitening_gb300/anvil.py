@@ -70,6 +70,11 @@ class TailDesc(ctypes.Structure):
                 ("eff_wd", ctypes.c_float), ("beta2", ctypes.c_float)]
 
 
+class ScheduleRun(ctypes.Structure):
+    _fields_ = [("phase", ctypes.c_int), ("op", ctypes.c_int), ("bank", ctypes.c_int), ("mat0", ctypes.c_int),
+                ("nmat", ctypes.c_int), ("begin", ctypes.c_int), ("tiles", ctypes.c_int)]
+
+
 class ProfileRecord(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("ms", ctypes.c_float)]
 
@@ -104,6 +109,8 @@ _lib.anvil_profile_begin.argtypes = [_i]
 _lib.anvil_profile_begin.restype = _i
 _lib.anvil_profile_end.argtypes = [ctypes.POINTER(ProfileRecord), _i]
 _lib.anvil_profile_end.restype = _i
+_lib.anvil_schedule_runs.argtypes = [ctypes.POINTER(BankDesc), _i, _i, ctypes.POINTER(ScheduleRun), _i]
+_lib.anvil_schedule_runs.restype = _i
 _lib.anvil_status_string.argtypes = [_i]
 _lib.anvil_status_string.restype = ctypes.c_char_p
 _lib.anvil_last_cuda_error.restype = ctypes.c_char_p
@@ -323,6 +330,18 @@ def adam_step(param, grad, exp_avg, exp_avg_sq, beta1, beta2, eps, step_size, ef
     st = _lib.anvil_adam_step(param.data_ptr(), grad.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(),
                               param.numel(), beta1, beta2, eps, step_size, eff_wd, _stream_arg(stream))
     _check(st, "anvil_adam_step")
+
+
+def schedule_runs(shapes, nmaps=6):
+    """The cascade kernel's item order for banks of these (g, m, n) shapes (host only, no
+    GPU needed): a list of dicts with phase, op, bank, mat0, nmat, begin, tiles."""
+    arr = (BankDesc * len(shapes))(*[_raw_desc(g, m, n) for g, m, n in shapes])
+    n = _lib.anvil_schedule_runs(arr, len(shapes), nmaps, None, 0)
+    if n < 0:
+        raise AnvilError(ERR_INVALID_ARG, "anvil_schedule_runs")
+    runs = (ScheduleRun * max(n, 1))()
+    _lib.anvil_schedule_runs(arr, len(shapes), nmaps, runs, n)
+    return [{f: getattr(r, f) for f, _ in ScheduleRun._fields_} for r in runs[:n]]
 
 
 def device_error(clear=True):

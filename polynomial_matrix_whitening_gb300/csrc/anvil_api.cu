@@ -21,6 +21,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <new>
 
 
 #include "../../include/anvil.h"
@@ -151,6 +152,17 @@ struct Layout {
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// The cascade kernel's bank order: the call's banks, heaviest tiles first (they open
+// every phase), ties in call order.
+void cascade_bank_order(const Geom* bank, int nbanks, int* order) {
+    for (int i = 0; i < nbanks; ++i) order[i] = i;
+    std::stable_sort(order, order + nbanks, [&](int x, int y) {
+        const long long wx = static_cast<long long>(bank[x].s_pad) * bank[x].L_pad;
+        const long long wy = static_cast<long long>(bank[y].s_pad) * bank[y].L_pad;
+        return wx > wy;
+    });
+}
 
 anvil_status make_layout(const anvil_bank_desc* banks, int nbanks, Layout* L) {
     if (!banks || nbanks < 1 || nbanks > ANVIL_MAX_BANKS) return ANVIL_ERR_INVALID_ARG;
@@ -399,14 +411,8 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
     cp->norm = cp->chain + L.total_mats;
     unsigned* sched_ctr = cp->norm + L.total_mats;  // [SCHED_COUNTERS]
     cp->err = dev->err;
-    // banks in the call's order, heaviest tiles first (the first items of each phase)
     int order[ANVIL_MAX_BANKS];
-    for (int i = 0; i < nbanks; ++i) order[i] = i;
-    std::stable_sort(order, order + nbanks, [&](int x, int y) {
-        const long long wx = static_cast<long long>(L.bank[x].s_pad) * L.bank[x].L_pad;
-        const long long wy = static_cast<long long>(L.bank[y].s_pad) * L.bank[y].L_pad;
-        return wx > wy;
-    });
+    cascade_bank_order(L.bank, nbanks, order);
     for (int q = 0; q < nbanks; ++q) {
         const int i = order[q];
         const Geom& G = L.bank[i];
@@ -881,6 +887,50 @@ anvil_status anvil_bank_step_noalloc(const float* grad, float* velocity, int g, 
     return run_step(&b, 1, nullptr, maps, nmaps, margin, eps, scratch,
                     static_cast<size_t>(ANVIL_STATIC_SCRATCH_BYTES),
                     static_cast<cudaStream_t>(stream), nullptr);
+}
+
+int anvil_schedule_runs(const anvil_bank_desc* banks, int nbanks, int nmaps, anvil_schedule_run* runs,
+                        int cap) {
+    if (nmaps < 1 || nmaps > ANVIL_MAX_MAPS || cap < 0 || (cap > 0 && !runs)) return -1;
+    Layout L;
+    if (make_layout(banks, nbanks, &L) != ANVIL_OK) return -1;
+    CascadeParams* cp = new (std::nothrow) CascadeParams;
+    if (!cp) return -1;
+    memset(cp, 0, sizeof(*cp));
+    int order[ANVIL_MAX_BANKS];
+    cascade_bank_order(L.bank, nbanks, order);
+    for (int q = 0; q < nbanks; ++q) {
+        const Geom& G = L.bank[order[q]];
+        CascadeBank& cb = cp->bank[q];
+        cb.g = G.g;
+        cb.s_pad = G.s_pad;
+        cb.L_pad = G.L_pad;
+        cb.m = G.m;
+        cb.n = G.n;
+        cb.tall = G.tall;
+        cb.T = G.s_pad / PAIR;
+        cb.ntl = G.L_pad / PAIR;
+        cb.mat_begin = G.mat_begin;
+    }
+    cp->nbanks = nbanks;
+    anvil_map maps[ANVIL_MAX_MAPS];
+    for (int k = 0; k < nmaps; ++k) maps[k] = anvil_map{1.f, 0.f, 0.f};  // coefficients do not shape the order
+    build_phases(cp, maps, nmaps);
+    order_normalize_interleaved(cp);
+    const int nruns = cp->nruns;
+    for (int r = 0; r < nruns && r < cap; ++r) {
+        const CascadeRun& R = cp->run[r];
+        const CascadeBank& cb = cp->bank[R.bank];
+        runs[r].phase = R.phase;
+        runs[r].op = cp->phase[R.phase].op;
+        runs[r].bank = order[R.bank];
+        runs[r].mat0 = R.mat0;
+        runs[r].nmat = static_cast<int>(R.nmat);
+        runs[r].begin = R.begin;
+        runs[r].tiles = phase_tiles(cb, cp->phase[R.phase].op);
+    }
+    delete cp;
+    return nruns;
 }
 
 }  // extern "C"
