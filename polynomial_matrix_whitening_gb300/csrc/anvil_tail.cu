@@ -233,9 +233,20 @@ __global__ void __launch_bounds__(256) tail_apply_kernel(const __grid_constant__
         const TailBank& B = p.bank[bi];
         const long long lt = t - B.chunk_begin;
         const int cpr = (B.n + 7) / 8;  // chunks per row
-        const long long rowg = lt / cpr;
-        const int c0 = static_cast<int>(lt % cpr) * 8;
-        const int mat = static_cast<int>(rowg / B.m), row = static_cast<int>(rowg % B.m);
+        int mat, row, c0;
+        if (lt < 0x7fffffffLL) {
+            // 32-bit division (the common case: a bank of under 2^31 chunks)
+            const unsigned l = static_cast<unsigned>(lt), ucpr = static_cast<unsigned>(cpr);
+            const unsigned rowg = l / ucpr;
+            c0 = static_cast<int>(l - rowg * ucpr) * 8;
+            mat = static_cast<int>(rowg / static_cast<unsigned>(B.m));
+            row = static_cast<int>(rowg - static_cast<unsigned>(mat) * static_cast<unsigned>(B.m));
+        } else {
+            const long long rowg = lt / cpr;
+            c0 = static_cast<int>(lt % cpr) * 8;
+            mat = static_cast<int>(rowg / B.m);
+            row = static_cast<int>(rowg % B.m);
+        }
         const size_t mn = static_cast<size_t>(B.m) * B.n;
         const size_t base = static_cast<size_t>(mat) * mn + static_cast<size_t>(row) * B.n + c0;
         const float lr = B.eff_lr[mat];
