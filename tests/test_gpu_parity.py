@@ -320,6 +320,27 @@ def test_many_matrices_item_order(A, shapes):
             assert rel(f64(got[k]), f64(out_or[k])) <= OUT_RTOL
 
 
+@pytest.mark.parametrize("shape", [(1, 4096, 16384), (1, 16384, 4096), (2, 2048, 8192)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_large_shapes_singular_values(A, shape):
+    """Sizes past the oracle's reach (up to 16 row blocks per matrix and the largest
+    dimension): for Gaussian gradients with an aspect ratio of 4, every singular value of
+    the normalised X lies in [0.01, 1/1.05], where the composite map is within 5e-4 of 1
+    (the SVD form of the method), so every singular value of out must be 1 up to the bf16
+    roundings of the cascade."""
+    g, m, n = shape
+    grad = W.gaussian([9000, 1234, 0], (g, m, n), 0.02)
+    vel = np.zeros((2, g, m, n), dtype=np.float32)
+    bank = gpu_bank(A, grad, vel, dict(momentum=0.95, fast_beta=0.85, fast_weight=1.0, slow_beta=0.98))
+    A.multi_bank_step([bank], A.alloc_workspace([shape]))
+    torch.cuda.synchronize()
+    assert A.device_error() == A.OK
+    for i in range(g):
+        sv = torch.linalg.svdvals(bank.out[i].float())
+        assert torch.isfinite(sv).all()
+        assert float(sv.min()) > 0.97 and float(sv.max()) < 1.03, (float(sv.min()), float(sv.max()))
+
+
 def test_cuda_graph_with_device_scalars(A):
     """A captured step reads the device scalar block when it runs: replays with new
     scalars equal eager calls with those scalars as host values."""
