@@ -305,9 +305,24 @@ cudaError_t launch_tail_scale(const TailParams& p, cudaStream_t stream) {
     return launch_pdl(lane_scale_kernel, dim3(p.total_mats), dim3(SCALE_THREADS), 0, stream, p);
 }
 
+// Blocks of tail_apply_kernel that are resident at once on this device (cached per
+// device): the grid-stride loop covers the elements in one wave of resident blocks, so no
+// partial second wave trails the first.
+static int g_apply_blocks[64];
+
 cudaError_t launch_tail_apply(const TailParams& p, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e) return e;
+    int& resident = g_apply_blocks[dev & 63];
+    if (resident == 0) {
+        int per_sm = 0, sms = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tail_apply_kernel, 256, 0))) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+        resident = per_sm > 0 && sms > 0 ? per_sm * sms : 152;
+    }
     long long blocks = (p.total_chunks + 255) / 256;
-    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (blocks > resident) blocks = resident;
     if (blocks < 1) blocks = 1;
     return launch_pdl(tail_apply_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
 }
