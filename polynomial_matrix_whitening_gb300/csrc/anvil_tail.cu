@@ -107,13 +107,24 @@ __global__ void __launch_bounds__(256) lane_power_kernel(const __grid_constant__
             const int col = c0 + 8 * cx;
             float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (col < B.n)
-                for (int i = slice; i < B.m; i += 8) {
-                    const uint4 q = __ldcs(reinterpret_cast<const uint4*>(v + static_cast<size_t>(i) * B.n + col));
-                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+                // rows slice, slice + 8, ... in that order, eight rows' loads in flight at once
+                for (int i0 = slice; i0 < B.m; i0 += 64) {
+                    uint4 q[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float x = bf2f(static_cast<uint16_t>((k & 1) ? w[k >> 1] >> 16 : w[k >> 1] & 0xffffu));
-                        s[k] = __fadd_rn(s[k], __fmul_rn(x, x));
+                    for (int u = 0; u < 8; ++u) {
+                        const int i = i0 + 8 * u;
+                        q[u] = i < B.m ? __ldcs(reinterpret_cast<const uint4*>(v + static_cast<size_t>(i) * B.n + col))
+                                       : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (i0 + 8 * u >= B.m) break;
+                        const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float x = bf2f(static_cast<uint16_t>((k & 1) ? w[k >> 1] >> 16 : w[k >> 1] & 0xffffu));
+                            s[k] = __fadd_rn(s[k], __fmul_rn(x, x));
+                        }
                     }
                 }
 #pragma unroll
