@@ -48,7 +48,7 @@ __host__ __device__ inline long long power_blocks(const TailBank& B) {
     const int span = B.vec8 ? POWER_COLS : 32;
     return static_cast<long long>(B.g) * ((B.n + span - 1) / span);
 }
-__global__ void __launch_bounds__(256) lane_power_kernel(const __grid_constant__ TailParams p) {
+__global__ void __launch_bounds__(256, 5) lane_power_kernel(const __grid_constant__ TailParams p) {
     pdl_allow_next();
     pdl_wait_previous();
     const long long blk = blockIdx.x;
