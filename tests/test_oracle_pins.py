@@ -182,7 +182,7 @@ def test_f64_iteration_closed_form_other_maps():
 @pytest.mark.parametrize("shape", [(64, 192), (192, 64), (96, 96)])
 def test_bf16_oracle_near_closed_form_gaussian(shape):
     """Well-conditioned input: the bf16 pipeline lands within bf16 accuracy of U F(S/d) V^T
-    (the benchmark spec tolerance 3e-2; measured about 5e-3)."""
+    (acceptance tolerance 3e-2 against the closed form; measured about 5e-3)."""
     g = W.gaussian([6, shape[0]], shape, 0.02)
     X = oracle.f32_to_bf16(g)
     out = f64(oracle.cascade(X))
