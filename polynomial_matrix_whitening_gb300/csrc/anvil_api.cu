@@ -57,7 +57,6 @@ const anvil_map kAnvilMaps[6] = {
 // ---------------------------------------------------------------- per-device set-up
 struct DeviceState {
     bool ready = false;
-    anvil_status status = ANVIL_OK;
     unsigned* err = nullptr;
     int sm_count = 0;
 };
@@ -120,22 +119,22 @@ struct Profiler {
 };
 Profiler g_prof;
 
-// Runs `launch`, bracketed by two events on `stream` when profiling is on.
+// Runs `launch`, bracketed by two events on `stream` when profiling is on.  A timed
+// launch holds the profiler's lock throughout, so anvil_profile_end on another thread
+// cannot destroy its events in between.
 template <class F>
 cudaError_t profiled(int kind, cudaStream_t stream, F&& launch) {
-    int slot = -1;
-    {
-        std::lock_guard<std::mutex> lock(g_prof.mu);
-        if (g_prof.active && g_prof.used < g_prof.cap) slot = g_prof.used++;
+    std::unique_lock<std::mutex> lock(g_prof.mu);
+    if (!g_prof.active || g_prof.used >= g_prof.cap) {
+        lock.unlock();
+        return launch();
     }
+    const int slot = g_prof.used++;
+    g_prof.kind[slot] = kind;
     cudaError_t e;
-    if (slot >= 0) {
-        g_prof.kind[slot] = kind;
-        if ((e = cudaEventRecord(g_prof.ev[2 * slot], stream))) return e;
-    }
+    if ((e = cudaEventRecord(g_prof.ev[2 * slot], stream))) return e;
     if ((e = launch())) return e;
-    if (slot >= 0 && (e = cudaEventRecord(g_prof.ev[2 * slot + 1], stream))) return e;
-    return cudaSuccess;
+    return cudaEventRecord(g_prof.ev[2 * slot + 1], stream);
 }
 
 // ---------------------------------------------------------------- geometry and layout
@@ -147,7 +146,7 @@ struct Geom {
 struct Layout {
     Geom bank[ANVIL_MAX_BANKS];
     int nbanks, total_mats;
-    size_t d_bytes, part_elems, y_elems, a_elems;
+    size_t part_elems, y_elems, a_elems;
     size_t off_d, off_cnt, off_part, off_y0, off_y1, off_a, off_b, total;
 };
 
@@ -209,7 +208,7 @@ struct Range {
 };
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
-anvil_status check_banks(const anvil_bank_desc* banks, int nbanks, const Layout& L) {
+anvil_status check_banks(const anvil_bank_desc* banks, int nbanks) {
     Range rg[ANVIL_MAX_BANKS][3];
     for (int i = 0; i < nbanks; ++i) {
         const anvil_bank_desc& b = banks[i];
@@ -223,7 +222,6 @@ anvil_status check_banks(const anvil_bank_desc* banks, int nbanks, const Layout&
         rg[i][1] = {reinterpret_cast<uintptr_t>(b.velocity), reinterpret_cast<uintptr_t>(b.velocity + 2 * cnt)};
         rg[i][2] = {reinterpret_cast<uintptr_t>(b.out), reinterpret_cast<uintptr_t>(b.out + cnt)};
     }
-    (void)L;
     // written buffers (velocity, out) must overlap nothing else of the call
     for (int i = 0; i < nbanks; ++i)
         for (int w = 1; w <= 2; ++w)
@@ -279,7 +277,7 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
     anvil_status st;
     Layout L;
     if ((st = make_layout(banks, nbanks, &L)) != ANVIL_OK) return st;
-    if ((st = check_banks(banks, nbanks, L)) != ANVIL_OK) return st;
+    if ((st = check_banks(banks, nbanks)) != ANVIL_OK) return st;
     if ((st = check_maps(maps, nmaps)) != ANVIL_OK) return st;
     if (!workspace || ws_bytes < L.total) return ANVIL_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255) return ANVIL_ERR_ALIGNMENT;

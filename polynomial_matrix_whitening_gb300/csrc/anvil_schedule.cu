@@ -168,79 +168,4 @@ void order_normalize_interleaved(CascadeParams* cp) {
     cp->run[nr].begin = items;
 }
 
-// Matrix by matrix in a staggered start: every bank releases its matrices at an even
-// rate over the step, and each (matrix, phase) is placed by its estimated ready time
-// (the matrix's release plus the latencies of the phases before it).  A matrix then runs
-// its phases close together, so the tiles one phase writes are mostly still in L2 when
-// the next phase reads them, while the matrices in flight together keep every CTA pair
-// busy.  Costs are in units of one 64-deep k-block of a 256x256 tile.
-void order_staggered(CascadeParams* cp, int npairs) {
-    const double kEpi = 6.0;    // epilogue of a tile that no product overlaps
-    const double kSync = 8.0;   // completion -> publish -> dependants see it
-    auto cost = [&](const CascadeBank& b, int op) -> double {
-        if (op == OP_NORMALIZE) return kEpi;
-        const int K = (op == OP_GRAM || op == OP_GRAM_NORM) ? b.L_pad : b.s_pad;
-        return K / 64.0;
-    };
-    double work = 0.0;
-    int total_mats = 0;
-    for (int q = 0; q < cp->nbanks; ++q) {
-        const CascadeBank& b = cp->bank[q];
-        total_mats += b.g;
-        for (int p = 0; p < cp->nphases; ++p)
-            work += static_cast<double>(b.g) * phase_tiles(b, cp->phase[p].op) * cost(b, cp->phase[p].op);
-    }
-    const double t_est = work / (npairs > 0 ? npairs : 1);
-    // matrices per run, so that the list fits
-    int chunk = 1;
-    while (((total_mats + chunk - 1) / chunk + cp->nbanks) * cp->nphases > MAX_RUNS) ++chunk;
-    struct Seg {
-        double ready;
-        int bank, mat0, nmat, phase;
-    };
-    std::vector<Seg> segs;
-    for (int q = 0; q < cp->nbanks; ++q) {
-        const CascadeBank& b = cp->bank[q];
-        double chain = 0.0;
-        for (int p = 0; p < cp->nphases; ++p) chain += cost(b, cp->phase[p].op) + kSync;
-        const double span = t_est > chain ? t_est - chain : 0.0;
-        for (int m0 = 0; m0 < b.g; m0 += chunk) {
-            const int nm = std::min(chunk, b.g - m0);
-            double t = span * m0 / b.g;
-            for (int p = 0; p < cp->nphases; ++p) {
-                segs.push_back({t, q, m0, nm, p});
-                t += cost(b, cp->phase[p].op) + kSync;
-            }
-        }
-    }
-    std::stable_sort(segs.begin(), segs.end(), [](const Seg& x, const Seg& y) {
-        if (x.ready != y.ready) return x.ready < y.ready;
-        if (x.phase != y.phase) return x.phase < y.phase;
-        return x.bank < y.bank;
-    });
-    int items = 0, nr = 0;
-    for (const Seg& sg : segs) {
-        const CascadeBank& b = cp->bank[sg.bank];
-        const int n = sg.nmat * phase_tiles(b, cp->phase[sg.phase].op);
-        if (nr > 0) {
-            CascadeRun& last = cp->run[nr - 1];
-            if (last.phase == sg.phase && last.bank == sg.bank &&
-                static_cast<int>(last.mat0 + last.nmat) == sg.mat0) {
-                last.nmat += static_cast<uint32_t>(sg.nmat);
-                items += n;
-                continue;
-            }
-        }
-        CascadeRun& r = cp->run[nr++];
-        r.begin = items;
-        r.phase = static_cast<uint8_t>(sg.phase);
-        r.bank = static_cast<uint8_t>(sg.bank);
-        r.mat0 = static_cast<uint16_t>(sg.mat0);
-        r.nmat = static_cast<uint32_t>(sg.nmat);
-        items += n;
-    }
-    cp->nruns = nr;
-    cp->run[nr].begin = items;
-}
-
 }  // namespace anvil

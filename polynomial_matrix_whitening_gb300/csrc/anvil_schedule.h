@@ -18,8 +18,5 @@ void order_phase_major(CascadeParams* cp, int* phase_run);
 // Phase-major, with the normalisation's tiles spread over the product phases before the
 // first X-update (which do not read the normalised X).
 void order_normalize_interleaved(CascadeParams* cp);
-// Matrices released at an even rate, (matrix, phase) by estimated ready time, for L2
-// reuse between the phases of a matrix; npairs = CTA pairs of the persistent grid.
-void order_staggered(CascadeParams* cp, int npairs);
 
 }  // namespace anvil
