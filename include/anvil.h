@@ -41,7 +41,8 @@ extern "C" {
 typedef enum {
     ANVIL_OK = 0,
     ANVIL_ERR_INVALID_ARG = 1,       /* null pointer, g/m/n < 1, nmaps out of range, ... */
-    ANVIL_ERR_UNSUPPORTED_SHAPE = 2, /* a dimension above ANVIL_MAX_DIM / ANVIL_MAX_BATCH */
+    ANVIL_ERR_UNSUPPORTED_SHAPE = 2, /* a dimension above ANVIL_MAX_DIM / ANVIL_MAX_BATCH, or a
+                                        call of over 2^40 padded elements (terabytes of workspace) */
     ANVIL_ERR_ALIGNMENT = 3,         /* pointer not aligned to its element size / workspace to 256 B */
     ANVIL_ERR_ALIAS = 4,             /* a written buffer overlaps another buffer of the call */
     ANVIL_ERR_WORKSPACE = 5,         /* workspace too small, or cannot be allocated during capture */

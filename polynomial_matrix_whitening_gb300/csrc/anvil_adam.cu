@@ -1,7 +1,7 @@
 // anvil_adam.cu -- the Adam step with cautious weight decay that the page uses for the
 // parameters outside the ANVIL banks (page "modded-nanogpt track_1_short/optim/anvil.py",
 // `_adam_update_step`), as one HBM-bound elementwise kernel: 16 bytes read and 12 bytes
-// written per element, eight elements per thread per iteration (two 16-byte vectors of
+// written per element, four elements per thread per iteration (one 16-byte vector of
 // each array).  Every rounding follows the page's fp32 tensor operations one at a time.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(256) adam_kernel(const AdamParams a) {
 }
 
 cudaError_t launch_adam(const AdamParams& a, cudaStream_t stream) {
+    // grid-stride, at most 16 blocks for each of a GB300's 152 SMs: 2.67 waves of the
+    // resident blocks, measured faster than one, two or three whole waves
     long long blocks = (a.count / 4 + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     if (blocks < 1) blocks = 1;

@@ -192,6 +192,9 @@ anvil_status make_layout(const anvil_bank_desc* banks, int nbanks, Layout* L) {
         L->y_elems += static_cast<size_t>(b.g) * G.s_pad * G.L_pad;
         L->a_elems += static_cast<size_t>(b.g) * G.s_pad * G.s_pad;
     }
+    // 32-bit tile and item counts (the momentum grid, the cascade's item numbers: at most
+    // MAX_PHASES items per 256 x 256 block of Y) hold below 2^40 elements of Y, 2 TB
+    if (L->y_elems > (static_cast<size_t>(1) << 40)) return ANVIL_ERR_UNSUPPORTED_SHAPE;
     L->off_d = 0;
     L->off_cnt = align256(L->off_d + sizeof(float) * L->total_mats);
     L->off_part = align256(L->off_cnt + sizeof(unsigned) * (2 * L->total_mats + SCHED_COUNTERS));

@@ -66,6 +66,7 @@ def test_workspace_bytes():
     (dict(m=0), anvil.ERR_INVALID_ARG),
     (dict(n=-1), anvil.ERR_INVALID_ARG),
     (dict(m=20000), anvil.ERR_UNSUPPORTED_SHAPE),
+    (dict(g=65535, m=16384, n=16384), anvil.ERR_UNSUPPORTED_SHAPE),  # 2^44 elements
     (dict(grad=G + 2), anvil.ERR_ALIGNMENT),
     (dict(grad=G + 1, grad_bf16=1), anvil.ERR_ALIGNMENT),
     (dict(out=3 * G + 1), anvil.ERR_ALIGNMENT),
