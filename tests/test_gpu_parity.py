@@ -341,6 +341,49 @@ def test_large_shapes_singular_values(A, shape):
         assert float(sv.min()) > 0.97 and float(sv.max()) < 1.03, (float(sv.min()), float(sv.max()))
 
 
+def test_largest_square_block_diagonal(A):
+    """The largest small side, 16384 x 16384 (64 x 64 output tiles, 256 k-blocks per Gram
+    tile), checked element by element against the oracle.  The gradient holds 64 copies of
+    one 256 x 256 Gaussian block G1 on its diagonal and zeros elsewhere.  Every step of the
+    method keeps that structure exactly: momentum of a zero is zero, and the off-diagonal
+    blocks of X X^T, b A + c A A and a X + B X are sums of exact zeros.  The blocks share
+    one d: the trace is 64 times the block's, and in fp32 sqrt(64 tr) = 8 sqrt(tr) exactly,
+    so d is the oracle's d for the single block G1 with the margin multiplied by 8 (exact
+    too), up to the order in which the trace is summed.  So each diagonal block of out must
+    match the oracle's step on G1 with margin 8 x 1.05 within the bf16 bar, and every other
+    block must be zero."""
+    nb, k = 256, 64
+    size = nb * k
+    g1 = W.gaussian([9100, 0], (1, nb, nb), 0.02)
+    scal = dict(momentum=0.95, fast_beta=0.85, fast_weight=1.0, slow_beta=0.98)
+    want, _ = oracle.bank_step(g1, np.zeros((2, 1, nb, nb), np.float32), **scal,
+                               margin=float(np.float32(8.0) * np.float32(oracle.FROBENIUS_MARGIN)))
+    dev = torch.device("cuda")
+    grad = torch.zeros((1, size, size), dtype=torch.float32, device=dev)
+    blk = torch.from_numpy(g1[0]).to(dev)
+    for b in range(k):
+        grad[0, b * nb:(b + 1) * nb, b * nb:(b + 1) * nb] = blk
+    vel = torch.zeros((2, 1, size, size), dtype=torch.float32, device=dev)
+    out = torch.empty((1, size, size), dtype=torch.bfloat16, device=dev)
+    bank = A.Bank(grad, vel, out, **scal)
+    A.multi_bank_step([bank], A.alloc_workspace([(1, size, size)]))
+    torch.cuda.synchronize()
+    assert A.device_error() == A.OK
+    del grad, vel
+    tiles = out[0].view(k, nb, k, nb)
+    amax = tiles.abs().amax(dim=(1, 3)).float()
+    diag = torch.arange(k, device=dev)
+    assert torch.isfinite(amax).all()
+    off = amax.clone()
+    off[diag, diag] = 0.0
+    assert float(off.max()) == 0.0, "a block off the diagonal is not zero"
+    errs = []
+    for b in range(k):
+        got = bits(tiles[b, :, b, :])
+        errs.append(rel(f64(got), f64(want[0])))
+    assert max(errs) <= OUT_RTOL, max(errs)
+
+
 def test_cuda_graph_with_device_scalars(A):
     """A captured step reads the device scalar block when it runs: replays with new
     scalars equal eager calls with those scalars as host values."""

@@ -291,6 +291,29 @@ def test_zero_padding_invariance_bitwise(shape, pad):
     assert not b[rows:, :].any() and not b[:, cols:].any()
 
 
+@pytest.mark.parametrize("nb,k", [(24, 4), (40, 16)])
+def test_block_diagonal_copies_share_one_d(nb, k):
+    """k copies of one block on the diagonal: the Gram, b A + c A A and a X + B X keep the
+    off-diagonal blocks exactly zero, so each diagonal block goes through the method on
+    its own, normalised by the whole matrix's d.  The whole trace is k times the block's,
+    so (k a power of 4, sqrt exact in fp32) that d is the block's own with the margin
+    multiplied by sqrt(k), up to the order in which the trace is summed."""
+    X1 = oracle.f32_to_bf16(W.gaussian([13, nb, k], (nb, nb), 0.02))
+    size = nb * k
+    Xw = np.zeros((size, size), np.uint16)
+    for b in range(k):
+        Xw[b * nb:(b + 1) * nb, b * nb:(b + 1) * nb] = X1
+    whole = oracle.cascade(Xw).reshape(k, nb, k, nb)
+    margin = float(np.float32(np.sqrt(k)) * np.float32(oracle.FROBENIUS_MARGIN))
+    want = f64(oracle.cascade(X1, margin=margin))
+    for b in range(k):
+        for c in range(k):
+            if b != c:
+                assert not f64(whole[b, :, c, :]).any()
+        got = f64(whole[b, :, b, :])
+        assert np.linalg.norm(got - want) <= 1e-3 * np.linalg.norm(want)
+
+
 @pytest.mark.parametrize("k", [-3, 2, 5])
 def test_power_of_two_scaling_bitwise(k):
     """With eps = 0, grad * 2^k leaves the output unchanged bit for bit."""
