@@ -111,7 +111,10 @@ anvil_status anvil_multi_bank_step(const anvil_bank_desc* banks, int nbanks,
  * the cached size frees and allocates it (cudaFree / cudaMalloc, which
  * synchronise the device), so make one call of the largest size before
  * capturing this function in a CUDA graph; a call that would have to grow it
- * while the stream is capturing returns ANVIL_ERR_WORKSPACE.
+ * while the stream is capturing returns ANVIL_ERR_WORKSPACE.  Every call on a
+ * device uses that one workspace: two calls whose work can overlap on the GPU
+ * (different streams, or threads) corrupt each other's results, so serialise
+ * them, or give each stream its own workspace through anvil_multi_bank_step.
  * maps = NULL selects the page's six ANVIL_MAPS. */
 anvil_status anvil_bank_step(const float* grad, float* velocity, int g, int m, int n,
                              float momentum, float fast_beta, float fast_weight, float slow_beta,
