@@ -14,7 +14,7 @@ oracle on a bounded sample of the same workload.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl anvil|reference]
   python bench.py --ncu-case     # two eager steps of the same workload, for ncu captures
 
-``--impl reference`` times the CPU oracle (the reference arm of this build) on the same
+``--impl reference`` times the CPU oracle (the reference arm: no installable reference exists) on the same
 workload and metric.  With N > 1 (launched by torch.distributed.run) every rank runs an
 independent replica of the step on its own GPU: the path shards by whole matrices and
 has no exchange step, so there is no collective on the data path.
