@@ -808,7 +808,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 case OP_SQPOLY: epi_tile<OP_SQPOLY>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
                 case OP_XUPDATE: epi_tile<OP_XUPDATE>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
                 case OP_XUPDATE_OUT: epi_tile<OP_XUPDATE_OUT>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
-                default: normalize_tile(bk, c, rank, x.grp, quad * 32 + lane); break;
+                default:
+                    normalize_tile(bk, c, rank, x.grp, quad * 32 + lane);
+                    // the group's plain stores precede its leader's publication of the tile,
+                    // which may come before the next iteration's group barrier
+                    named_barrier_sync(1 + x.grp, 128);
+                    break;
             }
             // publish the group's previous tile: its stores are older than this tile's two
             // (one per quarter), so they have long completed
