@@ -320,6 +320,47 @@ def test_many_matrices_item_order(A, shapes):
             assert rel(f64(got[k]), f64(out_or[k])) <= OUT_RTOL
 
 
+@pytest.mark.parametrize("case,reps", [
+    ("full_step", 20),
+    ("400_matrices", 30),
+    ("tiny", 100),
+], ids=["full_step", "400_matrices", "tiny"])
+def test_repeated_steps_are_bitwise_identical(A, case, reps):
+    """The same step, repeated on the same inputs, gives the same bits every time: every
+    value the cascade reads between its phases is complete when it is read (completion
+    counters, publication after the stores), and every sum has a fixed order.  The bench's
+    three banks, 400 small matrices (the densest dependency waits) and tiny matrices whose
+    phases follow one another at once."""
+    if case == "full_step":
+        wl = W.workloads()["full_step"]
+        sc = wl.scalars(0)
+        shapes = [(b.g, b.m, b.n) for b in wl.banks]
+        grads = [wl.grad(j, 0) for j in range(len(shapes))]
+        vels = [wl.velocity(j) for j in range(len(shapes))]
+        scal = scal_dict(sc)
+    else:
+        shapes = ([(200, 24, 16), (120, 8, 40), (80, 20, 20)] if case == "400_matrices"
+                  else [(1, 3, 4), (2, 4, 3), (1, 1, 1), (1, 8, 2)])
+        grads, vels = zip(*[W.random_case(950 + j, g, m, n) for j, (g, m, n) in enumerate(shapes)])
+        scal = dict(momentum=0.95, fast_beta=0.85, fast_weight=0.4385, slow_beta=0.98)
+    banks = [gpu_bank(A, gr, ve, scal) for gr, ve in zip(grads, vels)]
+    vel0 = [b.velocity.clone() for b in banks]
+    ws = A.alloc_workspace(shapes)
+    first = None
+    for r in range(reps):
+        for b, v in zip(banks, vel0):
+            b.velocity.copy_(v)
+        A.multi_bank_step(banks, ws)
+        outs = [b.out.view(torch.int16).clone() for b in banks]
+        if first is None:
+            first = outs
+        else:
+            for k, (o, f) in enumerate(zip(outs, first)):
+                assert torch.equal(o, f), (r, k)
+    torch.cuda.synchronize()
+    assert A.device_error() == A.OK
+
+
 @pytest.mark.parametrize("shape", [(1, 4096, 16384), (1, 16384, 4096), (2, 2048, 8192)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_large_shapes_singular_values(A, shape):
