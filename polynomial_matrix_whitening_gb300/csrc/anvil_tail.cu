@@ -26,14 +26,16 @@ namespace anvil {
 // One grid over every bank (a block finds its bank from power_begin).
 // Lanes along rows (m >= n): each warp sums POWER_ROWS consecutive rows of the bank (rows
 // of consecutive matrices are contiguous); with the vector layout (n % 8 == 0, 16-byte
-// aligned) lane k takes 8-element chunks k, k + 32, ... of every row, the rows' loads in
-// flight together, otherwise single elements; a fixed shuffle tree adds each row's 32
-// partial sums.
+// aligned) lane k takes 8-element chunks k, k + 32, ... of every row, POWER_CHUNKS chunks
+// of each of the warp's rows loaded before any is summed (one memory round trip for rows
+// of up to 768 elements), otherwise single elements; a fixed shuffle tree adds each row's
+// 32 partial sums.
 // Lanes along columns (m < n): a block covers 256 columns of one matrix (8 per thread with
 // the vector layout, else 32 columns) with 8 row slices; slice k sums rows k, k + 8, ...;
 // the slice sums of a column are added in slice order.
 constexpr int POWER_COLS = 256;  // columns per block, lanes along columns, vector layout
 constexpr int POWER_ROWS = 4;    // rows per warp, lanes along rows
+constexpr int POWER_CHUNKS = 3;  // 16-byte chunks of each row a lane loads before summing
 __device__ __forceinline__ float sumsq8(uint4 q, float s) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -48,7 +50,7 @@ __host__ __device__ inline long long power_blocks(const TailBank& B) {
     const int span = B.vec8 ? POWER_COLS : 32;
     return static_cast<long long>(B.g) * ((B.n + span - 1) / span);
 }
-__global__ void __launch_bounds__(256, 5) lane_power_kernel(const __grid_constant__ TailParams p) {
+__global__ void __launch_bounds__(256, 4) lane_power_kernel(const __grid_constant__ TailParams p) {
     pdl_allow_next();
     pdl_wait_previous();
     const long long blk = blockIdx.x;
@@ -68,15 +70,19 @@ __global__ void __launch_bounds__(256, 5) lane_power_kernel(const __grid_constan
         for (int k = 0; k < POWER_ROWS; ++k) s[k] = 0.f;
         if (B.vec8) {
             const int nc = B.n / 8;
-            for (int j = lane; j < nc; j += 32) {
-                uint4 q[POWER_ROWS];
+            for (int j0 = lane; j0 < nc; j0 += 32 * POWER_CHUNKS) {
+                uint4 q[POWER_CHUNKS][POWER_ROWS];
 #pragma unroll
-                for (int k = 0; k < POWER_ROWS; ++k)
-                    q[k] = row0 + k < nrows
-                               ? __ldcs(reinterpret_cast<const uint4*>(B.update + static_cast<size_t>(row0 + k) * B.n) + j)
-                               : make_uint4(0u, 0u, 0u, 0u);
+                for (int u = 0; u < POWER_CHUNKS; ++u)
 #pragma unroll
-                for (int k = 0; k < POWER_ROWS; ++k) s[k] = sumsq8(q[k], s[k]);
+                    for (int k = 0; k < POWER_ROWS; ++k)
+                        q[u][k] = (j0 + 32 * u < nc && row0 + k < nrows)
+                                      ? __ldcs(reinterpret_cast<const uint4*>(B.update + static_cast<size_t>(row0 + k) * B.n) + j0 + 32 * u)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int u = 0; u < POWER_CHUNKS; ++u)
+#pragma unroll
+                    for (int k = 0; k < POWER_ROWS; ++k) s[k] = sumsq8(q[u][k], s[k]);
             }
         } else {
 #pragma unroll
