@@ -110,6 +110,13 @@ def step_flops(banks, nmaps=6):
 
 # ------------------------------------------------------------------ clocks
 
+def physical_gpu(local):
+    """The nvidia-smi id (index, UUID or bus id, as CUDA_VISIBLE_DEVICES lists it) of this
+    rank's GPU."""
+    ids = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    return ids[local] if local < len(ids) else str(local)
+
+
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons every 200 ms while running."""
     FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
@@ -312,8 +319,7 @@ def run_anvil(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
-                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler = ClockSampler(physical_gpu(local))
     with sampler, torch.cuda.stream(stream):
         time.sleep(0.25)
         e0.record(stream)

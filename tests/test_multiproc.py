@@ -53,3 +53,18 @@ def test_reference_arm_prints_on_rank_zero_only(tmp_path):
     lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
     assert len(lines) == 1 and lines[0]["impl"] == "reference"
     assert lines[0]["value"] > 0 and lines[0]["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.parametrize("visible,local,want", [
+    (None, 0, "0"), (None, 3, "3"), ("4,5", 1, "5"), ("GPU-aa, GPU-bb", 1, "GPU-bb"), ("", 2, "2"),
+])
+def test_clock_sampler_gets_each_ranks_physical_gpu(monkeypatch, visible, local, want):
+    """The clocks recorded beside a rank's number are its own GPU's: the id CUDA_VISIBLE_DEVICES
+    lists for its local rank (index or UUID, as nvidia-smi -i takes them)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    if visible is None:
+        monkeypatch.delenv("CUDA_VISIBLE_DEVICES", raising=False)
+    else:
+        monkeypatch.setenv("CUDA_VISIBLE_DEVICES", visible)
+    assert bench.physical_gpu(local) == want
