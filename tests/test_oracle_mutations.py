@@ -35,6 +35,16 @@ MUTATIONS = {
     "adam_mask_reversed": ("const float mask = (u * p[e] > 0.0f) ? 1.0f : 0.0f;",
                            "const float mask = (u * p[e] < 0.0f) ? 1.0f : 0.0f;"),
     "adam_second_moment_unsquared": ("(c2 * g[e]) * g[e]", "(c2 * g[e])"),
+    "scale_not_rounded_to_bf16": ("for (int l = 0; l < nl; ++l) scale[l] = round_bf16(scale[l] * ratio);",
+                                  "for (int l = 0; l < nl; ++l) scale[l] = scale[l] * ratio;"),
+    "power_mean_over_lane_count": ("power[l] = s / (float)lane_len;", "power[l] = s / (float)nl;"),
+    "gain_from_old_energy": ("            le[l] = lerp32(le[l], power[l], w);\n"
+                             "            const float gain = rsqrt_rn(le[l] > 1e-10f ? le[l] : 1e-10f);",
+                             "            const float gain = rsqrt_rn(le[l] > 1e-10f ? le[l] : 1e-10f);\n"
+                             "            le[l] = lerp32(le[l], power[l], w);"),
+    "adam_eps_inside_sqrt": ("float u = (m / (sqrtf(v) + eps)) * step_size;", "float u = (m / sqrtf(v + eps)) * step_size;"),
+    "no_nesterov_lookahead": ("g = lerp32(g, blend, momentum);", "g = blend;"),
+    "X_over_d_squared": ("X[e] = f32_to_bf16(bf16_to_f32(X[e]) / d);", "X[e] = f32_to_bf16(bf16_to_f32(X[e]) / d2);"),
 }
 
 

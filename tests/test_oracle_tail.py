@@ -45,6 +45,41 @@ def test_equalizer_from_zero_state_equalises_lanes_and_keeps_the_norm(shape):
     np.testing.assert_allclose(le, 0.05 * P, rtol=1e-5)
 
 
+@pytest.mark.parametrize("shape,b2", [((2, 48, 16), 0.95), ((2, 16, 48), 0.9), ((1, 40, 40), 0.99)])
+def test_equalizer_output_bits_from_the_closed_form_scale(shape, b2):
+    """Bit for bit where the result is decided: from zero lane energy the lane scale is
+    s_l = gain_l * ||v|| / post_norm with gain_l = 1/sqrt((1-b2) P_l), evaluated here in fp64;
+    the page casts it to bf16 (torch's conversion here) and the output element is
+    bf16(v * bf16(s_l)), a product of two bf16 values, exact before its one rounding.  Lanes
+    whose s_l lies within 2^-14 (relative) of a bf16 rounding boundary, where fp32 evaluation
+    order may decide, are skipped."""
+    import torch
+    g, m, n = shape
+    v = graded(shape, 7 * m + n)
+    rows_lanes = m >= n
+    le0 = np.zeros((g, m if rows_lanes else n), np.float32)
+    veq, _ = oracle.rail_equalizer(v, le0, b2)
+    x = f64(v)
+    P = lanes(x, rows_lanes)                                 # [g, nl]
+    L = n if rows_lanes else m                               # lane length
+    le = (1.0 - np.float64(np.float32(b2))) * P
+    gain = 1.0 / np.sqrt(le)
+    post = np.sqrt((P * L * gain ** 2).sum(axis=1, keepdims=True))
+    pre = np.sqrt((P * L).sum(axis=1, keepdims=True))
+    s = gain * (pre / post)
+    s_bf = torch.from_numpy(s.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    # distance of s to the nearest bf16 rounding boundary (midpoint), relative
+    e = np.floor(np.log2(s))
+    ulp = 2.0 ** (e - 7)
+    frac = (s / ulp) % 1.0
+    robust = np.abs(frac - 0.5) * ulp > 2.0 ** -14 * s
+    assert robust.mean() > 0.9
+    prod = x * (s_bf[:, :, None] if rows_lanes else s_bf[:, None, :])
+    want = torch.from_numpy(prod.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    mask = np.broadcast_to(robust[:, :, None] if rows_lanes else robust[:, None, :], veq.shape)
+    np.testing.assert_array_equal(veq[mask], want[mask])
+
+
 def test_lane_energy_is_an_ema_over_steps():
     """The same update k times from zero: lane_energy_k = (1 - b2^k) P."""
     shape = (2, 24, 40)
