@@ -45,6 +45,9 @@ MUTATIONS = {
     "adam_eps_inside_sqrt": ("float u = (m / (sqrtf(v) + eps)) * step_size;", "float u = (m / sqrtf(v + eps)) * step_size;"),
     "no_nesterov_lookahead": ("g = lerp32(g, blend, momentum);", "g = blend;"),
     "X_over_d_squared": ("X[e] = f32_to_bf16(bf16_to_f32(X[e]) / d);", "X[e] = f32_to_bf16(bf16_to_f32(X[e]) / d2);"),
+    "maps_reversed": ("const float a = maps[3 * k], b = maps[3 * k + 1], c = maps[3 * k + 2];",
+                      "const int kr = nmaps - 1 - k;\n        const float a = maps[3 * kr], b = maps[3 * kr + 1], c = maps[3 * kr + 2];"),
+    "trace_from_unrounded_gram": ("tr += bf16_to_f32(A[(size_t)i * s + i]);", "tr += Af[(size_t)i * s + i];"),
 }
 
 
