@@ -216,6 +216,28 @@ def test_other_coefficient_sets(A, name, shape):
         assert rel(f64(got[i]), f64(out[i])) <= OUT_RTOL, (name, i)
 
 
+@pytest.mark.parametrize("margin,eps", [(1.2, 1e-3), (2.0, 0.5)])
+@pytest.mark.parametrize("shape", [(3, 256, 768), (2, 520, 264)], ids=lambda s: "x".join(map(str, s)))
+def test_margin_and_eps_are_parameters(A, shape, margin, eps):
+    """d = sqrt(tr) * margin + eps with the caller's margin and eps (the page's
+    FROBENIUS_MARGIN and FROBENIUS_EPS made parameters): d from the traced step against the
+    oracle's (eps = 0.5 is about 8% of d here, a margin of 2 almost doubles it), and the
+    output within the bf16 bar."""
+    g, m, n = shape
+    grad, vel = W.random_case(131 + m, g, m, n)
+    sc = dict(momentum=0.95, fast_beta=0.85, fast_weight=0.4385, slow_beta=0.98)
+    bank = gpu_bank(A, grad, vel, sc)
+    t = A.bank_step_traced(bank, A.alloc_workspace([shape]), margin=margin, eps=eps)
+    torch.cuda.synchronize()
+    assert A.device_error() == A.OK
+    X_or, _, _ = oracle.momentum(grad, vel, **sc)
+    got = bits(bank.out)
+    for i in range(g):
+        o, tr = oracle.cascade(X_or[i], margin=margin, eps=eps, trace=True)
+        assert abs(float(t["d"][i]) - tr["d"][0]) <= 1e-4 * tr["d"][0], (i, float(t["d"][i]), tr["d"][0])
+        assert rel(f64(got[i]), f64(o)) <= OUT_RTOL, i
+
+
 @pytest.mark.parametrize("shape", [(22, 256, 768), (3, 300, 130), (2, 130, 257)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_bf16_grad_input(A, shape):
