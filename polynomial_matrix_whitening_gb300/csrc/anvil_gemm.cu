@@ -100,7 +100,7 @@ struct Item {
 // scheduler has none, and the readers free slots with relaxed arrivals (ordered after
 // their reads of the slot by a data dependency).
 constexpr int SDEPTH = 6;                         // ring slots
-constexpr int SAHEAD = 2;                         // entries the scheduler may run ahead of the producer
+constexpr int SAHEAD = 3;                         // entries the scheduler may run ahead of the producer
 constexpr int SCONSUMERS = 3 + 2 * EPI_GROUPS;    // both producers, the MMA, every epilogue group
 
 // A resolved item: two 16-byte words.
