@@ -352,6 +352,30 @@ def test_grouped_banks_equal_separate_calls(A):
         assert torch.equal(o.view(torch.int16), banks[2].out[i:i + 1].view(torch.int16))
 
 
+def test_eight_banks_in_one_call(A):
+    """The largest call by bank count (ANVIL_MAX_BANKS = 8), tall, wide, square and ragged
+    banks mixed: equal to one call per bank bit for bit, and each bank against the oracle."""
+    shapes = [(3, 256, 768), (2, 768, 256), (2, 300, 130), (1, 130, 300), (2, 520, 520),
+              (4, 64, 64), (1, 1000, 264), (2, 24, 16)]
+    assert len(shapes) == A.MAX_BANKS
+    sc = dict(momentum=0.95, fast_beta=0.85, fast_weight=0.4385, slow_beta=0.98)
+    cases = [W.random_case(170 + j, *s) for j, s in enumerate(shapes)]
+    banks = [gpu_bank(A, gr, ve, sc) for gr, ve in cases]
+    solo = [gpu_bank(A, gr, ve, sc) for gr, ve in cases]
+    A.multi_bank_step(banks, A.alloc_workspace(shapes))
+    for b, s in zip(solo, shapes):
+        A.multi_bank_step([b], A.alloc_workspace([s]))
+    torch.cuda.synchronize()
+    assert A.device_error() == A.OK
+    for (gr, ve), b, s in zip(cases, banks, solo):
+        assert torch.equal(b.out.view(torch.int16), s.out.view(torch.int16))
+        assert torch.equal(b.velocity, s.velocity)
+        out, _ = oracle.bank_step(gr, ve, **sc)
+        got = bits(b.out)
+        for i in range(gr.shape[0]):
+            assert rel(f64(got[i]), f64(out[i])) <= OUT_RTOL
+
+
 @pytest.mark.parametrize("shapes", [
     # 400 matrices: the normalisation interleaved with the first products, one run per
     # matrix and phase before the first X-update (about 1260 runs)
