@@ -155,14 +155,29 @@ def _stream_arg(stream):
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+def _require(cond, what):
+    """Argument check that survives python -O: the kernels trust every pointer and extent
+    they are given, so a wrong tensor must stop here."""
+    if not cond:
+        raise ValueError(what)
+
+
+def _on_one_gpu(tensors, what):
+    _require(all(t.is_cuda for t in tensors), f"{what}: every tensor must be on a CUDA device")
+    _require(len({t.device for t in tensors}) == 1, f"{what}: every tensor must be on the same device")
+    _require(all(t.is_contiguous() for t in tensors), f"{what}: every tensor must be contiguous")
+
+
 def _desc(grad, velocity, out, scalars=None):
     import torch
-    assert grad.dtype in (torch.float32, torch.bfloat16), "grad fp32 or bf16"
-    assert velocity.dtype == torch.float32, "velocity fp32"
-    assert out.dtype == torch.bfloat16, "out is bf16"
-    assert grad.is_contiguous() and velocity.is_contiguous() and out.is_contiguous()
+    _require(grad.dtype in (torch.float32, torch.bfloat16), "grad must be fp32 or bf16")
+    _require(velocity.dtype == torch.float32, "velocity must be fp32")
+    _require(out.dtype == torch.bfloat16, "out must be bf16")
+    _require(grad.dim() == 3, "grad must be [g, m, n]")
     g, m, n = grad.shape
-    assert velocity.shape == (2, g, m, n) and out.shape == (g, m, n)
+    _require(tuple(velocity.shape) == (2, g, m, n), "velocity must be [2, g, m, n]")
+    _require(tuple(out.shape) == (g, m, n), "out must be [g, m, n]")
+    _on_one_gpu((grad, velocity, out), "bank")
     s = scalars or {}
     return BankDesc(grad.data_ptr(), velocity.data_ptr(), out.data_ptr(), g, m, n,
                     Scalars(float(s.get("momentum", 0.95)), float(s.get("fast_beta", 0.85)),
@@ -187,8 +202,14 @@ def alloc_workspace(shapes, device=None):
     if nbytes == 0:
         raise AnvilError(ERR_INVALID_ARG, "workspace_bytes")
     ws = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
-    assert ws.data_ptr() % 256 == 0
+    _require(ws.data_ptr() % 256 == 0, "workspace not 256-byte aligned")
     return ws
+
+
+def _workspace_arg(workspace, ref):
+    """(pointer, bytes) of a workspace tensor on the same GPU as `ref`."""
+    _on_one_gpu((workspace, ref), "workspace")
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
 
 
 class Bank:
@@ -219,11 +240,13 @@ def multi_bank_step(banks, workspace, maps=None, margin=1.05, eps=1e-6, d_scalar
     marr, nm = _maps_arg(maps)
     dsp = None
     if d_scalars is not None:
-        assert d_scalars.is_cuda and d_scalars.dtype.is_floating_point and d_scalars.is_contiguous()
-        assert tuple(d_scalars.shape) == (len(banks), 4)
+        import torch
+        _require(d_scalars.dtype == torch.float32, "d_scalars must be fp32")
+        _require(tuple(d_scalars.shape) == (len(banks), 4), "d_scalars must be [nbanks, 4]")
+        _on_one_gpu((d_scalars, banks[0].grad), "d_scalars")
         dsp = d_scalars.data_ptr()
-    st = _lib.anvil_multi_bank_step(descs, len(banks), dsp, marr, nm, margin, eps,
-                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+    wsp, wsb = _workspace_arg(workspace, banks[0].grad)
+    st = _lib.anvil_multi_bank_step(descs, len(banks), dsp, marr, nm, margin, eps, wsp, wsb,
                                     _stream_arg(stream))
     _check(st, "anvil_multi_bank_step")
 
@@ -232,7 +255,7 @@ def bank_step(grad, velocity, out, momentum=0.95, fast_beta=0.85, fast_weight=0.
               slow_beta=0.98, maps=None, margin=1.05, eps=1e-6, stream=None):
     """One bank, host scalars, library-owned workspace (the page's anvil_cascade call)."""
     import torch
-    assert grad.dtype == torch.float32, "anvil_bank_step takes fp32 grads; use multi_bank_step for bf16"
+    _require(grad.dtype == torch.float32, "anvil_bank_step takes fp32 grads; use multi_bank_step for bf16")
     _desc(grad, velocity, out)
     g, m, n = grad.shape
     marr, nm = (None, 0) if maps is None else _maps_arg(maps)
@@ -250,7 +273,7 @@ def bank_step_noalloc(grad, velocity, out, momentum=0.95, fast_beta=0.85, fast_w
     """bank_step with the library's fixed device scratch (no allocation by the call); for
     callers that cannot allocate device memory.  Calls that overlap on the GPU race."""
     import torch
-    assert grad.dtype == torch.float32, "anvil_bank_step_noalloc takes fp32 grads"
+    _require(grad.dtype == torch.float32, "anvil_bank_step_noalloc takes fp32 grads")
     _desc(grad, velocity, out)
     g, m, n = grad.shape
     marr, nm = (None, 0) if maps is None else _maps_arg(maps)
@@ -275,10 +298,9 @@ def bank_step_traced(bank: Bank, workspace, maps=None, margin=1.05, eps=1e-6, st
          "B": torch.empty((nm, g, s, s), dtype=torch.bfloat16, device=dev)}
     tr = Trace(*(t[k].data_ptr() for k in ("X_raw", "d", "X", "A", "B")))
     desc = bank.desc()
-    st = _lib.anvil_bank_step_traced(ctypes.byref(desc), None, marr, nm, margin, eps,
-                                     workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                     ctypes.byref(tr),
-                                     _stream_arg(stream))
+    wsp, wsb = _workspace_arg(workspace, bank.grad)
+    st = _lib.anvil_bank_step_traced(ctypes.byref(desc), None, marr, nm, margin, eps, wsp, wsb,
+                                     ctypes.byref(tr), _stream_arg(stream))
     _check(st, "anvil_bank_step_traced")
     return t
 
@@ -295,14 +317,19 @@ class Tail:
 
     def desc(self):
         import torch
+        _require(self.update.dim() == 3, "update must be [g, m, n]")
         g, m, n = self.update.shape
-        assert self.update.dtype == torch.bfloat16 and self.param.dtype == torch.bfloat16
-        assert self.mantissa.dtype in (torch.int16, torch.uint16) and self.mantissa.shape == (g, m, n)
-        assert self.velocity.shape == (2, g, m, n) and self.velocity.dtype == torch.float32
-        assert self.lane_energy.shape == (g, m if m >= n else n) and self.lane_energy.dtype == torch.float32
-        assert self.eff_lr.shape == (g,) and self.eff_lr.dtype == torch.float32
-        for t in (self.update, self.velocity, self.lane_energy, self.param, self.mantissa, self.eff_lr):
-            assert t.is_cuda and t.is_contiguous()
+        _require(self.update.dtype == torch.bfloat16 and self.param.dtype == torch.bfloat16,
+                 "update and param must be bf16")
+        _require(tuple(self.param.shape) == (g, m, n), "param must be [g, m, n]")
+        _require(self.mantissa.dtype in (torch.int16, torch.uint16) and tuple(self.mantissa.shape) == (g, m, n),
+                 "mantissa must be 16-bit [g, m, n]")
+        _require(tuple(self.velocity.shape) == (2, g, m, n) and self.velocity.dtype == torch.float32,
+                 "velocity must be fp32 [2, g, m, n]")
+        _require(tuple(self.lane_energy.shape) == (g, m if m >= n else n) and self.lane_energy.dtype == torch.float32,
+                 "lane_energy must be fp32 [g, max(m, n)]")
+        _require(tuple(self.eff_lr.shape) == (g,) and self.eff_lr.dtype == torch.float32, "eff_lr must be fp32 [g]")
+        _on_one_gpu((self.update, self.velocity, self.lane_energy, self.param, self.mantissa, self.eff_lr), "tail")
         return TailDesc(self.update.data_ptr(), self.velocity.data_ptr(), self.lane_energy.data_ptr(),
                         self.param.data_ptr(), self.mantissa.data_ptr(), self.eff_lr.data_ptr(),
                         g, m, n, self.eff_wd, self.beta2)
@@ -317,8 +344,8 @@ def tail_workspace_bytes(shapes):
 def update_tail(tails, workspace, stream=None):
     """The page's update tail (equaliser + sign-aligned decay) over several banks."""
     descs = (TailDesc * len(tails))(*[t.desc() for t in tails])
-    st = _lib.anvil_update_tail(descs, len(tails), workspace.data_ptr(),
-                                workspace.numel() * workspace.element_size(), _stream_arg(stream))
+    wsp, wsb = _workspace_arg(workspace, tails[0].update)
+    st = _lib.anvil_update_tail(descs, len(tails), wsp, wsb, _stream_arg(stream))
     _check(st, "anvil_update_tail")
 
 
@@ -326,7 +353,9 @@ def adam_step(param, grad, exp_avg, exp_avg_sq, beta1, beta2, eps, step_size, ef
     """The page's Adam step with cautious weight decay, in place on fp32 CUDA tensors."""
     import torch
     for t in (param, grad, exp_avg, exp_avg_sq):
-        assert t.is_cuda and t.dtype == torch.float32 and t.is_contiguous() and t.numel() == param.numel()
+        _require(t.dtype == torch.float32 and t.numel() == param.numel(),
+                 "adam_step: fp32 tensors of one size")
+    _on_one_gpu((param, grad, exp_avg, exp_avg_sq), "adam_step")
     st = _lib.anvil_adam_step(param.data_ptr(), grad.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(),
                               param.numel(), beta1, beta2, eps, step_size, eff_wd, _stream_arg(stream))
     _check(st, "anvil_adam_step")

@@ -127,3 +127,33 @@ def test_tail_argument_errors():
     assert tail(param=4 * G + 1) == anvil.ERR_ALIGNMENT
     assert tail(mantissa=4 * G + 16) == anvil.ERR_ALIAS   # mantissa over the parameter
     assert tail(lane_energy=2 * G) == anvil.ERR_ALIAS     # state written over the rails
+
+
+def test_binding_rejects_tensors_the_kernels_cannot_take():
+    """The Python binding refuses, before any CUDA call (and whatever python -O strips),
+    tensors whose pointers or extents the kernels would trust: host tensors, wrong dtypes
+    or shapes, a workspace off the banks' device."""
+    import torch
+    g, m, n = 2, 8, 4
+    grad = torch.zeros((g, m, n))
+    vel = torch.zeros((2, g, m, n))
+    out = torch.zeros((g, m, n), dtype=torch.bfloat16)
+    ws = torch.zeros(1 << 16, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA device"):
+        anvil.multi_bank_step([anvil.Bank(grad, vel, out)], ws)
+    with pytest.raises(ValueError, match="velocity must be"):
+        anvil.multi_bank_step([anvil.Bank(grad, torch.zeros((g, m, n)), out)], ws)
+    with pytest.raises(ValueError, match="out must be bf16"):
+        anvil.multi_bank_step([anvil.Bank(grad, vel, torch.zeros((g, m, n)))], ws)
+    with pytest.raises(ValueError, match="grad must be"):
+        anvil.multi_bank_step([anvil.Bank(grad.double(), vel, out)], ws)
+    with pytest.raises(ValueError, match="fp32 grads"):
+        anvil.bank_step(grad.bfloat16(), vel, out)
+    with pytest.raises(ValueError, match="CUDA device"):
+        anvil.adam_step(*(torch.zeros(16) for _ in range(4)), 0.9, 0.95, 1e-8, 1e-3, 0.0)
+    with pytest.raises(ValueError, match="one size"):
+        anvil.adam_step(torch.zeros(16), torch.zeros(8), torch.zeros(16), torch.zeros(16), 0.9, 0.95, 1e-8, 1e-3, 0.0)
+    tail = anvil.Tail(out, vel, torch.zeros((g, m)), out.clone(), torch.zeros((g, m, n), dtype=torch.int32),
+                      torch.zeros(g), 0.1, 0.9)
+    with pytest.raises(ValueError, match="mantissa"):
+        anvil.update_tail([tail], ws)
