@@ -125,7 +125,8 @@ def momentum(grad, velocity, momentum, fast_beta, fast_weight, slow_beta):
     """
     grad = np.ascontiguousarray(grad, np.float32)
     vel = np.array(velocity, np.float32, copy=True, order="C")
-    assert vel.shape == (2,) + grad.shape
+    if vel.shape != (2,) + grad.shape:
+        raise ValueError("velocity must be [2, g, m, n]")
     g = np.empty_like(grad)
     X = np.empty(grad.shape, np.uint16)
     lib().oracle_momentum(_ptr(grad), _ptr(vel[0]), _ptr(vel[1]), grad.size, momentum,
@@ -182,7 +183,8 @@ def bank_step(grad, velocity, momentum, fast_beta, fast_weight, slow_beta, maps=
     grad = np.ascontiguousarray(grad, np.float32)
     g, rows, cols = grad.shape
     vel = np.array(velocity, np.float32, copy=True, order="C")
-    assert vel.shape == (2, g, rows, cols)
+    if vel.shape != (2, g, rows, cols):
+        raise ValueError("velocity must be [2, g, m, n]")
     m = _maps32(maps)
     out = np.empty(grad.shape, np.uint16)
     rc = lib().oracle_bank_step(_ptr(grad), _ptr(vel), g, rows, cols, momentum, fast_beta,
@@ -199,7 +201,8 @@ def rail_equalizer(v_bits, lane_energy, beta2):
     v_bits = np.ascontiguousarray(v_bits, np.uint16)
     g, rows, cols = v_bits.shape
     le = np.array(lane_energy, np.float32, copy=True, order="C")
-    assert le.shape == (g, rows if rows >= cols else cols)
+    if le.shape != (g, rows if rows >= cols else cols):
+        raise ValueError("lane_energy must be [g, max(rows, cols)]")
     out = np.empty_like(v_bits)
     lib().oracle_rail_equalizer(_ptr(v_bits), g, rows, cols, _ptr(le), beta2, _ptr(out))
     return out, le
@@ -214,7 +217,8 @@ def sign_aligned_decay(p_bits, mantissa, update_bits, gate, wd, lr):
     gt = np.ascontiguousarray(gate, np.float32)
     lr = np.ascontiguousarray(lr, np.float32)
     g = p.shape[0]
-    assert lr.shape == (g,) and p.shape == mt.shape == u.shape == gt.shape
+    if not (lr.shape == (g,) and p.shape == mt.shape == u.shape == gt.shape):
+        raise ValueError("lr [g] and p, mantissa, update, gate of one shape")
     lib().oracle_sign_aligned_decay(_ptr(p), _ptr(mt), _ptr(u), _ptr(gt), g, p[0].size, wd, _ptr(lr))
     return p, mt
 
@@ -233,7 +237,8 @@ def adam_step(p, g, exp_avg, exp_avg_sq, beta1, beta2, eps, step_size, eff_wd):
     m = np.array(exp_avg, np.float32, copy=True, order="C")
     v = np.array(exp_avg_sq, np.float32, copy=True, order="C")
     g = np.ascontiguousarray(g, np.float32)
-    assert p.shape == g.shape == m.shape == v.shape
+    if not (p.shape == g.shape == m.shape == v.shape):
+        raise ValueError("param, grad, exp_avg, exp_avg_sq of one shape")
     lib().oracle_adam_step(_ptr(p), _ptr(g), _ptr(m), _ptr(v), p.size, beta1, beta2, eps, step_size,
                            eff_wd)
     return p, m, v
