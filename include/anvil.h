@@ -24,8 +24,9 @@
  * stream).  A step is three kernels on that stream: momentum + cast, the normaliser d,
  * and one persistent kernel for the whole cascade (the normalisation and every product of
  * every map).  No call below allocates, frees or synchronises, except
- * anvil_bank_step on its first use of a size (documented there) and the
- * diagnostic anvil_device_error.  Errors are returned as status codes; no
+ * anvil_bank_step on its first use of a size (documented there), the error reads
+ * anvil_last_device_error (waits for its stream) and anvil_device_error (waits for the
+ * device).  Errors are returned as status codes; no
  * exception crosses the ABI.
  */
 #ifndef ANVIL_H
@@ -47,7 +48,7 @@ typedef enum {
     ANVIL_ERR_ALIAS = 4,             /* a written buffer overlaps another buffer of the call */
     ANVIL_ERR_WORKSPACE = 5,         /* workspace too small, or cannot be allocated during capture */
     ANVIL_ERR_CUDA = 6,              /* a CUDA runtime/driver call or a launch failed */
-    ANVIL_ERR_TIMEOUT = 7,           /* a bounded device-side wait gave up (see anvil_device_error) */
+    ANVIL_ERR_TIMEOUT = 7,           /* a bounded device-side wait gave up (see anvil_last_device_error) */
     ANVIL_ERR_DEVICE = 8             /* current device is not sm_103 (the kernels are sm_103a only) */
 } anvil_status;
 
@@ -230,6 +231,14 @@ anvil_status anvil_bank_step_traced(const anvil_bank_desc* bank, const anvil_sca
  * kernel sets when one of its bounded waits gives up instead of hanging.
  * Synchronises the device.  Returns ANVIL_OK, ANVIL_ERR_TIMEOUT or ANVIL_ERR_CUDA. */
 anvil_status anvil_device_error(int clear);
+
+/* The error word as the work queued so far on `stream` leaves it: waits for that stream
+ * only (cudaStreamSynchronize), then reads and resets the word with one atomic exchange
+ * on the device, so a timeout is reported once.  The word belongs to the device, not to
+ * the stream: a wait that gave up in work on another stream shows here too if it gave up
+ * before this read, and otherwise in a later read.  Returns ANVIL_OK, ANVIL_ERR_TIMEOUT,
+ * ANVIL_ERR_CUDA or ANVIL_ERR_DEVICE. */
+anvil_status anvil_last_device_error(void* stream);
 
 /* Self-test of the bounded waits: launches one block that waits on a barrier
  * nothing will ever complete, for at most timeout_us microseconds, after which

@@ -103,6 +103,8 @@ _lib.anvil_adam_step.argtypes = [_vp, _vp, _vp, _vp, _sz, _f, _f, _f, _f, _f, _v
 _lib.anvil_adam_step.restype = _i
 _lib.anvil_device_error.argtypes = [_i]
 _lib.anvil_device_error.restype = _i
+_lib.anvil_last_device_error.argtypes = [_vp]
+_lib.anvil_last_device_error.restype = _i
 _lib.anvil_selftest_wait_timeout.argtypes = [ctypes.c_uint, _vp]
 _lib.anvil_selftest_wait_timeout.restype = _i
 _lib.anvil_profile_begin.argtypes = [_i]
@@ -376,6 +378,12 @@ def schedule_runs(shapes, nmaps=6):
 def device_error(clear=True):
     """Status of the device error word (ANVIL_OK or ANVIL_ERR_TIMEOUT); synchronises."""
     return _lib.anvil_device_error(1 if clear else 0)
+
+
+def last_device_error(stream=None):
+    """Status of the device error word after the work queued on `stream` (default: the
+    current stream); waits for that stream only and resets the word."""
+    return _lib.anvil_last_device_error(_stream_arg(stream))
 
 
 def selftest_wait_timeout(timeout_us, stream=None):

@@ -487,6 +487,17 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
     return ANVIL_OK;
 }
 
+// Workspace bytes of one call after run_step's checks that need no workspace or device
+// (shapes, pointers, maps); 0 with *st set when one fails.
+size_t checked_layout_bytes(const anvil_bank_desc* bank, const anvil_map* maps, int nmaps,
+                            anvil_status* st) {
+    Layout L;
+    if ((*st = make_layout(bank, 1, &L)) != ANVIL_OK) return 0;
+    if ((*st = check_banks(bank, 1)) != ANVIL_OK) return 0;
+    if ((*st = check_maps(maps, nmaps)) != ANVIL_OK) return 0;
+    return L.total;
+}
+
 // ---------------------------------------------------------------- update tail
 struct TailLayout {
     int total_mats;
@@ -711,8 +722,13 @@ anvil_status anvil_bank_step(const float* grad, float* velocity, int g, int m, i
         maps = kAnvilMaps;
         nmaps = 6;
     }
-    const size_t need = anvil_workspace_bytes(&b, 1);
-    if (need == 0) return ANVIL_ERR_INVALID_ARG;
+    // the argument checks and the device check come before the workspace is touched, so a
+    // bad call returns the same status as anvil_multi_bank_step and allocates nothing
+    anvil_status st;
+    const size_t need = checked_layout_bytes(&b, maps, nmaps, &st);
+    if (st != ANVIL_OK) return st;
+    DeviceState* ds = nullptr;
+    if ((st = device_setup(&ds)) != ANVIL_OK) return st;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -755,6 +771,16 @@ anvil_status anvil_device_error(int clear) {
     if (clear && (e = cudaMemset(dev->err, 0, sizeof(unsigned))))
         return cuda_fail(e, "clear error word");
     if (clear && (e = cudaDeviceSynchronize())) return cuda_fail(e, "cudaDeviceSynchronize");
+    return (word & DEVERR_TIMEOUT) ? ANVIL_ERR_TIMEOUT : ANVIL_OK;
+}
+
+anvil_status anvil_last_device_error(void* stream) {
+    DeviceState* dev = nullptr;
+    anvil_status st = device_setup(&dev);
+    if (st != ANVIL_OK) return st;
+    unsigned word = 0;
+    cudaError_t e = read_error_word_on_stream(dev->err, 1, &word, static_cast<cudaStream_t>(stream));
+    if (e) return cuda_fail(e, "read error word");
     return (word & DEVERR_TIMEOUT) ? ANVIL_ERR_TIMEOUT : ANVIL_OK;
 }
 
@@ -855,16 +881,18 @@ anvil_status anvil_bank_step_noalloc(const float* grad, float* velocity, int g, 
         maps = kAnvilMaps;
         nmaps = 6;
     }
-    Layout L;
-    anvil_status st = make_layout(&b, 1, &L);
+    anvil_status st;
+    const size_t need = checked_layout_bytes(&b, maps, nmaps, &st);
     if (st != ANVIL_OK) return st;
-    if (L.total > ANVIL_STATIC_SCRATCH_BYTES) {
+    if (need > ANVIL_STATIC_SCRATCH_BYTES) {
         snprintf(g_last_error, sizeof(g_last_error),
                  "anvil_bank_step_noalloc: %d x %d x %d needs %zu bytes of scratch; the fixed "
                  "scratch holds %zu",
-                 g, m, n, L.total, static_cast<size_t>(ANVIL_STATIC_SCRATCH_BYTES));
+                 g, m, n, need, static_cast<size_t>(ANVIL_STATIC_SCRATCH_BYTES));
         return ANVIL_ERR_WORKSPACE;
     }
+    DeviceState* ds = nullptr;
+    if ((st = device_setup(&ds)) != ANVIL_OK) return st;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "anvil_device.cuh"
 #include "anvil_internal.h"
 
@@ -162,8 +164,15 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
     }
 }
 
+// The step's first kernel is launched without programmatic serialisation, so it starts
+// after whatever the stream ran before it has finished.  Measured on a CUDA graph of 20
+// consecutive steps: with a programmatic edge from the previous step's cascade the steps
+// took 1.11-1.13 ms, with a plain edge 1.05-1.07 ms, as separate per-step graphs do.
+// (Its griddepcontrol.wait is then a no-op; its launch_dependents still lets the norm_d
+// kernel that follows be scheduled early.)
 cudaError_t launch_momentum(const MomentumParams& p, cudaStream_t stream) {
-    return launch_pdl(momentum_kernel, dim3(p.total_tiles), dim3(256), 0, stream, p);
+    momentum_kernel<<<dim3(p.total_tiles), dim3(256), 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 static_assert(SCHED_COUNTERS <= 256, "norm_d_kernel zeroes the item counters with one block");
@@ -281,6 +290,28 @@ cudaError_t launch_wait_selftest(unsigned timeout_us, unsigned* err, cudaStream_
     wait_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<unsigned long long>(timeout_us) * 1000ull,
                                                err);
     return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- per-stream error read
+// Each read takes the error word with one atomic (exchange with 0 when clearing) into a
+// slot of its own, which the host then copies back on the same stream.
+constexpr int ERROR_SLOTS = 64;
+__device__ unsigned g_error_taken[ERROR_SLOTS];
+
+__global__ void take_error_kernel(unsigned* err, unsigned* slot, int clear) {
+    *slot = clear ? atomicExch(err, 0u) : atomicOr(err, 0u);
+}
+
+cudaError_t read_error_word_on_stream(unsigned* err, int clear, unsigned* word, cudaStream_t stream) {
+    static std::atomic<unsigned> next{0};
+    unsigned* slots = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&slots), g_error_taken);
+    if (e) return e;
+    unsigned* slot = slots + (next.fetch_add(1u) % ERROR_SLOTS);
+    take_error_kernel<<<1, 1, 0, stream>>>(err, slot, clear);
+    if ((e = cudaGetLastError())) return e;
+    if ((e = cudaMemcpyAsync(word, slot, sizeof(unsigned), cudaMemcpyDeviceToHost, stream))) return e;
+    return cudaStreamSynchronize(stream);
 }
 
 unsigned* device_error_word() {

@@ -197,5 +197,8 @@ cudaError_t launch_wait_selftest(unsigned timeout_us, unsigned* err, cudaStream_
 
 // Device address of the current device's error word (null if it cannot be had).
 unsigned* device_error_word();
+// Reads the error word (and clears it if asked) after the work queued on `stream`, with one
+// atomic on the device; waits for that stream only.
+cudaError_t read_error_word_on_stream(unsigned* err, int clear, unsigned* word, cudaStream_t stream);
 
 }  // namespace anvil

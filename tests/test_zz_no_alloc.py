@@ -15,10 +15,10 @@ import pytest
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
+import oracle  # noqa: E402
 from polynomial_matrix_whitening_gb300 import workloads as W  # noqa: E402
 
-OUT_RTOL = 1e-2   # relative Frobenius error per matrix, as in the parity tests
-VEL_RTOL = 1e-6
+OUT_RTOL = 1e-2   # relative Frobenius error per matrix against the oracle, as in the parity tests
 
 
 @pytest.fixture(scope="module")
@@ -38,10 +38,13 @@ def _call(fn, grad, vel, out, sc):
 
 @pytest.mark.parametrize("shape", [(3, 300, 130), (22, 256, 768), (2, 130, 1000)])
 def test_noalloc_matches_bank_step_twice(A, shape):
+    """Both entry points run the same kernels on the same layout, so their rails and outputs
+    must be equal bit for bit, on two calls in a row (the second sees whatever the first
+    left in the fixed scratch); the ragged shape is also checked against the oracle."""
     lib = A.library()
     dev = torch.device("cuda")
     sc = (0.95, 0.85, 0.4385, 0.98)
-    for call in range(2):  # two calls in a row: the second sees what the first left behind
+    for call in range(2):
         grad, vel = W.random_case(700 + 10 * call + shape[1], *shape)
         g_d = torch.from_numpy(grad).to(dev)
         v_ref = torch.from_numpy(vel).to(dev)
@@ -51,13 +54,17 @@ def test_noalloc_matches_bank_step_twice(A, shape):
         assert _call(lib.anvil_bank_step, g_d, v_ref, o_ref, sc) == A.OK
         assert _call(lib.anvil_bank_step_noalloc, g_d, v_new, o_new, sc) == A.OK
         torch.cuda.synchronize()
-        vr, vn = v_ref.cpu().numpy(), v_new.cpu().numpy()
-        assert np.max(np.abs(vn - vr)) <= VEL_RTOL * np.max(np.abs(vr))
-        r = o_ref.double().cpu().numpy()
-        x = o_new.double().cpu().numpy()
-        assert np.isfinite(x).all()
-        for i in range(shape[0]):
-            assert np.linalg.norm(x[i] - r[i]) <= OUT_RTOL * np.linalg.norm(r[i]), (call, i)
+        assert torch.equal(v_new, v_ref), call
+        assert torch.equal(o_new.view(torch.int16), o_ref.view(torch.int16)), call
+        if shape == (3, 300, 130):
+            out_or, vel_or = oracle.bank_step(grad, vel, *sc)
+            np.testing.assert_array_equal(v_new.cpu().numpy(), vel_or)
+            got = o_new.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+            for i in range(shape[0]):
+                x = oracle.bf16_to_f32(got[i]).astype(np.float64)
+                r = oracle.bf16_to_f32(out_or[i]).astype(np.float64)
+                assert np.isfinite(x).all()
+                assert np.linalg.norm(x - r) <= OUT_RTOL * np.linalg.norm(r), (call, i)
     assert A.device_error() == A.OK
 
 
