@@ -47,13 +47,19 @@ def rel(a, b):
     return np.linalg.norm(a - b) / (n if n > 0 else 1.0)
 
 
-# Ill-conditioned inputs (power-law, rank-32 plus noise): the method amplifies bf16-level
-# noise in the small singular directions (F'(0) = 643), so the full-matrix difference
-# between two correct implementations that sum in different orders sits near 1e-2 (one
-# flipped input ulp moves the oracle's own output by 0.2-0.5% on these inputs).  There the
-# 1e-2 bar applies on the dominant subspace (sigma/d >= 3.3e-3, where F >= 0.999), with a
-# 3e-2 full-matrix bound.
+# Ill-conditioned input (the power-law workload, sigma_i = i^-1.5): the cascade amplifies
+# bf16-level differences in the small singular directions (F'(0) = 643), and how products
+# are summed decides the bf16 roundings of the Gram.  The oracle sums in sequential fp32 with
+# round-to-nearest; the tensor cores that run these products, here and in the page's own
+# arrangement (torch bmm / baddbmm in bf16, i.e. cuBLAS), accumulate with a bias toward
+# zero, which over the 2816-long Gram sums leaves the output 1.2-1.3% from the oracle on
+# this input.  The bar there: the full-matrix error may exceed 1e-2 only up to 1.1x the
+# distance between the page's arrangement run by torch on this GPU and the oracle (and
+# never 3e-2), and the 1e-2 bar holds on the dominant subspace (sigma/d >= 3.3e-3, where
+# F >= 0.999).  (The two tensor-core results need not be close to each other: on a
+# rank-32 + noise matrix both sat 0.6% from the oracle and 1.5% from one another.)
 ILL_FULL_RTOL = 3e-2
+ILL_PAGE_FACTOR = 1.1
 
 
 def dominant_rel(out_gpu, out_or, X_or):
@@ -64,17 +70,52 @@ def dominant_rel(out_gpu, out_or, X_or):
     return rel(P(out_gpu), P(out_or))
 
 
+def torch_arrangement(X_bits, maps=oracle.ANVIL_MAPS, margin=1.05, eps=1e-6):
+    """The page's tensor operations on one bf16 matrix, run by torch on this GPU: matrix
+    products in bf16 with fp32 accumulation (cuBLAS), `b A + c A A` and `a X + X B` each
+    one fp32 epilogue and one bf16 rounding (baddbmm), the trace from the bf16 Gram's
+    diagonal.  A measure of what tensor-core accumulation does to this input, not an
+    expected value: the expected value is the oracle's."""
+    prev = torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction
+    torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = False
+    try:
+        x = torch.from_numpy(np.ascontiguousarray(X_bits).view(np.int16)).cuda().view(torch.bfloat16)
+        tall = x.shape[0] > x.shape[1]
+
+        def gram(y):
+            return (y.mT @ y) if tall else (y @ y.mT)
+
+        a0 = gram(x)
+        d = a0.diagonal().float().sum().sqrt() * np.float32(margin) + np.float32(eps)
+        y = (x.float() / d).to(torch.bfloat16)
+        acc = (a0.float() / (d * d)).to(torch.bfloat16)
+        for k, (a, b, c) in enumerate(maps):
+            a, b, c = (float(np.float32(v)) for v in (a, b, c))
+            if k > 0:
+                acc = gram(y)
+            bm = torch.baddbmm(acc[None], acc[None], acc[None], beta=b, alpha=c)[0]
+            y = (torch.baddbmm(y[None], y[None], bm[None], beta=a)[0] if tall
+                 else torch.baddbmm(y[None], bm[None], y[None], beta=a)[0])
+        return bits(y)
+    finally:
+        torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = prev
+
+
 def check_output(out_gpu, out_or, X_or, ill):
-    """Returns (full-matrix rel error, dominant-subspace rel error) after asserting the bar."""
+    """Returns (full-matrix rel error, dominant-subspace rel error or None, the page
+    arrangement's rel error or None) after asserting the bar."""
     got, want = f64(out_gpu), f64(out_or)
     assert np.isfinite(got).all()
     full = rel(got, want)
     if not ill:
         assert full <= OUT_RTOL, full
-        return full, None
+        return full, None, None
+    page = f64(torch_arrangement(X_or))
+    e_page = rel(page, want)
     dom = dominant_rel(out_gpu, out_or, X_or)
-    assert dom <= OUT_RTOL and full <= ILL_FULL_RTOL, (full, dom)
-    return full, dom
+    assert dom <= OUT_RTOL, dom
+    assert full <= max(OUT_RTOL, ILL_PAGE_FACTOR * e_page) and full <= ILL_FULL_RTOL, (full, e_page)
+    return full, dom, e_page
 
 
 def gpu_bank(A, grad, vel, scal):
@@ -101,6 +142,18 @@ def test_bounded_wait_gives_up_and_reports(A):
     assert A.device_error(clear=True) == A.OK
     x = torch.ones(4, device="cuda")
     assert float(x.sum()) == 4.0
+
+
+def test_last_device_error_reads_one_stream(A):
+    """The per-stream read: a wait that gives up in work queued on a side stream is
+    reported by anvil_last_device_error on that stream, once (the read resets the word),
+    without waiting for the device."""
+    s = torch.cuda.Stream()
+    assert A.last_device_error(s) == A.OK
+    A.selftest_wait_timeout(2000, stream=s)
+    assert A.last_device_error(s) == A.ERR_TIMEOUT
+    assert A.last_device_error(s) == A.OK
+    assert A.device_error(clear=True) == A.OK
 
 
 # ------------------------------------------------------------------ stage by stage
@@ -573,8 +626,8 @@ def _closed_form_check(X_bits, out_bits, tall, ill_conditioned):
     return rel(blk, np.diag(F[keep]))
 
 
-WORKLOAD_STEPS = {"single_wide": 1, "single_wide_blend": 1, "qk_bank": 10, "vo_bank": 3,
-                  "mlp_bank": 2}
+WORKLOAD_STEPS = {"single_wide": 1, "single_wide_blend": 1, "qk_bank": 10, "vo_bank": 10,
+                  "mlp_bank": 10}
 
 
 @pytest.mark.parametrize("name", list(WORKLOAD_STEPS))
@@ -599,76 +652,94 @@ def test_workload_parity(A, name):
         A.multi_bank_step([bank], ws)
         X_or, _, vel_or = oracle.momentum(grad, vel_or, sc.momentum, sc.fast_beta, sc.fast_weight,
                                           sc.slow_beta)
+        # the rails every step (every element), the output at the first and last step
+        vg = bank.velocity.cpu().numpy()
+        assert np.max(np.abs(vg - vel_or)) <= VEL_RTOL * np.max(np.abs(vel_or)), step
         if step in (0, steps - 1):
-            torch.cuda.synchronize()
-            vg = bank.velocity.cpu().numpy()
-            assert np.max(np.abs(vg - vel_or)) <= VEL_RTOL * np.max(np.abs(vel_or))
             out = bits(bank.out)
             ill = wl.kind == "power_law"
             for i in sample:
                 o = oracle.cascade(X_or[i])
-                full, dom = check_output(out[i], o, X_or[i], ill)
+                full, dom, e_page = check_output(out[i], o, X_or[i], ill)
                 cf = _closed_form_check(X_or[i], out[i], b0.m > b0.n, ill)
                 print(f"{name} step {step} matrix {i}: vs oracle {full:.2e}"
-                      f"{'' if dom is None else f' (dominant {dom:.2e})'}, vs closed form {cf:.2e}")
+                      f"{'' if dom is None else f' (dominant {dom:.2e}; page arrangement {e_page:.2e})'}"
+                      f", vs closed form {cf:.2e}")
                 assert cf <= CLOSED_RTOL
 
 
 def test_full_step_graph_parity(A):
-    """All three banks in one grouped step, captured in one CUDA graph per grad-pool entry,
-    100 replays; parity checked at steps 1, 2, 50 and 100 on matrices {0, 10, 11, 21}."""
+    """All three banks, the whole 100-step sequence captured in ONE CUDA graph (the grad
+    pool of 4 cycled by pointer, the post-engage scalars read from a device block when the
+    graph runs) and replayed once.  Inside the graph, after steps 1, 2, 50 and 100, the
+    outputs and rails of matrices {0, 10, 11, 21} of every bank are copied aside; each is
+    checked against the oracle run step by step: rails within 1e-6, Gaussian outputs within
+    the plain 1e-2 full-matrix bar.  The rank-32 + noise matrices (11-21) are held to the
+    ill-conditioned bar: once the rails mix the pool's four rank-32 gradients, their noise
+    directions sit where the cascade amplifies accumulation differences (the qk bank's
+    matrix 21 measured 1.02e-2 at step 50, as far from the oracle as the page's own
+    arrangement on this GPU)."""
     wl = W.workloads()["full_step"]
-    pool = [[wl.grad(j, p) for j in range(3)] for p in range(wl.pool)]
     dev = torch.device("cuda")
+    pool = [[wl.grad(j, p) for j in range(3)] for p in range(wl.pool)]
     pool_d = [[torch.from_numpy(x).to(dev) for x in p] for p in pool]
     vels = [wl.velocity(j) for j in range(3)]
-    banks = []
-    for j, b in enumerate(wl.banks):
-        banks.append(A.Bank(pool_d[0][j], torch.from_numpy(vels[j]).to(dev),
-                            torch.empty((b.g, b.m, b.n), dtype=torch.bfloat16, device=dev),
-                            **scal_dict(wl.scalars(0))))
-    shapes = [b.shape for b in banks]
-    ws = A.alloc_workspace(shapes)
+    sc = wl.scalars(0)
+    banks = [A.Bank(pool_d[0][j], torch.from_numpy(vels[j]).to(dev),
+                    torch.empty((b.g, b.m, b.n), dtype=torch.bfloat16, device=dev), **scal_dict(sc))
+             for j, b in enumerate(wl.banks)]
+    ws = A.alloc_workspace([b.shape for b in banks])
+    dsc = torch.tensor([[sc.momentum, sc.fast_beta, sc.fast_weight, sc.slow_beta]] * 3,
+                       dtype=torch.float32, device=dev)
+    check, sample = (1, 2, 50, 100), [0, 10, 11, 21]
+    snap_out = {t: [torch.empty((len(sample), b.m, b.n), dtype=torch.bfloat16, device=dev)
+                    for b in wl.banks] for t in check}
+    snap_vel = {t: [torch.empty((2, len(sample), b.m, b.n), dtype=torch.float32, device=dev)
+                    for b in wl.banks] for t in check}
+    vel0 = [b.velocity.clone() for b in banks]
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
-    graphs = []
-    vel0 = [b.velocity.clone() for b in banks]
+    graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(s):
-        for p in range(wl.pool):
-            for j, b in enumerate(banks):
-                b.grad = pool_d[p][j]
-            A.multi_bank_step(banks, ws, stream=s)  # warm-up (outside capture)
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=s):
-                A.multi_bank_step(banks, ws, stream=s)
-            graphs.append(gr)
+        A.multi_bank_step(banks, ws, d_scalars=dsc, stream=s)  # device set-up, outside capture
+        s.synchronize()
         for b, v in zip(banks, vel0):
             b.velocity.copy_(v)
+        with torch.cuda.graph(graph, stream=s):
+            for step in range(1, 101):
+                for j, b in enumerate(banks):
+                    b.grad = pool_d[(step - 1) % wl.pool][j]
+                A.multi_bank_step(banks, ws, d_scalars=dsc, stream=s)
+                if step in check:
+                    for j, b in enumerate(banks):
+                        for k, i in enumerate(sample):
+                            snap_out[step][j][k].copy_(b.out[i])
+                            snap_vel[step][j][:, k].copy_(b.velocity[:, i])
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
-    vel_or = vels
-    check = {1, 2, 50, 100}
-    sample = [0, 10, 11, 21]
+    graph.replay()
+    torch.cuda.synchronize()
+    assert A.device_error() == A.OK
+
+    vel_or = [np.ascontiguousarray(v[:, sample]) for v in vels]
     for step in range(1, 101):
-        graphs[(step - 1) % wl.pool].replay()
-        sc = wl.scalars(step - 1)
         Xs = []
         for j in range(3):
-            X, _, vel_or[j] = oracle.momentum(pool[(step - 1) % wl.pool][j], vel_or[j], sc.momentum,
-                                              sc.fast_beta, sc.fast_weight, sc.slow_beta)
+            grad = np.ascontiguousarray(pool[(step - 1) % wl.pool][j][sample])
+            X, _, vel_or[j] = oracle.momentum(grad, vel_or[j], sc.momentum, sc.fast_beta,
+                                              sc.fast_weight, sc.slow_beta)
             Xs.append(X)
-        if step in check:
-            torch.cuda.synchronize()
-            for j, b in enumerate(banks):
-                vg = b.velocity.cpu().numpy()
-                assert np.max(np.abs(vg - vel_or[j])) <= VEL_RTOL * np.max(np.abs(vel_or[j]))
-                out = bits(b.out)
-                for i in sample:
-                    o = oracle.cascade(Xs[j][i])
-                    full, dom = check_output(out[i], o, Xs[j][i], i >= 11)
-                    tall = b.grad.shape[1] > b.grad.shape[2]
-                    cf = _closed_form_check(Xs[j][i], out[i], tall, i >= 11)
-                    print(f"full_step step {step} bank {j} matrix {i}: vs oracle {full:.2e}"
-                          f"{'' if dom is None else f' (dominant {dom:.2e})'}, vs closed form {cf:.2e}")
-                    assert cf <= CLOSED_RTOL
-    assert A.device_error() == A.OK
+        if step not in check:
+            continue
+        for j, b in enumerate(wl.banks):
+            vg = snap_vel[step][j].cpu().numpy()
+            assert np.max(np.abs(vg - vel_or[j])) <= VEL_RTOL * np.max(np.abs(vel_or[j])), (step, j)
+            out = bits(snap_out[step][j])
+            for k, i in enumerate(sample):
+                o = oracle.cascade(Xs[j][k])
+                full, dom, e_page = check_output(out[k], o, Xs[j][k], i >= 11)
+                cf = _closed_form_check(Xs[j][k], out[k], b.m > b.n, i >= 11)
+                print(f"full_step step {step} bank {j} matrix {i}: vs oracle {full:.2e}"
+                      f"{'' if dom is None else f' (dominant {dom:.2e}; page arrangement {e_page:.2e})'}"
+                      f", vs closed form {cf:.2e}{' (dominant subspace)' if i >= 11 else ''}")
+                assert cf <= CLOSED_RTOL
