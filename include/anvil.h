@@ -49,7 +49,8 @@ typedef enum {
     ANVIL_ERR_WORKSPACE = 5,         /* workspace too small, or cannot be allocated during capture */
     ANVIL_ERR_CUDA = 6,              /* a CUDA runtime/driver call or a launch failed */
     ANVIL_ERR_TIMEOUT = 7,           /* a bounded device-side wait gave up (see anvil_last_device_error) */
-    ANVIL_ERR_DEVICE = 8             /* current device is not sm_103 (the kernels are sm_103a only) */
+    ANVIL_ERR_DEVICE = 8,            /* current device is not sm_103 (the kernels are sm_103a only) */
+    ANVIL_ERR_UNAVAILABLE = 9        /* a diagnostic this build of the library does not include */
 } anvil_status;
 
 /* One quintic spectral map f(s) = a s + b s^3 + c s^5 (an ANVIL_MAPS entry). */
@@ -294,6 +295,26 @@ typedef struct {
     int tiles;  /* items per matrix in this phase */
 } anvil_schedule_run;
 int anvil_schedule_runs(const anvil_bank_desc* banks, int nbanks, int nmaps, anvil_schedule_run* runs, int cap);
+
+/* Per-item timeline of the cascade kernel, for performance work.  Only a library built
+ * with the timeline option (build.py --timeline, which writes libanvil_timeline.so)
+ * records it; this library returns ANVIL_ERR_UNAVAILABLE.  Item t (0-based, in the
+ * order of anvil_schedule_runs) of the latest cascade launch owns 16 64-bit words
+ * starting at word 16 t, for t < ANVIL_TIMELINE_ITEMS:
+ *   0 pair | (op | bank << 8 | phase << 16) << 16 | matrix << 48;  1 block row | block
+ *   column << 16 | k-blocks << 32;  then %globaltimer nanoseconds when 2 the pair's
+ *   scheduler took it, 3 its input phases were complete, 4 its entry was handed out,
+ *   5 the first operand load was armed, 6 the MMA issuer read it, 7 its accumulator was
+ *   free, 8 its first k-block landed, 9 its last MMAs were issued, 10 the epilogue found
+ *   the accumulator complete, 11 the epilogue was done;  12 and 13: SM cycles (clock64)
+ *   at 8 and 9;  14 SM cycles the MMA issuer waited for k-blocks after the first to
+ *   land;  15 SM cycles the producer waited for free operand stages.  Words of a field
+ *   an item does not have (a normalisation tile has no MMA) stay zero.
+ * anvil_timeline_read copies min(bytes, the buffer) to host memory (synchronous; call
+ * after the launch has completed).  anvil_timeline_clear zeroes the buffer. */
+#define ANVIL_TIMELINE_ITEMS 16384
+anvil_status anvil_timeline_read(void* host, size_t bytes);
+anvil_status anvil_timeline_clear(void);
 
 /* Human-readable name of a status. */
 const char* anvil_status_string(anvil_status status);

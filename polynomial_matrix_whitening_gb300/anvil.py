@@ -17,7 +17,10 @@ import os
 import re
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libanvil.so")
+# ANVIL_LIBRARY=timeline loads the timeline build (build.py --timeline) instead, for the
+# cascade timeline tool; the computation is the same.
+LIB_PATH = os.path.join(_HERE, "libanvil_timeline.so" if os.environ.get("ANVIL_LIBRARY") == "timeline"
+                        else "libanvil.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "anvil.h")
 
 if not os.path.exists(LIB_PATH):
@@ -27,9 +30,9 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 STATUS = {0: "ANVIL_OK", 1: "ANVIL_ERR_INVALID_ARG", 2: "ANVIL_ERR_UNSUPPORTED_SHAPE",
           3: "ANVIL_ERR_ALIGNMENT", 4: "ANVIL_ERR_ALIAS", 5: "ANVIL_ERR_WORKSPACE",
-          6: "ANVIL_ERR_CUDA", 7: "ANVIL_ERR_TIMEOUT", 8: "ANVIL_ERR_DEVICE"}
+          6: "ANVIL_ERR_CUDA", 7: "ANVIL_ERR_TIMEOUT", 8: "ANVIL_ERR_DEVICE", 9: "ANVIL_ERR_UNAVAILABLE"}
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_ALIGNMENT, ERR_ALIAS, ERR_WORKSPACE, \
-    ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(9)
+    ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE, ERR_UNAVAILABLE = range(10)
 KERNEL_KINDS = ("momentum", "norm_d", "normalize", "gram_norm", "gram", "sqpoly", "xupdate",
                 "xupdate_out", "tail_power", "tail_scale", "tail_apply", "adam", "cascade")
 MAX_MAPS, MAX_BANKS = 16, 8
@@ -113,6 +116,10 @@ _lib.anvil_profile_end.argtypes = [ctypes.POINTER(ProfileRecord), _i]
 _lib.anvil_profile_end.restype = _i
 _lib.anvil_schedule_runs.argtypes = [ctypes.POINTER(BankDesc), _i, _i, ctypes.POINTER(ScheduleRun), _i]
 _lib.anvil_schedule_runs.restype = _i
+_lib.anvil_timeline_read.argtypes = [_vp, _sz]
+_lib.anvil_timeline_read.restype = _i
+_lib.anvil_timeline_clear.argtypes = []
+_lib.anvil_timeline_clear.restype = _i
 _lib.anvil_status_string.argtypes = [_i]
 _lib.anvil_status_string.restype = ctypes.c_char_p
 _lib.anvil_last_cuda_error.restype = ctypes.c_char_p
@@ -373,6 +380,23 @@ def schedule_runs(shapes, nmaps=6):
     runs = (ScheduleRun * max(n, 1))()
     _lib.anvil_schedule_runs(arr, len(shapes), nmaps, runs, n)
     return [{f: getattr(r, f) for f, _ in ScheduleRun._fields_} for r in runs[:n]]
+
+
+TIMELINE_ITEMS, TIMELINE_FIELDS = 16384, 16
+
+
+def timeline_clear():
+    """Zeroes the cascade timeline (timeline build only; AnvilError otherwise)."""
+    _check(_lib.anvil_timeline_clear(), "anvil_timeline_clear")
+
+
+def timeline_read():
+    """The cascade timeline as a numpy uint64 array [TIMELINE_ITEMS, TIMELINE_FIELDS]
+    (timeline build only; AnvilError otherwise)."""
+    import numpy as np
+    buf = np.zeros((TIMELINE_ITEMS, TIMELINE_FIELDS), dtype=np.uint64)
+    _check(_lib.anvil_timeline_read(buf.ctypes.data, buf.nbytes), "anvil_timeline_read")
+    return buf
 
 
 def device_error(clear=True):

@@ -19,6 +19,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libanvil.so")
+# The timeline build (-DANVIL_TIMELINE): the same library with the cascade kernel's
+# per-item timestamps, for performance work only (anvil_timeline_read).
+BUILD_TL = os.path.join(PKG, "_build_timeline")
+LIB_TL = os.path.join(PKG, "libanvil_timeline.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I" + os.path.join(ROOT, "include")] + ARCH
@@ -41,15 +45,20 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), timeline: bool = False) -> str:
+    """Compiles and links libanvil.so (or, with timeline=True, libanvil_timeline.so);
+    returns the library's path."""
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
                      + glob.glob(os.path.join(ROOT, "include", "*.h")))
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir, lib = (BUILD_TL, LIB_TL) if timeline else (BUILD, LIB)
+    if timeline:
+        extra_flags = list(extra_flags) + ["-DANVIL_TIMELINE"]
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     jobs = []
     for src in sources:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         if force or _stale(obj, [src] + headers):
             jobs.append([cc, "-c", src, "-o", obj] + NVCC_FLAGS + list(extra_flags))
     if jobs:
@@ -60,17 +69,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
             if r.returncode != 0:
                 raise RuntimeError(f"nvcc failed on {cmd[2]}")
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in sources]
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    objs = [os.path.join(build_dir, os.path.basename(s)[:-3] + ".o") for s in sources]
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [cc, "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
-            raise RuntimeError("nvcc link of libanvil.so failed")
-        os.replace(tmp, LIB)
-    return LIB
+            raise RuntimeError(f"nvcc link of {os.path.basename(lib)} failed")
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, timeline="--timeline" in sys.argv))

@@ -33,6 +33,7 @@
 using namespace anvil;
 
 static_assert(ANVIL_MAX_MAPS <= MAX_CASCADE_MAPS, "phase table too small for ANVIL_MAX_MAPS");
+static_assert(TL_ITEMS == ANVIL_TIMELINE_ITEMS && TL_FIELDS == 16, "timeline layout of include/anvil.h");
 static_assert(sizeof(CascadeParams) <= 32764, "cascade parameters exceed the kernel parameter limit");
 
 namespace {
@@ -321,11 +322,13 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         if ((st = encode_map(&B.tm[TM_B], B.b, G.g, G.s_pad, G.s_pad, BK, TILE))) return st;
         if ((st = encode_map(&B.tm[TM_AN], B.a, G.g, G.s_pad, G.s_pad, BK, BK))) return st;
         if ((st = encode_map(&B.tm[TM_BN], B.b, G.g, G.s_pad, G.s_pad, BK, BK))) return st;
-        // the last X-update of a wide bank stores `out` [g, m, n] by TMA (boxes of Y) when
-        // its rows are 16-byte aligned; tall banks (out = Y^T) and the rest take plain stores
+        // the last X-update stores `out` [g, m, n] by TMA when its rows are 16-byte aligned:
+        // boxes of Y (64 columns x 128 rows) for a wide bank, transposed 64 x 64 boxes for a
+        // tall one (out = Y^T); other shapes take plain stores
         memset(&B.tm[TM_OUT], 0, sizeof(CUtensorMap));
-        B.out_tma = !G.tall && (G.n % 8 == 0) && !(reinterpret_cast<uintptr_t>(banks[i].out) & 15);
-        if (B.out_tma && (st = encode_map(&B.tm[TM_OUT], banks[i].out, G.g, G.m, G.n, BK, TILE)))
+        B.out_tma = (G.n % 8 == 0) && !(reinterpret_cast<uintptr_t>(banks[i].out) & 15);
+        if (B.out_tma &&
+            (st = encode_map(&B.tm[TM_OUT], banks[i].out, G.g, G.m, G.n, BK, G.tall ? BK : TILE)))
             return st;
     }
 
@@ -855,11 +858,25 @@ const char* anvil_status_string(anvil_status s) {
         case ANVIL_ERR_CUDA: return "ANVIL_ERR_CUDA";
         case ANVIL_ERR_TIMEOUT: return "ANVIL_ERR_TIMEOUT";
         case ANVIL_ERR_DEVICE: return "ANVIL_ERR_DEVICE";
+        case ANVIL_ERR_UNAVAILABLE: return "ANVIL_ERR_UNAVAILABLE";
     }
     return "ANVIL_ERR_UNKNOWN";
 }
 
 const char* anvil_last_cuda_error(void) { return g_last_error; }
+
+anvil_status anvil_timeline_read(void* host, size_t bytes) {
+    if (!host || !bytes) return ANVIL_ERR_INVALID_ARG;
+    const cudaError_t e = timeline_copy(host, bytes, 0);
+    if (e == cudaErrorNotSupported) return ANVIL_ERR_UNAVAILABLE;
+    return e ? cuda_fail(e, "timeline read") : ANVIL_OK;
+}
+
+anvil_status anvil_timeline_clear(void) {
+    const cudaError_t e = timeline_copy(nullptr, 0, 1);
+    if (e == cudaErrorNotSupported) return ANVIL_ERR_UNAVAILABLE;
+    return e ? cuda_fail(e, "timeline clear") : ANVIL_OK;
+}
 
 anvil_status anvil_bank_step_noalloc(const float* grad, float* velocity, int g, int m, int n,
                                      float momentum, float fast_beta, float fast_weight,

@@ -77,6 +77,24 @@ constexpr int PUB_WARP = 2 + EPI_GROUPS * 4;
 constexpr int SCHED_WARP = PUB_WARP + 1;
 constexpr int GEMM_THREADS = 32 * (SCHED_WARP + 1);
 
+// Per-item timeline (only in a library built with -DANVIL_TIMELINE; the macro is empty
+// otherwise and its arguments are not evaluated).  Item t of a launch owns TL_FIELDS
+// 64-bit words, written by the leader CTA of the pair that ran it (TL_* field names in
+// anvil_internal.h): %globaltimer nanoseconds at each hand-off, SM cycles around the
+// k-loop.
+#ifdef ANVIL_TIMELINE
+__device__ unsigned long long g_timeline[TL_ITEMS * TL_FIELDS];
+#define TL_PUT(t, k, v)                                                              \
+    do {                                                                             \
+        const int tl_t_ = (t);                                                       \
+        if (tl_t_ >= 0 && tl_t_ < TL_ITEMS) g_timeline[tl_t_ * TL_FIELDS + (k)] = (v); \
+    } while (0)
+#else
+#define TL_PUT(t, k, v) \
+    do {                \
+    } while (0)
+#endif
+
 __host__ __device__ constexpr bool op_sym(int op) {
     return op == OP_GRAM || op == OP_GRAM_NORM || op == OP_SQPOLY;
 }
@@ -399,8 +417,11 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
     const int col0 = c.bj * PAIR;
     const int r = x.r;
     // the direct tile leaves by TMA except the last X-update into an `out` that cannot
-    // take it (a tall bank's X = Y^T, or rows not 16-byte aligned)
-    const bool tma_direct = OP != OP_XUPDATE_OUT || bk.out_tma;
+    // take it (rows not 16-byte aligned: plain stores); a tall bank's X = Y^T leaves by TMA
+    // too, written transposed into the staging box: quarter q of this CTA's 128 rows is
+    // out rows col0 + 64q .. +63 by out columns row0 .. row0 + 127, two 64 x 64 boxes of out
+    const bool tma_trans = OP == OP_XUPDATE_OUT && bk.tall && bk.out_tma;
+    const bool tma_direct = OP != OP_XUPDATE_OUT || (bk.out_tma && !bk.tall);
     uint64_t coef_x = f2_pack(OP == OP_SQPOLY ? P.b : P.a, OP == OP_SQPOLY ? P.b : P.a);
     const uint64_t coef_v = f2_pack(P.c, P.c);
     float dd = 0.f;
@@ -421,7 +442,16 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
         } else if (!mbar_wait(&x.epi_bar[q], in_phase, p.err)) {
             x.fail = true;
         }
-        const uint32_t drow = smem_u32(x.stg) + static_cast<uint32_t>(box * QBOX + r * 128);
+        const uint32_t dbox = smem_u32(x.stg) + static_cast<uint32_t>(box * QBOX);
+        const uint32_t drow = dbox + static_cast<uint32_t>(r * 128);
+        // transposed output overwrites other threads' input rows: the group reads all of
+        // the quarter's input first
+        uint4 xall[8];
+        if (tma_trans) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) xall[j] = lds128(drow + static_cast<uint32_t>((j ^ (r & 7)) << 4));
+            named_barrier_sync(1 + x.grp, 128);
+        }
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
             // 16-byte chunk j of this 128-byte row sits at chunk j ^ (r % 8); the chunk's
@@ -429,7 +459,9 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
             uint4 xin[4];
             if (has_in) {
 #pragma unroll
-                for (int w = 0; w < 4; ++w) xin[w] = lds128(drow + static_cast<uint32_t>(((cc * 4 + w) ^ (r & 7)) << 4));
+                for (int w = 0; w < 4; ++w)
+                    xin[w] = tma_trans ? xall[cc * 4 + w]
+                                       : lds128(drow + static_cast<uint32_t>(((cc * 4 + w) ^ (r & 7)) << 4));
             }
             float v[32];
             tmem_ld_32x32b_x32(tbase + q * 64 + cc * 32, v);
@@ -452,8 +484,19 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
                 }
                 if (tma_direct)
                     sts128(drow + static_cast<uint32_t>(((cc * 4 + w) ^ (r & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+                if (tma_trans) {
+                    // element (r, y) of the quarter: out row y is line y of box r / 64 (128-byte
+                    // lines, 16-byte chunk k of line y at k ^ (y % 8)), out column r % 64
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int y = cc * 32 + 8 * w + e;
+                        sts16(dbox + static_cast<uint32_t>((r >> 6) * 8192 + y * 128 +
+                                                           ((((r & 63) >> 3) ^ (y & 7)) << 4) + (r & 7) * 2),
+                              half_of(o, e));
+                    }
+                }
                 const int c8 = cb + 8 * w;  // column of o[0]'s low half
-                if (OP == OP_XUPDATE_OUT && !tma_direct) {
+                if (OP == OP_XUPDATE_OUT && !tma_direct && !tma_trans) {
                     uint16_t* out = bk.out + static_cast<size_t>(c.mat) * bk.m * bk.n;
                     if (bk.tall) {
                         // X = Y^T: element (row0 + r, c8 + e) -> out row c8 + e, column row0 + r
@@ -484,6 +527,17 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
             if (x.leader) {
                 tma_store_3d(&bk.tm[P.map_out], x.stg + box * QBOX, col0 + 64 * q, row0, c.mat);
                 bulk_commit_group();
+            }
+            x.last_box = box;
+        } else if (tma_trans) {
+            if (x.leader) {
+                // out [g, m, n]: column coordinate (innermost) = Y row, row coordinate = Y
+                // column; boxes wholly in the padding are skipped, the rest clip at m and n
+                for (int h = 0; h < 2; ++h)
+                    if (row0 + 64 * h < bk.n && col0 + 64 * q < bk.m)
+                        tma_store_3d(&bk.tm[P.map_out], x.stg + box * QBOX + h * 8192, row0 + 64 * h, col0 + 64 * q,
+                                     c.mat);
+                bulk_commit_group();  // one group per quarter, as on the other paths
             }
             x.last_box = box;
         }
@@ -593,14 +647,25 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 const int nkb = w.nkb();
                 bool ok = true;
+#ifdef ANVIL_TIMELINE
+                unsigned long long tl_wait = 0;
+#endif
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t r = static_cast<uint32_t>(it / STAGES);
+#ifdef ANVIL_TIMELINE
+                    const unsigned long long tl_c0 = clock64();
+#endif
                     if (!mbar_wait(&empty_bar[s], (r & 1u) ^ 1u, p.err)) {
                         ok = false;
                         break;
                     }
+#ifdef ANVIL_TIMELINE
+                    tl_wait += clock64() - tl_c0;
+                    if (kb == nkb - 1 && rank == 0) TL_PUT(w.t(), TL_PROD_WAIT_CLK, tl_wait);
+#endif
                     if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * STAGE);
+                    if (kb == 0 && rank == 0) TL_PUT(w.t(), TL_PROD_FIRST, globaltimer_ns());
                     load_kblock(p, w, kb, rank, smem + s * STAGE, map_to_rank(&full_bar[s], 0));
                     issued = it + 1;
                 }
@@ -626,19 +691,35 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 const int ab = mt & 1;
                 const uint32_t u = static_cast<uint32_t>(mt >> 1);
                 ++mt;
+                TL_PUT(w.t(), TL_MMA_TAKEN, globaltimer_ns());
                 if (!mbar_wait(&tempty_bar[ab], (u & 1u) ^ 1u, p.err)) {
                     aborted = 1;
                     break;
                 }
+                TL_PUT(w.t(), TL_MMA_ACC_FREE, globaltimer_ns());
                 tc_fence_after();
                 const uint32_t dacc = tmem + static_cast<uint32_t>(ab * BN);
                 bool ok = true;
+#ifdef ANVIL_TIMELINE
+                unsigned long long tl_wait = 0;
+#endif
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = it % STAGES;
                     const uint32_t r = static_cast<uint32_t>(it / STAGES);
+#ifdef ANVIL_TIMELINE
+                    const unsigned long long tl_c0 = clock64();
+#endif
                     if (!mbar_wait(&full_bar[s], r & 1u, p.err)) {
                         ok = false;
                         break;
+                    }
+#ifdef ANVIL_TIMELINE
+                    if (kb > 0) tl_wait += clock64() - tl_c0;  // waits inside the k-loop only
+                    if (kb == nkb - 1) TL_PUT(w.t(), TL_MMA_WAIT_CLK, tl_wait);
+#endif
+                    if (kb == 0) {
+                        TL_PUT(w.t(), TL_MMA_FIRST, globaltimer_ns());
+                        TL_PUT(w.t(), TL_MMA_FIRST_CLK, clock64());
                     }
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(smem + s * STAGE);
@@ -657,6 +738,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                         umma_bf16_pair(dacc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
                     umma_commit_pair(&empty_bar[s], 3);  // frees stage s in both CTAs
+                    if (kb == nkb - 1) {
+                        TL_PUT(w.t(), TL_MMA_LAST, globaltimer_ns());
+                        TL_PUT(w.t(), TL_MMA_LAST_CLK, clock64());
+                    }
                 }
                 if (!ok) {
                     aborted = 1;
@@ -685,6 +770,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 const unsigned next = aborted ? static_cast<unsigned>(nitems) : atomicAdd(p.next_item, 1u);
                 int t = next >= static_cast<unsigned>(nitems) ? nitems : static_cast<int>(next);
                 Work w = make_work(p, item0, nitems, t);
+                if (t < nitems) {
+                    TL_PUT(t, TL_META, (static_cast<unsigned long long>(blockIdx.x >> 1)) |
+                                           (static_cast<unsigned long long>(w.w0.y) << 16) |
+                                           (static_cast<unsigned long long>(w.mat()) << 48));
+                    TL_PUT(t, TL_TILE, static_cast<unsigned long long>(w.bi()) |
+                                           (static_cast<unsigned long long>(w.bj()) << 16) |
+                                           (static_cast<unsigned long long>(w.nkb()) << 32));
+                    TL_PUT(t, TL_SCHED_TAKE, globaltimer_ns());
+                }
                 // the entry goes out once the phases the item reads are complete for its
                 // matrix, so no role of the pair waits on another pair after taking it
                 if (t < nitems && !deps_wait(p, work_item(w))) {
@@ -692,10 +786,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                     t = nitems;
                     w = make_work(p, item0, nitems, t);
                 }
+                if (t < nitems) TL_PUT(t, TL_SCHED_READY, globaltimer_ns());
                 if (!sched_push(sring, k, w, p.err)) {
                     aborted = 1;
                     break;
                 }
+                if (t < nitems) TL_PUT(t, TL_SCHED_PUSH, globaltimer_ns());
                 if (t >= nitems) break;
             }
         }
@@ -798,10 +894,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 const uint32_t u = static_cast<uint32_t>(mt >> 1);
                 ++mt;
                 if (!mbar_wait(&tfull_bar[ab], u & 1u, p.err)) x.fail = true;
+                if (x.leader && x.grp == 0 && rank == 0) TL_PUT(w.t(), TL_EPI_START, globaltimer_ns());
                 tc_fence_after();
                 tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(ab * BN);
                 tempty = ab ? tempty_leader1 : tempty_leader0;
             }
+            if (op == OP_NORMALIZE && x.leader && x.grp == 0 && rank == 0)
+                TL_PUT(w.t(), TL_EPI_START, globaltimer_ns());
             switch (op) {
                 case OP_GRAM: epi_tile<OP_GRAM>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
                 case OP_GRAM_NORM: epi_tile<OP_GRAM_NORM>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
@@ -815,6 +914,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                     named_barrier_sync(1 + x.grp, 128);
                     break;
             }
+            if (x.leader && x.grp == 0 && rank == 0) TL_PUT(w.t(), TL_EPI_END, globaltimer_ns());
             // publish the group's previous tile: its stores are older than this tile's two
             // (one per quarter), so they have long completed
             if (x.leader && pending) {
@@ -884,6 +984,24 @@ cudaError_t launch_cascade(const CascadeParams& p, cudaStream_t stream) {
     cfg.gridDim = dim3(2 * pairs, 1, 1);
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, cascade_kernel, p);
+}
+
+cudaError_t timeline_copy(void* host, size_t bytes, int clear) {
+#ifdef ANVIL_TIMELINE
+    void* dev = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&dev, g_timeline);
+    if (e) return e;
+    if (host && bytes) {
+        const size_t n = bytes < sizeof(g_timeline) ? bytes : sizeof(g_timeline);
+        if ((e = cudaMemcpy(host, dev, n, cudaMemcpyDeviceToHost))) return e;
+    }
+    return clear ? cudaMemset(dev, 0, sizeof(g_timeline)) : cudaSuccess;
+#else
+    (void)host;
+    (void)bytes;
+    (void)clear;
+    return cudaErrorNotSupported;
+#endif
 }
 
 cudaError_t gemm_prepare() {

@@ -108,7 +108,7 @@ enum MapSlot : int {
     TM_YN1 = 3,  // Y1, the same
     TM_A = 4,    // A [g][s_pad][s_pad], box {64, 128}
     TM_B = 5,    // B, the same
-    TM_OUT = 6,  // out [g][m][n], box {64, 128} (wide banks whose rows are 16-byte aligned)
+    TM_OUT = 6,  // out [g][m][n], box {64, 128} (wide) or {64, 64} (tall), rows 16-byte aligned
     TM_AN = 7,   // A, box {64, 64}: an upper block read as the transpose of a lower one
     TM_BN = 8,   // B, the same
     TM_COUNT = 9
@@ -126,7 +126,7 @@ struct CascadeBank {
     uint16_t* y1;       // normalised X (its output)
     const float* d;     // [g] normaliser of this bank's matrices
     int g, s_pad, L_pad, m, n, tall;
-    int out_tma;        // out is written through TM_OUT (wide bank, rows 16-byte aligned)
+    int out_tma;        // out is written through TM_OUT (rows 16-byte aligned; tall: transposed boxes)
     int T, ntl;         // s_pad / PAIR and L_pad / PAIR: row and column blocks of Y
     int mat_begin;      // first matrix of this bank among all matrices of the call
 };
@@ -183,6 +183,32 @@ constexpr unsigned SIGNALS_PER_TILE = 4;
 constexpr int SCHED_COUNTERS = MAX_PHASES + 1;
 cudaError_t launch_cascade(const CascadeParams& p, cudaStream_t stream);
 cudaError_t gemm_prepare();  // sets the cascade kernel's shared-memory limit on this device
+
+// Per-item timeline of the cascade kernel (a library built with -DANVIL_TIMELINE): the
+// 64-bit fields each item of the latest launches records.  timeline_copy copies up to
+// `bytes` to the host (if host != NULL), then zeroes the buffer if `clear`;
+// cudaErrorNotSupported in a library built without it.
+constexpr int TL_ITEMS = 16384;  // ANVIL_TIMELINE_ITEMS
+enum TimelineField : int {
+    TL_META = 0,          // pair | (op | bank << 8 | phase << 16) << 16 | matrix << 48
+    TL_TILE = 1,          // block row | block column << 16 | k-blocks << 32
+    TL_SCHED_TAKE = 2,    // scheduler took the item (ns)
+    TL_SCHED_READY = 3,   // its input phases were complete (ns)
+    TL_SCHED_PUSH = 4,    // its entry was in the ring (ns)
+    TL_PROD_FIRST = 5,    // producer armed its first k-block (ns)
+    TL_MMA_TAKEN = 6,     // MMA issuer read the entry (ns)
+    TL_MMA_ACC_FREE = 7,  // its accumulator was free (ns)
+    TL_MMA_FIRST = 8,     // first k-block landed, first MMA issued (ns)
+    TL_MMA_LAST = 9,      // last k-block's MMAs issued (ns)
+    TL_EPI_START = 10,    // epilogue found the accumulator complete (ns)
+    TL_EPI_END = 11,      // epilogue done with the tile (ns)
+    TL_MMA_FIRST_CLK = 12,
+    TL_MMA_LAST_CLK = 13,
+    TL_MMA_WAIT_CLK = 14,   // SM cycles the MMA issuer waited for k-blocks 1.. to land
+    TL_PROD_WAIT_CLK = 15,  // SM cycles the producer waited for free ring stages
+    TL_FIELDS = 16
+};
+cudaError_t timeline_copy(void* host, size_t bytes, int clear);
 
 // ---------------------------------------------------------------- tracing / self-test
 // dst [g, m, n] (natural layout) <- Y [g, s_pad, L_pad] (small-side-major), bf16.
