@@ -164,6 +164,7 @@ def report(res, cascade_ms, clocks_note):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--dump", default=None, help="also save the raw timelines (npz) to this path")
     args = ap.parse_args()
     sys.path.insert(0, ROOT)
     from polynomial_matrix_whitening_gb300 import build as B
@@ -191,7 +192,7 @@ def main():
     for _ in range(3):
         anvil.multi_bank_step(banks, ws)
     torch.cuda.synchronize()
-    results = []
+    results, raw = [], []
     for rep in range(args.reps):
         anvil.timeline_clear()
         with anvil.profile(max_records=16) as prof:
@@ -203,6 +204,10 @@ def main():
         casc = [ms for k, ms in prof.records if k == "cascade"]
         res = analyse(decode(tl, bank_of_index))
         results.append((res, casc[0] if casc else float("nan")))
+        raw.append(tl)
+    if args.dump:
+        np.savez_compressed(args.dump, timelines=np.stack(raw),
+                            bank_of_index=np.array([bank_of_index[q] for q in range(len(bank_of_index))]))
     # report the median launch by span
     results.sort(key=lambda r: r[0]["span"])
     res, ms = results[len(results) // 2]
