@@ -249,7 +249,7 @@ def oracle_sample(wl, per_bank, min_seconds=0.0):
     return total / est, secs, oracle.num_threads(), ", ".join(picks) + f" x {rounds} rounds"
 
 
-REFERENCE_BUDGET_S = 150.0   # CPU seconds the reference arm may spend on its warm-up and timed steps
+REFERENCE_BUDGET_S = 150.0   # default CPU seconds the reference arm may spend on its warm-up and timed steps
 
 
 def workload_config(world):
@@ -269,7 +269,8 @@ def run_reference(args, world, rank):
     """The CPU oracle on the bench's step: the same banks, grad pool (step s reads pool
     entry s mod 4) and running rails as the GPU arm.  Every step is the whole 66-matrix
     step when the warm-up and timed steps fit REFERENCE_BUDGET_S; otherwise each step takes
-    the same number of matrices from every bank (the step's own bank mix), as many as fit."""
+    the same number of matrices from every bank (the step's own bank mix), as many as fit.
+    (The budget is --reference-budget, default REFERENCE_BUDGET_S.)"""
     if rank != 0:
         return
     import oracle
@@ -287,8 +288,8 @@ def run_reference(args, world, rank):
         t_full += b.g * (time.perf_counter() - t0)
     g_full = min(b.g for b in wl.banks)
     nsteps = args.steps + args.warmup
-    per_bank = g_full if nsteps * t_full <= REFERENCE_BUDGET_S else \
-        max(1, int(g_full * REFERENCE_BUDGET_S / (nsteps * t_full)))
+    budget = args.reference_budget
+    per_bank = g_full if nsteps * t_full <= budget else max(1, int(g_full * budget / (nsteps * t_full)))
     vel = [np.zeros((2, per_bank, b.m, b.n), np.float32) for b in wl.banks]
 
     def step(s):
@@ -462,44 +463,75 @@ def run_anvil(args, world, rank, local):
     mom_ms = per_kind.get("momentum", [1, 0.0])[1] / prof_steps
 
     # ---- the page's update tail after the step (equaliser + sign-aligned decay update
-    # on a bf16 + mantissa master weight), timed alone on graph replays
-    tails, tail_ws = [], None
+    # on a bf16 + mantissa master weight), timed alone on graph replays: as a separate call
+    # on the step's outputs, and with the step-to-tail link (the step also writes the slow
+    # rail's sign bits, which the tail reads instead of the fp32 rail); the link's cost in
+    # the step is the momentum kernel's extra time in eager steps that write it
     gen = torch.Generator(device=dev).manual_seed(5)
-    for b in banks:
-        g_, m_, n_ = b.shape
-        nl = m_ if m_ >= n_ else n_
-        w0 = torch.randn((g_, m_, n_), device=dev, generator=gen) * 0.05
-        bits = w0.view(torch.int32)
-        tails.append(anvil.Tail(b.out, b.velocity,
-                                torch.zeros((g_, nl), dtype=torch.float32, device=dev),
-                                (bits >> 16).to(torch.int16).view(torch.bfloat16).contiguous(),
-                                (bits & 0xFFFF).to(torch.int16).contiguous(),
-                                torch.full((g_,), 0.02, dtype=torch.float32, device=dev), 0.1, 0.95))
-    tail_ws = torch.empty(anvil.tail_workspace_bytes([b.shape for b in banks]), dtype=torch.uint8,
-                          device=dev)
-    with torch.cuda.stream(stream):
-        anvil.update_tail(tails, tail_ws, stream=stream)
-        g_tail = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_tail, stream=stream):
+    elems = sum(b.shape[0] * b.shape[1] * b.shape[2] for b in banks)
+
+    def time_tail(links):
+        tails = []
+        for b, lk in zip(banks, links):
+            g_, m_, n_ = b.shape
+            nl = m_ if m_ >= n_ else n_
+            bits = (torch.randn((g_, m_, n_), device=dev, generator=gen) * 0.05).view(torch.int32)
+            tails.append(anvil.Tail(b.out, b.velocity, torch.zeros((g_, nl), dtype=torch.float32, device=dev),
+                                    (bits >> 16).to(torch.int16).view(torch.bfloat16).contiguous(),
+                                    (bits & 0xFFFF).to(torch.int16).contiguous(),
+                                    torch.full((g_,), 0.02, dtype=torch.float32, device=dev), 0.1, 0.95,
+                                    tail_link=lk))
+        tail_ws = torch.empty(anvil.tail_workspace_bytes([b.shape for b in banks]), dtype=torch.uint8, device=dev)
+        with torch.cuda.stream(stream):
             anvil.update_tail(tails, tail_ws, stream=stream)
-        for _ in range(nwarm):
-            g_tail.replay()
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    tail_reps = max(nsteps, 20)
+            g_tail = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_tail, stream=stream):
+                anvil.update_tail(tails, tail_ws, stream=stream)
+            for _ in range(nwarm):
+                g_tail.replay()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(nsteps, 20)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(reps):
+                g_tail.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / reps
+
+    def tail_entry(ms, bytes_per_elem, note):
+        tb = elems * bytes_per_elem
+        return {"ms_per_step": ms, "achieved": tb / (ms / 1000.0) / 1e9, "unit": "GB/s",
+                "frac": tb / (ms / 1000.0) / 1e9 / peaks["hbm_gbs"], "bytes_per_step": tb, "note": note}
+
+    # algorithmic bytes per element: lane powers read update 2; the apply reads update 2,
+    # param and mantissa 2 x 2 and the gate (the fp32 rail 4, or the link's sign words 0.25)
+    # and writes param and mantissa 2 x 2
+    update_tail = tail_entry(time_tail([None] * len(banks)), 16.0,
+                             "3 launches: lane powers (2 B/elem), lane scales, fused equalise + decay (14 B/elem)")
+    links = [anvil.alloc_tail_link(b.shape, device=dev) for b in banks]
+    for b, lk in zip(banks, links):
+        b.tail_link = lk
     with torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(tail_reps):
-            g_tail.replay()
-        t1.record(stream)
+        for s in range(2):
+            anvil.multi_bank_step(banks, ws, stream=stream)
+        torch.cuda.synchronize()
+        with anvil.profile(max_records=prof_steps * launches_per_step + 8) as prof_l:
+            for s in range(prof_steps):
+                for b, gt in zip(banks, pool_d[s % wl.pool]):
+                    b.grad = gt
+                anvil.multi_bank_step(banks, ws, stream=stream)
     torch.cuda.synchronize()
-    tail_ms = t0.elapsed_time(t1) / tail_reps
-    tail_bytes = sum(b.shape[0] * b.shape[1] * b.shape[2] for b in banks) * 16.0
-    update_tail = {"ms_per_step": tail_ms, "achieved": tail_bytes / (tail_ms / 1000.0) / 1e9,
-                   "unit": "GB/s", "frac": tail_bytes / (tail_ms / 1000.0) / 1e9 / peaks["hbm_gbs"],
-                   "bytes_per_step": tail_bytes,
-                   "note": "3 launches: lane powers (2 B/elem), lane scales, fused equalise + "
-                           "decay (14 B/elem)"}
+    mom_link = [t for k, t in prof_l.records if k == "momentum"]
+    update_tail_linked = tail_entry(time_tail(links), 12.25,
+                                    "3 launches: lane powers, lane scales, fused equalise + decay gated by the "
+                                    "slow-rail sign bits the step wrote into the tail link (10.25 B/elem)")
+    update_tail_linked["step_cost_ms"] = statistics.mean(mom_link) - mom_ms
+    update_tail_linked["step_cost_note"] = ("the momentum kernel's extra time per step for writing the "
+                                            "link's sign bits (eager steps, CUDA events)")
+    for b in banks:
+        b.tail_link = None
 
     # ---- the page's Adam step on an lm_head-sized fp32 parameter (768 x 50304)
     cnt = 768 * 50304
@@ -601,7 +633,8 @@ def run_anvil(args, world, rank, local):
             "gemm_phase_frac_of_peak": (alg / (gemm_ms / 1000.0) / 1e12) / tensor_peak,
             "momentum_frac_of_hbm": (work["momentum"] / (mom_ms / 1000.0) / 1e9) / peaks["hbm_gbs"],
             "profiled_ms_per_step": prof_ms_step,
-            "roofline": roofline, "kernels": kernels, "update_tail": update_tail, "adam": adam,
+            "roofline": roofline, "kernels": kernels, "update_tail": update_tail,
+            "update_tail_linked": update_tail_linked, "adam": adam,
             "e2e": {"value": mats * world / (e2e_ms / 1000.0), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": launches_per_step * nsteps,
@@ -639,6 +672,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["anvil", "reference"], default="anvil")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-budget", type=float, default=REFERENCE_BUDGET_S,
+                    help="CPU seconds the reference arm's warm-up and timed steps may take")
     ap.add_argument("--ncu-case", action="store_true")
     args = ap.parse_args()
     if args.ncu_case:

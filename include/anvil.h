@@ -66,9 +66,14 @@ typedef struct { float momentum, fast_beta, fast_weight, slow_beta; } anvil_scal
  *                          gradient is bf16); read only (never written)
  *   velocity  [2, g, m, n] fp32, read and written in place; rail 0 fast, rail 1 slow
  *   out       [g, m, n]    bf16 bits, written
+ *   tail_link  optional DEVICE buffer of anvil_tail_link_bytes(g, m, n) bytes, 256-byte
+ *              aligned, or NULL: the step also writes there the sign of every slow-rail
+ *              value (2 bits per element: the sign, and whether the tail must read the
+ *              value itself), so that anvil_update_tail given the same buffer gates its
+ *              decay without reading the fp32 slow rail (0.25 instead of 4 bytes per element)
  * grad must be aligned to its element size, velocity to 4 bytes, out to 2 bytes; out
- * must not overlap grad, velocity or any buffer of another bank in the same call.
- * `scalars` is used when the call's device scalar array is NULL. */
+ * and tail_link must not overlap grad, velocity or any buffer of another bank in the
+ * same call.  `scalars` is used when the call's device scalar array is NULL. */
 typedef struct {
     const void* grad;
     float* velocity;
@@ -76,7 +81,14 @@ typedef struct {
     int g, m, n;
     anvil_scalars scalars;
     int grad_bf16;
+    void* tail_link;
 } anvil_bank_desc;
+
+/* Bytes of the step-to-tail link buffer of one bank of g matrices of m x n (0 if the
+ * shape is invalid).  Its contents are internal to the library: written by the step
+ * (anvil_multi_bank_step, anvil_bank_step_traced), read by anvil_update_tail, valid
+ * until the bank's next step. */
+size_t anvil_tail_link_bytes(int g, int m, int n);
 
 #define ANVIL_MAX_MAPS 16     /* maps per call */
 #define ANVIL_MAX_BANKS 8     /* banks per anvil_multi_bank_step call */
@@ -169,6 +181,9 @@ anvil_status anvil_bank_step_noalloc(const float* grad, float* velocity, int g, 
  *   param       [g, m, n] bf16 bits of the parameter; read and written
  *   mantissa    [g, m, n] uint16, the low half of the fp32 master weight; read and written
  *   eff_lr      [g] fp32 per-matrix learning rate, read when the kernels run
+ *   tail_link   NULL, or the link buffer the step that produced `update` (its out) and
+ *               `velocity` was given: the tail then takes the slow rail's signs from it,
+ *               with the same results
  * Written buffers must not overlap any other buffer of the call. */
 typedef struct {
     const uint16_t* update;
@@ -179,14 +194,16 @@ typedef struct {
     const float* eff_lr;
     int g, m, n;
     float eff_wd, beta2;
+    const void* tail_link;
 } anvil_tail_desc;
 
 /* Bytes of device workspace anvil_update_tail needs (0 if the descriptors are invalid). */
 size_t anvil_tail_workspace_bytes(const anvil_tail_desc* banks, int nbanks);
 
 /* The update tail over nbanks banks (1 <= nbanks <= ANVIL_MAX_BANKS), three grouped
- * launches on the stream; workspace as for anvil_multi_bank_step (256-byte aligned,
- * caller-owned, contents on entry irrelevant).  Allocates nothing, never synchronises. */
+ * launches on the stream;
+ * workspace as for anvil_multi_bank_step (256-byte aligned, caller-owned, contents on
+ * entry irrelevant).  Allocates nothing, never synchronises. */
 anvil_status anvil_update_tail(const anvil_tail_desc* banks, int nbanks, void* workspace,
                                size_t workspace_bytes, void* stream);
 

@@ -57,7 +57,7 @@ class Scalars(ctypes.Structure):
 class BankDesc(ctypes.Structure):
     _fields_ = [("grad", ctypes.c_void_p), ("velocity", ctypes.c_void_p), ("out", ctypes.c_void_p),
                 ("g", ctypes.c_int), ("m", ctypes.c_int), ("n", ctypes.c_int),
-                ("scalars", Scalars), ("grad_bf16", ctypes.c_int)]
+                ("scalars", Scalars), ("grad_bf16", ctypes.c_int), ("tail_link", ctypes.c_void_p)]
 
 
 class Trace(ctypes.Structure):
@@ -70,7 +70,7 @@ class TailDesc(ctypes.Structure):
                 ("lane_energy", ctypes.c_void_p), ("param", ctypes.c_void_p),
                 ("mantissa", ctypes.c_void_p), ("eff_lr", ctypes.c_void_p),
                 ("g", ctypes.c_int), ("m", ctypes.c_int), ("n", ctypes.c_int),
-                ("eff_wd", ctypes.c_float), ("beta2", ctypes.c_float)]
+                ("eff_wd", ctypes.c_float), ("beta2", ctypes.c_float), ("tail_link", ctypes.c_void_p)]
 
 
 class ScheduleRun(ctypes.Structure):
@@ -98,6 +98,8 @@ _lib.anvil_bank_step_noalloc.restype = _i
 _lib.anvil_bank_step_traced.argtypes = [ctypes.POINTER(BankDesc), _vp, ctypes.POINTER(Map), _i,
                                         _f, _f, _vp, _sz, ctypes.POINTER(Trace), _vp]
 _lib.anvil_bank_step_traced.restype = _i
+_lib.anvil_tail_link_bytes.argtypes = [_i, _i, _i]
+_lib.anvil_tail_link_bytes.restype = _sz
 _lib.anvil_tail_workspace_bytes.argtypes = [ctypes.POINTER(TailDesc), _i]
 _lib.anvil_tail_workspace_bytes.restype = _sz
 _lib.anvil_update_tail.argtypes = [ctypes.POINTER(TailDesc), _i, _vp, _sz, _vp]
@@ -177,7 +179,32 @@ def _on_one_gpu(tensors, what):
     _require(all(t.is_contiguous() for t in tensors), f"{what}: every tensor must be contiguous")
 
 
-def _desc(grad, velocity, out, scalars=None):
+def _link_arg(link, g, m, n, ref):
+    """Device pointer of a tail-link buffer (uint8 tensor of tail_link_bytes, on ref's GPU)."""
+    if link is None:
+        return None
+    import torch
+    _require(link.dtype == torch.uint8 and link.dim() == 1, "tail_link must be a 1-D uint8 tensor")
+    _on_one_gpu((link, ref), "tail_link")
+    _require(link.numel() >= tail_link_bytes((g, m, n)), "tail_link smaller than tail_link_bytes")
+    _require(link.data_ptr() % 256 == 0, "tail_link not 256-byte aligned")
+    return link.data_ptr()
+
+
+def tail_link_bytes(shape):
+    """Bytes of the step-to-tail link buffer of one bank of this (g, m, n) shape."""
+    return int(_lib.anvil_tail_link_bytes(*[int(x) for x in shape]))
+
+
+def alloc_tail_link(shape, device=None):
+    """A step-to-tail link buffer for one bank (uint8 tensor, 256-byte aligned)."""
+    import torch
+    t = torch.empty(tail_link_bytes(shape), dtype=torch.uint8, device=device or "cuda")
+    _require(t.data_ptr() % 256 == 0, "tail_link not 256-byte aligned")
+    return t
+
+
+def _desc(grad, velocity, out, scalars=None, tail_link=None):
     import torch
     _require(grad.dtype in (torch.float32, torch.bfloat16), "grad must be fp32 or bf16")
     _require(velocity.dtype == torch.float32, "velocity must be fp32")
@@ -191,11 +218,11 @@ def _desc(grad, velocity, out, scalars=None):
     return BankDesc(grad.data_ptr(), velocity.data_ptr(), out.data_ptr(), g, m, n,
                     Scalars(float(s.get("momentum", 0.95)), float(s.get("fast_beta", 0.85)),
                             float(s.get("fast_weight", 0.4385)), float(s.get("slow_beta", 0.98))),
-                    1 if grad.dtype == torch.bfloat16 else 0)
+                    1 if grad.dtype == torch.bfloat16 else 0, _link_arg(tail_link, g, m, n, grad))
 
 
 def _raw_desc(g, m, n, grad=0, velocity=0, out=0, grad_bf16=0):
-    return BankDesc(grad, velocity, out, g, m, n, Scalars(0.95, 0.85, 0.4385, 0.98), grad_bf16)
+    return BankDesc(grad, velocity, out, g, m, n, Scalars(0.95, 0.85, 0.4385, 0.98), grad_bf16, None)
 
 
 def workspace_bytes(shapes):
@@ -222,20 +249,22 @@ def _workspace_arg(workspace, ref):
 
 
 class Bank:
-    """One bank of a multi-bank step: grad, velocity, out tensors and host scalars."""
+    """One bank of a multi-bank step: grad, velocity, out tensors and host scalars, and an
+    optional step-to-tail link buffer (alloc_tail_link) for the update tail of this step."""
 
     def __init__(self, grad, velocity, out, momentum=0.95, fast_beta=0.85, fast_weight=0.4385,
-                 slow_beta=0.98):
+                 slow_beta=0.98, tail_link=None):
         self.grad, self.velocity, self.out = grad, velocity, out
         self.scalars = dict(momentum=momentum, fast_beta=fast_beta, fast_weight=fast_weight,
                             slow_beta=slow_beta)
+        self.tail_link = tail_link
 
     @property
     def shape(self):
         return tuple(self.grad.shape)
 
     def desc(self):
-        return _desc(self.grad, self.velocity, self.out, self.scalars)
+        return _desc(self.grad, self.velocity, self.out, self.scalars, self.tail_link)
 
 
 def multi_bank_step(banks, workspace, maps=None, margin=1.05, eps=1e-6, d_scalars=None,
@@ -317,12 +346,15 @@ def bank_step_traced(bank: Bank, workspace, maps=None, margin=1.05, eps=1e-6, st
 class Tail:
     """One bank of the update tail: the step's out as update, its velocity (rail 1 gates the
     decay), lane_energy [g, m] if m >= n else [g, n] fp32, param (bf16) and mantissa
-    (uint16 as torch.int16) [g, m, n], eff_lr [g] fp32, and host eff_wd, beta2."""
+    (uint16 as torch.int16) [g, m, n], eff_lr [g] fp32, and host eff_wd, beta2; tail_link:
+    the link buffer the step that produced update and velocity was given, or None."""
 
-    def __init__(self, update, velocity, lane_energy, param, mantissa, eff_lr, eff_wd, beta2):
+    def __init__(self, update, velocity, lane_energy, param, mantissa, eff_lr, eff_wd, beta2,
+                 tail_link=None):
         self.update, self.velocity, self.lane_energy = update, velocity, lane_energy
         self.param, self.mantissa, self.eff_lr = param, mantissa, eff_lr
         self.eff_wd, self.beta2 = float(eff_wd), float(beta2)
+        self.tail_link = tail_link
 
     def desc(self):
         import torch
@@ -341,11 +373,11 @@ class Tail:
         _on_one_gpu((self.update, self.velocity, self.lane_energy, self.param, self.mantissa, self.eff_lr), "tail")
         return TailDesc(self.update.data_ptr(), self.velocity.data_ptr(), self.lane_energy.data_ptr(),
                         self.param.data_ptr(), self.mantissa.data_ptr(), self.eff_lr.data_ptr(),
-                        g, m, n, self.eff_wd, self.beta2)
+                        g, m, n, self.eff_wd, self.beta2, _link_arg(self.tail_link, g, m, n, self.update))
 
 
 def tail_workspace_bytes(shapes):
-    descs = (TailDesc * len(shapes))(*[TailDesc(0, 0, 0, 0, 0, 0, g, m, n, 0.0, 0.0)
+    descs = (TailDesc * len(shapes))(*[TailDesc(0, 0, 0, 0, 0, 0, g, m, n, 0.0, 0.0, None)
                                        for g, m, n in shapes])
     return int(_lib.anvil_tail_workspace_bytes(descs, len(shapes)))
 

@@ -213,24 +213,26 @@ struct Range {
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
 anvil_status check_banks(const anvil_bank_desc* banks, int nbanks) {
-    Range rg[ANVIL_MAX_BANKS][3];
+    Range rg[ANVIL_MAX_BANKS][4];
     for (int i = 0; i < nbanks; ++i) {
         const anvil_bank_desc& b = banks[i];
         if (!b.grad || !b.velocity || !b.out) return ANVIL_ERR_INVALID_ARG;
         const uintptr_t gsz = b.grad_bf16 ? 2 : 4;
         if ((reinterpret_cast<uintptr_t>(b.grad) & (gsz - 1)) || (reinterpret_cast<uintptr_t>(b.velocity) & 3) ||
-            (reinterpret_cast<uintptr_t>(b.out) & 1))
+            (reinterpret_cast<uintptr_t>(b.out) & 1) || (reinterpret_cast<uintptr_t>(b.tail_link) & 255))
             return ANVIL_ERR_ALIGNMENT;
         const size_t cnt = static_cast<size_t>(b.g) * b.m * b.n;
         rg[i][0] = {reinterpret_cast<uintptr_t>(b.grad), reinterpret_cast<uintptr_t>(b.grad) + gsz * cnt};
         rg[i][1] = {reinterpret_cast<uintptr_t>(b.velocity), reinterpret_cast<uintptr_t>(b.velocity + 2 * cnt)};
         rg[i][2] = {reinterpret_cast<uintptr_t>(b.out), reinterpret_cast<uintptr_t>(b.out + cnt)};
+        const uintptr_t lk = reinterpret_cast<uintptr_t>(b.tail_link);
+        rg[i][3] = {lk, lk ? lk + link_layout(b.g, b.m, b.n).total : lk};
     }
-    // written buffers (velocity, out) must overlap nothing else of the call
+    // written buffers (velocity, out, tail_link) must overlap nothing else of the call
     for (int i = 0; i < nbanks; ++i)
-        for (int w = 1; w <= 2; ++w)
+        for (int w = 1; w <= 3; ++w)
             for (int j = 0; j < nbanks; ++j)
-                for (int k = 0; k < 3; ++k) {
+                for (int k = 0; k < 4; ++k) {
                     if (i == j && k == w) continue;
                     if (overlap(rg[i][w], rg[j][k])) return ANVIL_ERR_ALIAS;
                 }
@@ -291,10 +293,12 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         for (int i = 0; i < nbanks; ++i) {
             const size_t cnt = static_cast<size_t>(banks[i].g) * banks[i].m * banks[i].n;
             const uintptr_t gsz = banks[i].grad_bf16 ? 2 : 4;
-            const Range r[3] = {{reinterpret_cast<uintptr_t>(banks[i].grad), reinterpret_cast<uintptr_t>(banks[i].grad) + gsz * cnt},
+            const uintptr_t lk = reinterpret_cast<uintptr_t>(banks[i].tail_link);
+            const Range r[4] = {{reinterpret_cast<uintptr_t>(banks[i].grad), reinterpret_cast<uintptr_t>(banks[i].grad) + gsz * cnt},
                                 {reinterpret_cast<uintptr_t>(banks[i].velocity), reinterpret_cast<uintptr_t>(banks[i].velocity + 2 * cnt)},
-                                {reinterpret_cast<uintptr_t>(banks[i].out), reinterpret_cast<uintptr_t>(banks[i].out + cnt)}};
-            for (int k = 0; k < 3; ++k)
+                                {reinterpret_cast<uintptr_t>(banks[i].out), reinterpret_cast<uintptr_t>(banks[i].out + cnt)},
+                                {lk, lk ? lk + link_layout(banks[i].g, banks[i].m, banks[i].n).total : lk}};
+            for (int k = 0; k < 4; ++k)
                 if (overlap(wr, r[k])) return ANVIL_ERR_ALIAS;
         }
     }
@@ -362,6 +366,11 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
             M.grad_bf16 = b.grad_bf16 ? 1 : 0;
             M.vec4 = (G.n % 4 == 0) && !(reinterpret_cast<uintptr_t>(b.grad) & (b.grad_bf16 ? 7 : 15)) &&
                      !(reinterpret_cast<uintptr_t>(b.velocity) & 15);
+            if (b.tail_link) {
+                const LinkLayout lk = link_layout(G.g, G.m, G.n);
+                M.gate = static_cast<uint64_t*>(b.tail_link);
+                M.nck = lk.nck;
+            }
             M.momentum = b.scalars.momentum;
             M.fast_beta = b.scalars.fast_beta;
             M.fast_weight = b.scalars.fast_weight;
@@ -529,14 +538,15 @@ anvil_status make_tail_layout(const anvil_tail_desc* banks, int nbanks, TailLayo
 }
 
 anvil_status check_tail(const anvil_tail_desc* banks, int nbanks) {
-    Range rg[ANVIL_MAX_BANKS][6];
+    Range rg[ANVIL_MAX_BANKS][7];
     for (int i = 0; i < nbanks; ++i) {
         const anvil_tail_desc& b = banks[i];
         if (!b.update || !b.velocity || !b.lane_energy || !b.param || !b.mantissa || !b.eff_lr)
             return ANVIL_ERR_INVALID_ARG;
         if ((reinterpret_cast<uintptr_t>(b.update) & 1) || (reinterpret_cast<uintptr_t>(b.param) & 1) ||
             (reinterpret_cast<uintptr_t>(b.mantissa) & 1) || (reinterpret_cast<uintptr_t>(b.velocity) & 3) ||
-            (reinterpret_cast<uintptr_t>(b.lane_energy) & 3) || (reinterpret_cast<uintptr_t>(b.eff_lr) & 3))
+            (reinterpret_cast<uintptr_t>(b.lane_energy) & 3) || (reinterpret_cast<uintptr_t>(b.eff_lr) & 3) ||
+            (reinterpret_cast<uintptr_t>(b.tail_link) & 255))
             return ANVIL_ERR_ALIGNMENT;
         const size_t cnt = static_cast<size_t>(b.g) * b.m * b.n;
         const size_t nl = static_cast<size_t>(b.g) * (b.m >= b.n ? b.m : b.n);
@@ -546,12 +556,14 @@ anvil_status check_tail(const anvil_tail_desc* banks, int nbanks) {
         rg[i][3] = {reinterpret_cast<uintptr_t>(b.update), reinterpret_cast<uintptr_t>(b.update + cnt)};
         rg[i][4] = {reinterpret_cast<uintptr_t>(b.velocity), reinterpret_cast<uintptr_t>(b.velocity + 2 * cnt)};
         rg[i][5] = {reinterpret_cast<uintptr_t>(b.eff_lr), reinterpret_cast<uintptr_t>(b.eff_lr + b.g)};
+        const uintptr_t lk = reinterpret_cast<uintptr_t>(b.tail_link);
+        rg[i][6] = {lk, lk ? lk + link_layout(b.g, b.m, b.n).total : lk};
     }
     // written buffers (lane_energy, param, mantissa) overlap nothing else of the call
     for (int i = 0; i < nbanks; ++i)
         for (int w = 0; w < 3; ++w)
             for (int j = 0; j < nbanks; ++j)
-                for (int k = 0; k < 6; ++k) {
+                for (int k = 0; k < 7; ++k) {
                     if (i == j && k == w) continue;
                     if (overlap(rg[i][w], rg[j][k])) return ANVIL_ERR_ALIAS;
                 }
@@ -600,6 +612,11 @@ anvil_status anvil_multi_bank_step(const anvil_bank_desc* banks, int nbanks,
                     workspace_bytes, static_cast<cudaStream_t>(stream), nullptr);
 }
 
+size_t anvil_tail_link_bytes(int g, int m, int n) {
+    if (g < 1 || m < 1 || n < 1 || g > ANVIL_MAX_BATCH || m > ANVIL_MAX_DIM || n > ANVIL_MAX_DIM) return 0;
+    return link_layout(g, m, n).total;
+}
+
 size_t anvil_tail_workspace_bytes(const anvil_tail_desc* banks, int nbanks) {
     TailLayout T;
     if (make_tail_layout(banks, nbanks, &T) != ANVIL_OK) return 0;
@@ -622,11 +639,13 @@ anvil_status anvil_update_tail(const anvil_tail_desc* banks, int nbanks, void* w
     memset(&tp, 0, sizeof(tp));
     tp.nbanks = nbanks;
     tp.total_mats = T.total_mats;
-    long long chunks = 0;
+    long long chunks = 0, rows = 0;
     int mats = 0;
     for (int i = 0; i < nbanks; ++i) {
         const anvil_tail_desc& b = banks[i];
         TailBank& B = tp.bank[i];
+        B.row_begin = rows;
+        rows += static_cast<long long>(b.g) * b.m;
         B.update = b.update;
         B.velocity = b.velocity;
         B.lane_energy = b.lane_energy;
@@ -645,10 +664,15 @@ anvil_status anvil_update_tail(const anvil_tail_desc* banks, int nbanks, void* w
                  !(reinterpret_cast<uintptr_t>(b.velocity) & 15);
         B.power = reinterpret_cast<float*>(ws + T.off_power) + T.lane_off[i];
         B.scale = reinterpret_cast<float*>(ws + T.off_scale) + T.lane_off[i];
+        if (b.tail_link) {  // the step's slow-rail sign words
+            B.sign = static_cast<const uint64_t*>(b.tail_link);
+            B.nck = link_layout(b.g, b.m, b.n).nck;
+        }
         mats += b.g;
         chunks += static_cast<long long>(b.g) * b.m * ((b.n + 7) / 8);
     }
     tp.total_chunks = chunks;
+    tp.total_rows = rows;
     cudaError_t e;
     if ((e = profiled(ANVIL_KERNEL_TAIL_POWER, s, [&] { return launch_tail_power(tp, s); })))
         return cuda_fail(e, "tail lane-power launch");
@@ -721,6 +745,7 @@ anvil_status anvil_bank_step(const float* grad, float* velocity, int g, int m, i
     b.scalars.fast_weight = fast_weight;
     b.scalars.slow_beta = slow_beta;
     b.grad_bf16 = 0;
+    b.tail_link = nullptr;
     if (!maps) {
         maps = kAnvilMaps;
         nmaps = 6;
@@ -894,6 +919,7 @@ anvil_status anvil_bank_step_noalloc(const float* grad, float* velocity, int g, 
     b.scalars.fast_weight = fast_weight;
     b.scalars.slow_beta = slow_beta;
     b.grad_bf16 = 0;
+    b.tail_link = nullptr;
     if (!maps) {
         maps = kAnvilMaps;
         nmaps = 6;

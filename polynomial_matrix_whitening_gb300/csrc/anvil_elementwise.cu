@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
     for (int k = 0; k < 4; ++k) {
         const int r = r0 + ty + 16 * k;
         float x[4] = {0.f, 0.f, 0.f, 0.f};
+        // tail link: the new slow rail's sign, and whether the tail must read the value
+        bool sgn[4] = {false, false, false, false}, exq[4] = {true, true, true, true};
         if (r < m) {
             const size_t base = static_cast<size_t>(r) * n + c;
             float g[4] = {0.f, 0.f, 0.f, 0.f}, v0[4] = {0.f, 0.f, 0.f, 0.f}, v1[4] = {0.f, 0.f, 0.f, 0.f};
@@ -109,6 +111,8 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
                 const float blend = __fadd_rn(__fmul_rn(fw, a), __fmul_rn(omw, b));
                 const float y = __fadd_rn(g[q], __fmul_rn(mom, __fsub_rn(blend, g[q])));
                 x[q] = in[q] ? round_bf(y) : 0.f;
+                sgn[q] = in[q] && signbit(b);
+                exq[q] = !in[q] || !(fabsf(b) >= 0x1p-100f && fabsf(b) <= 3.402823466e38f);
             }
             if (B.vec4) {
                 if (in[0]) {
@@ -122,6 +126,24 @@ __global__ void __launch_bounds__(256) momentum_kernel(const __grid_constant__ M
                         V0[base + q] = v0[q];
                         V1[base + q] = v1[q];
                     }
+            }
+        }
+        if (B.gate) {
+            // sign and exact-read bits of the warp's two rows (lanes 0-15: row of the even
+            // ty, 16-31: the odd one): bit 16 q + tx of a row's word is column c0 + 4 tx + q
+            const int half = threadIdx.x & 16;
+            uint64_t sw = 0, xw = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const unsigned bs = __ballot_sync(0xffffffffu, sgn[q]);
+                const unsigned bx = __ballot_sync(0xffffffffu, exq[q]);
+                sw |= static_cast<uint64_t>((bs >> half) & 0xffffu) << (16 * q);
+                xw |= static_cast<uint64_t>((bx >> half) & 0xffffu) << (16 * q);
+            }
+            if (tx == 0 && r < m && c0 < n) {
+                // [g, nck, m, 2]: a tile's 64 rows of one column chunk are 1 KB contiguous
+                uint64_t* gw = B.gate + ((static_cast<size_t>(mat) * B.nck + tc) * m + r) * 2;
+                *reinterpret_cast<ulonglong2*>(gw) = make_ulonglong2(sw, xw);
             }
         }
         if (!B.tall) {

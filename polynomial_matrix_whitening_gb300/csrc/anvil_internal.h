@@ -47,6 +47,22 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 
+// The step-to-tail link buffer of one bank (anvil_tail_link_bytes): the slow rail's sign
+// words, uint64 [g, nck, m, 2] for 64-column chunk k, out row r: word 0 bit 16 q + t is
+// the sign of the slow rail at column 64 k + 4 t + q (t < 16, q < 4), word 1's same bit
+// says that the value is zero, below 2^-100 in magnitude, infinite or NaN (the tail then
+// reads the fp32 rail itself).
+struct LinkLayout {
+    int nck;
+    size_t total;
+};
+inline LinkLayout link_layout(int g, int m, int n) {
+    LinkLayout k;
+    k.nck = (n + 63) / 64;
+    k.total = (16 * static_cast<size_t>(g) * m * k.nck + 255) & ~static_cast<size_t>(255);
+    return k;
+}
+
 // Bits of the device error word (set with atomicOr, read by anvil_device_error).
 enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_BOUNDS = 2u };
 
@@ -58,6 +74,8 @@ struct MomentumBank {
     float* part;         // [g, nlb, s_pad]: sums of squares of the bf16 values per 64-block
     int g, m, n, tall, s_pad, L_pad, nlb;
     int tiles_r, tiles_c;  // 64x64 tiles over the padded natural extent [rows, cols]
+    uint64_t* gate;        // tail link: slow-rail sign words [g, nck, m, 2] (NULL: none)
+    int nck;               // 64-column chunks per row, (n + 63) / 64
     int tile_begin;        // first tile of this bank in the grouped grid
     int vec4;              // n % 4 == 0 and aligned grad/velocity: 4-element vector path
     int grad_bf16;

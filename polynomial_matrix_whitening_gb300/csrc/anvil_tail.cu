@@ -306,6 +306,154 @@ __global__ void __launch_bounds__(256) tail_apply_kernel(const __grid_constant__
     }
 }
 
+// tail_element with the gate already decided (the tail link's path).
+__device__ __forceinline__ void tail_element_gated(float v, float scale, bool aligned_, float wd, float lr,
+                                                   uint16_t& p, uint16_t& mt) {
+    const float u = round_bf(__fmul_rn(v, scale));
+    float w = __uint_as_float((static_cast<uint32_t>(p) << 16) | mt);
+    const float aligned = aligned_ ? 1.f : 0.f;
+    const float decay = __fmul_rn(__fmul_rn(__fmul_rn(w, aligned), wd), lr);
+    w = __fsub_rn(__fsub_rn(w, decay), __fmul_rn(u, lr));
+    const uint32_t bits = __float_as_uint(w);
+    p = static_cast<uint16_t>(bits >> 16);
+    mt = static_cast<uint16_t>(bits & 0xffffu);
+}
+
+// With the tail link: the decay gate [slow rail * w >= 0] of an element follows from the
+// sign bits (the product of two numbers of magnitude at least 2^-100 and 2^-40 is not zero
+// and has the sign of their signs) unless the link flags the rail value (zero, below
+// 2^-100, not finite) or w is outside [2^-40, FLT_MAX] (its exponent field outside
+// [87, 254]): then the fp32 rail is read.  Bit k of the result: element k is aligned.
+// The 8 bits of columns 4 t .. 4 t + 7 of a link word (bit 16 q + t is column 4 t + q), in
+// column order: the bits at 0, 16, 32, 48 of (w >> t) gathered by one multiply.
+__device__ __forceinline__ unsigned link_bits8(uint64_t w, int t) {
+    const uint64_t lo = (w >> t) & 0x0001000100010001ull, hi = (w >> (t + 1)) & 0x0001000100010001ull;
+    constexpr uint64_t M = (1ull << 48) | (1ull << 33) | (1ull << 18) | (1ull << 3);
+    return static_cast<unsigned>(((lo * M) >> 48) & 0xfu) | (static_cast<unsigned>(((hi * M) >> 48) & 0xfu) << 4);
+}
+
+__device__ __forceinline__ unsigned link_gates(ulonglong2 sx, int c0, const float* rail, const uint32_t (&pw)[4],
+                                               const uint32_t (&mw)[4]) {
+    const int t = (c0 & 63) >> 2;  // the chunk's columns 4 t .. 4 t + 7 of its 64
+    const unsigned g8 = link_bits8(sx.x, t);
+    bool need_rail = link_bits8(sx.y, t) != 0u;
+    // w's sign bits (bit 15 and 31 of each param word hold elements 2q and 2q + 1)
+    const unsigned w8 = ((pw[0] >> 15) & 1u) | ((pw[0] >> 30) & 2u) | ((pw[1] >> 13) & 4u) | ((pw[1] >> 28) & 8u) |
+                        ((pw[2] >> 11) & 16u) | ((pw[2] >> 26) & 32u) | ((pw[3] >> 9) & 64u) | ((pw[3] >> 24) & 128u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const unsigned e2 = (pw[q] >> 7) & 0x00ff00ffu;  // both halves' exponent fields
+        need_rail |= __vcmpgtu2(__vsub2(e2, 0x00570057u), 0x00a700a7u) != 0u;
+    }
+    if (!need_rail) return ~(g8 ^ w8) & 0xffu;
+    const float4 r0 = __ldcs(reinterpret_cast<const float4*>(rail));
+    const float4 r1 = __ldcs(reinterpret_cast<const float4*>(rail + 4));
+    const float rv[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    unsigned gk = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int q = k >> 1, hi = k & 1;
+        const float w = __uint_as_float((hi ? (pw[q] & 0xffff0000u) : (pw[q] << 16)) | (hi ? (mw[q] >> 16) : (mw[q] & 0xffffu)));
+        gk |= (__fmul_rn(rv[k], w) >= 0.f ? 1u : 0u) << k;
+    }
+    return gk;
+}
+
+// With every bank's link: one warp per row at a time (grid-stride over the call's rows),
+// lane l taking the 8-element chunks l, l + 32, ... of the row, ROW_CHUNKS of them loaded
+// before any is computed.  The row's matrix, learning rate and
+// (rows as lanes) scale are found once per row.
+constexpr int ROW_CHUNKS = 2;
+__global__ void __launch_bounds__(256, 4) tail_apply_rows_kernel(const __grid_constant__ TailParams p) {
+    pdl_allow_next();
+    pdl_wait_previous();
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    for (long long rw = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); rw < p.total_rows;
+         rw += nwarps) {
+        int bi = 0;
+#pragma unroll 1
+        for (int i = 1; i < p.nbanks; ++i)
+            if (rw >= p.bank[i].row_begin) bi = i;
+        const TailBank& B = p.bank[bi];
+        const long long lrow = rw - B.row_begin;
+        const int mat = static_cast<int>(lrow / B.m), row = static_cast<int>(lrow - static_cast<long long>(mat) * B.m);
+        const size_t rbase = (static_cast<size_t>(mat) * B.m + row) * B.n;
+        const float lr = B.eff_lr[mat];
+        const bool rows_lanes = B.m >= B.n;
+        const float* S = B.scale + static_cast<size_t>(mat) * (rows_lanes ? B.m : B.n);
+        const float srow = rows_lanes ? S[row] : 0.f;
+        const float* rail = B.velocity + static_cast<size_t>(B.g) * B.m * B.n + rbase;
+        // the row's sign words of 64-column chunk k: sgn + 2 m k ([g, nck, m, 2])
+        const uint64_t* sgn = B.sign + (static_cast<size_t>(mat) * B.nck * B.m + row) * 2;
+        const size_t kstride = 2 * static_cast<size_t>(B.m);
+        const int nch = (B.n + 7) / 8;
+        for (int cb = lane; cb < nch; cb += 32 * ROW_CHUNKS) {
+            uint4 vu[ROW_CHUNKS], pu[ROW_CHUNKS], mu[ROW_CHUNKS];
+            ulonglong2 sx[ROW_CHUNKS];
+#pragma unroll
+            for (int u = 0; u < ROW_CHUNKS; ++u) {
+                const int ci = cb + 32 * u;
+                if (B.vec8 && ci < nch) {
+                    vu[u] = *reinterpret_cast<const uint4*>(B.update + rbase + 8 * ci);
+                    pu[u] = *reinterpret_cast<const uint4*>(B.param + rbase + 8 * ci);
+                    mu[u] = *reinterpret_cast<const uint4*>(B.mantissa + rbase + 8 * ci);
+                    sx[u] = __ldg(reinterpret_cast<const ulonglong2*>(sgn + kstride * (ci >> 3)));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < ROW_CHUNKS; ++u) {
+                const int ci = cb + 32 * u, c0 = 8 * ci;
+                if (ci >= nch) break;
+                if (B.vec8) {
+                    uint32_t pw[4] = {pu[u].x, pu[u].y, pu[u].z, pu[u].w};
+                    uint32_t mw[4] = {mu[u].x, mu[u].y, mu[u].z, mu[u].w};
+                    const uint32_t vw[4] = {vu[u].x, vu[u].y, vu[u].z, vu[u].w};
+                    const unsigned gk = link_gates(sx[u], c0, rail + c0, pw, mw);
+                    float sc[8];
+                    if (rows_lanes) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) sc[k] = srow;
+                    } else {
+                        const float4 s0 = *reinterpret_cast<const float4*>(S + c0);
+                        const float4 s1 = *reinterpret_cast<const float4*>(S + c0 + 4);
+                        sc[0] = s0.x; sc[1] = s0.y; sc[2] = s0.z; sc[3] = s0.w;
+                        sc[4] = s1.x; sc[5] = s1.y; sc[6] = s1.z; sc[7] = s1.w;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int q = k >> 1, hi = k & 1;
+                        const float v = bf2f(static_cast<uint16_t>(hi ? vw[q] >> 16 : vw[q] & 0xffffu));
+                        uint16_t pp = static_cast<uint16_t>(hi ? pw[q] >> 16 : pw[q] & 0xffffu);
+                        uint16_t mm = static_cast<uint16_t>(hi ? mw[q] >> 16 : mw[q] & 0xffffu);
+                        tail_element_gated(v, sc[k], (gk >> k) & 1u, B.eff_wd, lr, pp, mm);
+                        pw[q] = hi ? ((pw[q] & 0xffffu) | (static_cast<uint32_t>(pp) << 16)) : ((pw[q] & 0xffff0000u) | pp);
+                        mw[q] = hi ? ((mw[q] & 0xffffu) | (static_cast<uint32_t>(mm) << 16)) : ((mw[q] & 0xffff0000u) | mm);
+                    }
+                    *reinterpret_cast<uint4*>(B.param + rbase + c0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+                    *reinterpret_cast<uint4*>(B.mantissa + rbase + c0) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+                } else {
+                    // unaligned or n % 8 != 0: element by element, the rail where the bits do not decide
+                    const unsigned sw = link_bits8(sgn[kstride * (ci >> 3)], (c0 & 63) >> 2);
+                    const unsigned xw = link_bits8(sgn[kstride * (ci >> 3) + 1], (c0 & 63) >> 2);
+                    for (int k = 0; k < 8 && c0 + k < B.n; ++k) {
+                        uint16_t pp = B.param[rbase + c0 + k], mm = B.mantissa[rbase + c0 + k];
+                        const uint32_t wb = (static_cast<uint32_t>(pp) << 16) | mm;
+                        const int bit = k;
+                        const bool ok = (!((xw >> bit) & 1u) && (((wb >> 23) & 0xffu) - 87u) <= 167u)
+                                            ? (((sw >> bit) ^ (wb >> 31)) & 1u) == 0u
+                                            : __fmul_rn(rail[c0 + k], __uint_as_float(wb)) >= 0.f;
+                        tail_element_gated(bf2f(B.update[rbase + c0 + k]), rows_lanes ? srow : S[c0 + k], ok, B.eff_wd,
+                                           lr, pp, mm);
+                        B.param[rbase + c0 + k] = pp;
+                        B.mantissa[rbase + c0 + k] = mm;
+                    }
+                }
+            }
+        }
+    }
+}
+
 cudaError_t launch_tail_power(const TailParams& p, cudaStream_t stream) {
     TailParams q = p;
     long long blocks = 0;
@@ -322,26 +470,29 @@ cudaError_t launch_tail_scale(const TailParams& p, cudaStream_t stream) {
     return launch_pdl(lane_scale_kernel, dim3(p.total_mats), dim3(SCALE_THREADS), 0, stream, p);
 }
 
-// Blocks of tail_apply_kernel that are resident at once on this device (cached per
-// device): the grid-stride loop covers the elements in one wave of resident blocks, so no
-// partial second wave trails the first.
-static int g_apply_blocks[64];
+// Blocks of each apply kernel that are resident at once on this device (cached per device):
+// the grid-stride loops cover the work in one wave of resident blocks, so no partial second
+// wave trails the first.
+static int g_apply_blocks[2][64];
 
 cudaError_t launch_tail_apply(const TailParams& p, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e) return e;
-    int& resident = g_apply_blocks[dev & 63];
+    bool link = true;  // the row kernel, with the link's sign words, when every bank has them
+    for (int i = 0; i < p.nbanks; ++i) link = link && p.bank[i].sign != nullptr;
+    void (*kernel)(TailParams) = link ? tail_apply_rows_kernel : tail_apply_kernel;
+    int& resident = g_apply_blocks[link ? 1 : 0][dev & 63];
     if (resident == 0) {
         int per_sm = 0, sms = 0;
-        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tail_apply_kernel, 256, 0))) return e;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0))) return e;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
         resident = per_sm > 0 && sms > 0 ? per_sm * sms : 152;
     }
-    long long blocks = (p.total_chunks + 255) / 256;
-    if (blocks > resident) blocks = resident;
+    const long long work = link ? (p.total_rows + 7) / 8 : (p.total_chunks + 255) / 256;  // blocks to cover it
+    long long blocks = work < resident ? work : resident;
     if (blocks < 1) blocks = 1;
-    return launch_pdl(tail_apply_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
+    return launch_pdl(kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
 }
 
 }  // namespace anvil

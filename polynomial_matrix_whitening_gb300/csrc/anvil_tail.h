@@ -17,16 +17,19 @@ struct TailBank {
     int g, m, n;
     int mat_begin;            // first matrix of this bank in the call
     long long chunk_begin;    // first 8-element row chunk of this bank in the call
+    long long row_begin;      // first row of this bank in the call (g * m rows per bank)
     long long power_begin;    // first block of this bank in the lane-power grid (set by its launcher)
     int vec8;                 // n % 8 == 0 and 16-byte aligned buffers: vector path
     float* power;             // workspace [g, nl]: lane powers
     float* scale;             // workspace [g, nl]: bf16-rounded lane scales
+    const uint64_t* sign;     // tail link slow-rail sign words [g, nck, m, 2] (NULL: read the rail)
+    int nck;
 };
 
 struct TailParams {
     TailBank bank[8];
     int nbanks, total_mats;
-    long long total_chunks;
+    long long total_chunks, total_rows;
 };
 
 cudaError_t launch_tail_power(const TailParams& p, cudaStream_t stream);

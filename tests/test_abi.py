@@ -44,8 +44,10 @@ def _call(descs, maps=None, nmaps=6, ws=1 << 40, ws_bytes=1 << 40, margin=1.05, 
 G = 1 << 32  # fake, aligned device addresses far apart
 
 
-def d(g=2, m=40, n=24, grad=G, vel=2 * G, out=3 * G, grad_bf16=0):
-    return anvil._raw_desc(g, m, n, grad, vel, out, grad_bf16)
+def d(g=2, m=40, n=24, grad=G, vel=2 * G, out=3 * G, grad_bf16=0, link=None):
+    desc = anvil._raw_desc(g, m, n, grad, vel, out, grad_bf16)
+    desc.tail_link = link
+    return desc
 
 
 def test_workspace_bytes():
@@ -73,9 +75,22 @@ def test_workspace_bytes():
     (dict(out=G), anvil.ERR_ALIAS),            # out == grad
     (dict(out=2 * G + 4), anvil.ERR_ALIAS),    # out inside velocity
     (dict(vel=G + 64), anvil.ERR_ALIAS),       # velocity overlaps grad
+    (dict(link=4 * G + 16), anvil.ERR_ALIGNMENT),  # the tail link wants 256-byte alignment
+    (dict(link=3 * G), anvil.ERR_ALIAS),       # tail link over out
+    (dict(link=2 * G - 256), anvil.ERR_ALIAS),  # tail link running into the velocity
 ])
 def test_argument_errors(desc, code):
     assert _call([d(**desc)]) == code
+
+
+def test_tail_link_bytes():
+    """The step-to-tail link: two 64-bit words (the slow rail's sign bits, the bits that
+    send the tail to the fp32 rail) per 64 columns of every row, rounded up to 256 bytes."""
+    assert anvil.tail_link_bytes((0, 4, 4)) == 0
+    assert anvil.tail_link_bytes((1, 20000, 4)) == 0
+    for g, m, n in [(22, 2816, 768), (22, 768, 768), (3, 130, 300), (2, 5, 3)]:
+        words = 16 * g * m * -(-n // 64)
+        assert anvil.tail_link_bytes((g, m, n)) == -(-words // 256) * 256
 
 
 def test_alias_across_banks_and_workspace():
@@ -118,7 +133,7 @@ def test_adam_argument_errors():
 def test_tail_argument_errors():
     def tail(**kw):
         base = dict(update=G, velocity=2 * G, lane_energy=3 * G, param=4 * G, mantissa=5 * G,
-                    eff_lr=6 * G, g=2, m=40, n=24, eff_wd=0.1, beta2=0.95)
+                    eff_lr=6 * G, g=2, m=40, n=24, eff_wd=0.1, beta2=0.95, tail_link=None)
         base.update(kw)
         d = anvil.TailDesc(*[base[k] for k, _ in anvil.TailDesc._fields_])
         return L.anvil_update_tail(ctypes.byref(d), 1, 1 << 40, 1 << 40, None)
@@ -127,6 +142,8 @@ def test_tail_argument_errors():
     assert tail(param=4 * G + 1) == anvil.ERR_ALIGNMENT
     assert tail(mantissa=4 * G + 16) == anvil.ERR_ALIAS   # mantissa over the parameter
     assert tail(lane_energy=2 * G) == anvil.ERR_ALIAS     # state written over the rails
+    assert tail(tail_link=7 * G + 128) == anvil.ERR_ALIGNMENT
+    assert tail(tail_link=4 * G + 256) == anvil.ERR_ALIAS  # link under the parameter being written
 
 
 def test_binding_rejects_tensors_the_kernels_cannot_take():

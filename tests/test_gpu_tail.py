@@ -145,6 +145,99 @@ def test_step_then_tail_matches_oracle_step_then_tail(A):
     np.testing.assert_allclose(t.lane_energy.cpu().numpy(), le_o, rtol=2e-2)
 
 
+# --------------------------------------------------------------------------- tail link
+
+LINK_SHAPES = [(4, 256, 768), (3, 1000, 264), (2, 520, 520), (3, 300, 130), (2, 130, 300)]
+
+
+def linked_step(A, shape, seed, link=True):
+    grad, vel = W.random_case(seed, *shape)
+    sc = dict(momentum=0.95, fast_beta=0.85, fast_weight=0.4385, slow_beta=0.98)
+    dev = torch.device("cuda")
+    bank = A.Bank(torch.from_numpy(grad).to(dev), torch.from_numpy(vel).to(dev),
+                  torch.empty(shape, dtype=torch.bfloat16, device=dev), **sc,
+                  tail_link=A.alloc_tail_link(shape) if link else None)
+    A.multi_bank_step([bank], A.alloc_workspace([shape]))
+    return bank, grad, vel, sc
+
+
+@pytest.mark.parametrize("shape", LINK_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_linked_step_then_tail_matches_oracle(A, shape):
+    """The step writes the tail link (the slow rail's sign bits) and the tail reads them
+    instead of the fp32 rail: the parameter moves as the oracle's whole bank update within
+    the cascade's 1e-2 bar, and equals the unlinked tail on the same step output bit for
+    bit (the gates are the same, the lane powers are computed the same way)."""
+    bank, grad, vel, sc = linked_step(A, shape, 41 + shape[1])
+    _, _, le, p, mt, lr = tail_inputs(41, *shape)
+    dev = torch.device("cuda")
+    ws = torch.empty(A.tail_workspace_bytes([shape]), dtype=torch.uint8, device=dev)
+
+    def tail(link):
+        t = A.Tail(bank.out, bank.velocity, to_dev(le), to_dev(p), torch.from_numpy(mt.view(np.int16)).cuda(),
+                   to_dev(lr), 0.1, 0.95, tail_link=bank.tail_link if link else None)
+        A.update_tail([t], ws)
+        torch.cuda.synchronize()
+        return (t.param.view(torch.int16).cpu().numpy().view(np.uint16), t.mantissa.cpu().numpy().view(np.uint16),
+                t.lane_energy.cpu().numpy())
+    p_l, mt_l, le_l = tail(True)
+    p_u, mt_u, le_u = tail(False)
+    assert A.device_error() == A.OK
+    np.testing.assert_array_equal(le_l, le_u)
+    np.testing.assert_array_equal(p_l, p_u)
+    np.testing.assert_array_equal(mt_l, mt_u)
+    out_o, vel_o = oracle.bank_step(grad, vel, **sc)
+    p_o, mt_o, le_o, _ = oracle.update_tail(out_o, le, 0.95, p, mt, vel_o[1], 0.1, lr)
+    w0 = master(p, mt)
+    dg, do = master(p_l, mt_l) - w0, master(p_o, mt_o) - w0
+    for i in range(shape[0]):
+        assert np.linalg.norm(dg[i] - do[i]) <= 1e-2 * np.linalg.norm(do[i])
+    np.testing.assert_allclose(le_l, le_o, rtol=2e-2)
+
+
+def test_link_gate_on_zero_tiny_and_huge_values(A):
+    """The decay gate [slow rail * w >= 0] from the link's sign bits equals the one computed
+    from the fp32 rail on every element, where the rail is zero, subnormal or huge and the
+    master weight is zero, negative zero, tiny or huge (the cases the link sends back to the
+    fp32 rail): bit-identical."""
+    g, m, n = 2, 64, 36
+    rng = np.random.default_rng(77)
+    grad = (rng.standard_normal((g, m, n)) * 0.02).astype(np.float32)
+    vel = np.zeros((2, g, m, n), np.float32)
+    # the slow rail after the step: exactly zero, subnormal, huge (fast_weight = 1, so the
+    # cascade reads the fast rail only and stays finite)
+    grad[0, :16] = 0.0
+    vel[1, 0, 8:16] = np.float32(3e-39) * np.sign(rng.standard_normal((8, n)))
+    vel[1, 1, :4] = np.float32(3e38) * np.sign(rng.standard_normal((4, n)))
+    dev = torch.device("cuda")
+    sc = dict(momentum=0.95, fast_beta=0.85, fast_weight=1.0, slow_beta=0.98)
+    bank = A.Bank(torch.from_numpy(grad).to(dev), torch.from_numpy(vel).to(dev),
+                  torch.empty((g, m, n), dtype=torch.bfloat16, device=dev), **sc,
+                  tail_link=A.alloc_tail_link((g, m, n)))
+    A.multi_bank_step([bank], A.alloc_workspace([(g, m, n)]))
+    torch.cuda.synchronize()
+    w = (rng.standard_normal((g, m, n)) * 0.05).astype(np.float32)
+    w[:, :, 0] = 0.0
+    w[:, :, 1] = -0.0
+    w[:, :, 2] = np.float32(1e-20) * np.sign(rng.standard_normal((g, m)))
+    w[:, :, 3] = np.float32(1e30)
+    bits = w.view(np.uint32)
+    p = (bits >> 16).astype(np.uint16)
+    mt = (bits & 0xFFFF).astype(np.uint16)
+    le = np.zeros((g, m), np.float32)
+    lr = np.full(g, 0.02, np.float32)
+    ws = torch.empty(A.tail_workspace_bytes([(g, m, n)]), dtype=torch.uint8, device=dev)
+    res = []
+    for link in (True, False):
+        t = A.Tail(bank.out, bank.velocity, to_dev(le), to_dev(p), torch.from_numpy(mt.view(np.int16)).cuda(),
+                   to_dev(lr), 0.5, 0.95, tail_link=bank.tail_link if link else None)
+        A.update_tail([t], ws)
+        torch.cuda.synchronize()
+        res.append((t.param.view(torch.int16).cpu().numpy(), t.mantissa.cpu().numpy(), t.lane_energy.cpu().numpy()))
+    assert A.device_error() == A.OK
+    for a, b in zip(*res):
+        np.testing.assert_array_equal(a, b)
+
+
 # --------------------------------------------------------------------------- Adam
 
 @pytest.mark.parametrize("count,offset", [(1 << 20, 0), (1000003, 0), (4096, 1)])

@@ -46,7 +46,7 @@ def test_reference_arm_prints_on_rank_zero_only(tmp_path):
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", "29533", "bench.py", "--impl",
-           "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+           "reference", "--gpus", "2", "--steps", "1", "--warmup", "3", "--reference-budget", "4"]
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stderr[-2000:]
     import json
