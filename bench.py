@@ -13,6 +13,7 @@ oracle on a bounded sample of the same workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl anvil|reference]
   python bench.py --ncu-case     # two eager steps of the same workload, for ncu captures
+  python bench.py --tail-ncu-case  # one step writing the tail link, then the tail without and with it
 
 ``--impl reference`` times the CPU oracle (the reference arm: no installable reference exists) on the same
 workload and metric.  With N > 1 (launched by torch.distributed.run) every rank runs an
@@ -665,6 +666,40 @@ def run_ncu_case():
     print("ncu case done")
 
 
+def run_tail_ncu_case():
+    """One step of the bench workload that also writes the step-to-tail link, then the
+    update tail on its outputs once without and once with the link: a short program for
+    ncu captures of the tail kernels."""
+    import torch
+    from polynomial_matrix_whitening_gb300 import anvil
+    dev = torch.device("cuda", 0)
+    wl = W.workloads()[WORKLOAD]
+    sc = wl.scalars(0)
+    banks = [anvil.Bank(torch.from_numpy(wl.grad(j, 0)).to(dev), torch.from_numpy(wl.velocity(j)).to(dev),
+                        torch.empty((b.g, b.m, b.n), dtype=torch.bfloat16, device=dev),
+                        momentum=sc.momentum, fast_beta=sc.fast_beta, fast_weight=sc.fast_weight,
+                        slow_beta=sc.slow_beta, tail_link=anvil.alloc_tail_link((b.g, b.m, b.n), device=dev))
+             for j, b in enumerate(wl.banks)]
+    anvil.multi_bank_step(banks, anvil.alloc_workspace([b.shape for b in banks], device=dev))
+    gen = torch.Generator(device=dev).manual_seed(5)
+    tws = torch.empty(anvil.tail_workspace_bytes([b.shape for b in banks]), dtype=torch.uint8, device=dev)
+    for link in (False, True):
+        tails = []
+        for b in banks:
+            g_, m_, n_ = b.shape
+            bits = (torch.randn((g_, m_, n_), device=dev, generator=gen) * 0.05).view(torch.int32)
+            tails.append(anvil.Tail(b.out, b.velocity, torch.zeros((g_, m_ if m_ >= n_ else n_), device=dev),
+                                    (bits >> 16).to(torch.int16).view(torch.bfloat16).contiguous(),
+                                    (bits & 0xFFFF).to(torch.int16).contiguous(),
+                                    torch.full((g_,), 0.02, device=dev), 0.1, 0.95,
+                                    tail_link=b.tail_link if link else None))
+        anvil.update_tail(tails, tws)
+    torch.cuda.synchronize()
+    if anvil.device_error() != anvil.OK:
+        raise RuntimeError("device error word set")
+    print("tail ncu case done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -675,9 +710,13 @@ def main():
     ap.add_argument("--reference-budget", type=float, default=REFERENCE_BUDGET_S,
                     help="CPU seconds the reference arm's warm-up and timed steps may take")
     ap.add_argument("--ncu-case", action="store_true")
+    ap.add_argument("--tail-ncu-case", action="store_true")
     args = ap.parse_args()
     if args.ncu_case:
         run_ncu_case()
+        return
+    if args.tail_ncu_case:
+        run_tail_ncu_case()
         return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
