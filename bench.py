@@ -2,7 +2,7 @@
 """Benchmark of the ANVIL optimizer step on GB300: one full step over the three
 projection banks (qk 22x256x768, vo 22x768x768, mlp 22x2816x768; 66 matrices), mixed
 synthetic inputs (half Gaussian, half rank-32 plus 1e-3 noise), post-engage scalars,
-each step one CUDA-graph replay of its three launches (momentum, d, the cascade).
+each step one CUDA-graph replay of its four launches (momentum, d, X / d, the cascade).
 
 Prints one JSON line (rank 0).  ``value`` is whole-job matrices/s with the inputs
 resident in HBM; ``e2e`` is the same metric through the same C-ABI call with the
@@ -54,7 +54,7 @@ NCU_TRAFFIC = {
 
 
 def kernel_source_hash(kind):
-    name = "anvil_elementwise.cu" if kind in ("momentum", "norm_d") else "anvil_gemm.cu"
+    name = "anvil_elementwise.cu" if kind in ("momentum", "norm_d", "normalize") else "anvil_gemm.cu"
     with open(os.path.join(ROOT, "polynomial_matrix_whitening_gb300", "csrc", name), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
@@ -95,8 +95,7 @@ def algorithmic_work(banks, nmaps=6):
         w["momentum"] += g * m * n * 22.0        # 4 B grad + 2x(4+4) B rails + 2 B X
         w["normalize"] += g * m * n * 4.0        # read + write bf16
         w["norm_d"] += g * m * 4.0
-        # the cascade kernel: every product of every map (the normalisation's bytes are
-        # not counted: the kernel is bound by the tensor pipe)
+        # the cascade kernel: every product of every map
         w["cascade"] += g * nmaps * (s * (s + 1) * L + s * (s + 1) * s + 2.0 * s * s * L)
     return w
 
@@ -354,7 +353,7 @@ def run_anvil(args, world, rank, local):
             anvil.multi_bank_step(banks, ws, stream=stream)
         return gr
 
-    launches_per_step = 3   # momentum, norm_d, the cascade
+    launches_per_step = 4   # momentum, norm_d, normalize, the cascade
     nsteps, nwarm = args.steps, args.warmup
 
     def capture_sequence(count):
@@ -646,7 +645,7 @@ def run_anvil(args, world, rank, local):
 
 def run_ncu_case():
     """Two eager (non-graph) steps of the bench workload, one grad draw: a short program for
-    ncu captures (three launches per step: momentum, norm_d, the cascade)."""
+    ncu captures (four launches per step: momentum, norm_d, normalize, the cascade)."""
     import torch
     from polynomial_matrix_whitening_gb300 import anvil
     dev = torch.device("cuda", 0)

@@ -21,9 +21,8 @@
  * Every number is computed on the GPU by this library's own kernels; there is
  * no CPU path.  All calls are asynchronous on the given stream (a
  * cudaStream_t / CUstream handle passed as void*; NULL = legacy default
- * stream).  A step is three kernels on that stream: momentum + cast, the normaliser d,
- * and one persistent kernel for the whole cascade (the normalisation and every product of
- * every map).  No call below allocates, frees or synchronises, except
+ * stream).  A step is four kernels on that stream: momentum + cast, the normaliser d,
+ * the normalisation X / d, and one persistent kernel for every product of every map.  No call below allocates, frees or synchronises, except
  * anvil_bank_step on its first use of a size (documented there), the error reads
  * anvil_last_device_error (waits for its stream) and anvil_device_error (waits for the
  * device).  Errors are returned as status codes; no
@@ -272,7 +271,7 @@ anvil_status anvil_selftest_wait_timeout(unsigned timeout_us, void* stream);
  * with profiling on, while a stream is capturing).  end synchronises, writes up
  * to cap records in launch order, destroys the events and returns how many
  * launches were timed (negative on a CUDA error). */
-/* Kinds 2-7 are the cascade's phases, each its own launch in traced steps only; an
+/* Kinds 3-7 are the cascade's phases, each its own launch in traced steps only; an
  * untraced step runs them all in one ANVIL_KERNEL_CASCADE launch. */
 typedef enum {
     ANVIL_KERNEL_MOMENTUM = 0,     /* momentum + cast + diagonal partials */
@@ -287,7 +286,7 @@ typedef enum {
     ANVIL_KERNEL_TAIL_SCALE = 9,   /* update tail: lane energies and scales */
     ANVIL_KERNEL_TAIL_APPLY = 10,  /* update tail: equalise + sign-aligned decay update */
     ANVIL_KERNEL_ADAM = 11,        /* Adam step */
-    ANVIL_KERNEL_CASCADE = 12      /* the whole cascade (normalisation, every product of every map) */
+    ANVIL_KERNEL_CASCADE = 12      /* the whole cascade (every product of every map) */
 } anvil_kernel_kind;
 
 typedef struct { int kind; float ms; } anvil_profile_record;
@@ -297,14 +296,14 @@ int anvil_profile_end(anvil_profile_record* records, int cap);
 
 /* Diagnostic, host only (no CUDA call, no GPU needed): the order in which the cascade
  * kernel of anvil_multi_bank_step walks its work items for these banks and nmaps maps.
- * Items are 256 x 256 output tiles; the kernel's phases are the first Gram, the
- * normalisation, then per map the Gram (after the first map), B = bA + cA^2 and the
- * X-update.  The order is a list of runs, each one phase of a range of matrices of one
+ * Items are 256 x 256 output tiles; the kernel's phases are the first Gram, then per
+ * map the Gram (after the first map), B = bA + cA^2 and the X-update (the normalisation
+ * X / d is its own kernel, before the cascade).  The order is a list of runs, each one phase of a range of matrices of one
  * bank, matrix by matrix; every phase of a matrix comes after the phases it reads.
  * Writes up to cap runs and returns how many there are (-1 on invalid arguments). */
 typedef struct {
     int phase;  /* phase index, 0 = the first Gram */
-    int op;     /* 0 Gram, 1 first Gram, 2 B = bA + cA^2, 3 X-update, 4 last X-update, 5 normalisation */
+    int op;     /* 0 Gram, 1 first Gram, 2 B = bA + cA^2, 3 X-update, 4 last X-update */
     int bank;   /* index of the bank in the call */
     int mat0;   /* first matrix of the run */
     int nmat;   /* matrices in the run */
@@ -325,8 +324,7 @@ int anvil_schedule_runs(const anvil_bank_desc* banks, int nbanks, int nmaps, anv
  *   free, 8 its first k-block landed, 9 its last MMAs were issued, 10 the epilogue found
  *   the accumulator complete, 11 the epilogue was done;  12 and 13: SM cycles (clock64)
  *   at 8 and 9;  14 SM cycles the MMA issuer waited for k-blocks after the first to
- *   land;  15 SM cycles the producer waited for free operand stages.  Words of a field
- *   an item does not have (a normalisation tile has no MMA) stay zero.
+ *   land;  15 SM cycles the producer waited for free operand stages.
  * anvil_timeline_read copies min(bytes, the buffer) to host memory (synchronous; call
  * after the launch has completed).  anvil_timeline_clear zeroes the buffer. */
 #define ANVIL_TIMELINE_ITEMS 16384

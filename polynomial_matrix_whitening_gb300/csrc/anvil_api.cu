@@ -198,7 +198,7 @@ anvil_status make_layout(const anvil_bank_desc* banks, int nbanks, Layout* L) {
     if (L->y_elems > (static_cast<size_t>(1) << 40)) return ANVIL_ERR_UNSUPPORTED_SHAPE;
     L->off_d = 0;
     L->off_cnt = align256(L->off_d + sizeof(float) * L->total_mats);
-    L->off_part = align256(L->off_cnt + sizeof(unsigned) * (2 * L->total_mats + SCHED_COUNTERS));
+    L->off_part = align256(L->off_cnt + sizeof(unsigned) * (L->total_mats + SCHED_COUNTERS));
     L->off_y0 = align256(L->off_part + sizeof(float) * L->part_elems);
     L->off_y1 = align256(L->off_y0 + 2 * L->y_elems);
     L->off_a = align256(L->off_y1 + 2 * L->y_elems);
@@ -412,6 +412,27 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
                                              cudaMemcpyDeviceToDevice, stream)))
             return cuda_fail(e, "trace");
     }
+    // ---- X / d
+    NormXParams xp;
+    memset(&xp, 0, sizeof(xp));
+    xp.nbanks = nbanks;
+    for (int i = 0; i < nbanks; ++i) {
+        const Geom& G = L.bank[i];
+        NormXBank& X = xp.bank[i];
+        X.y0 = P[i].y[0];
+        X.y1 = P[i].y[1];
+        X.d = P[i].d;
+        X.chunks_per_mat = static_cast<long long>(G.s_pad) * G.L_pad / 8;
+        X.chunk_begin = xp.total_chunks;
+        xp.total_chunks += G.g * X.chunks_per_mat;
+    }
+    if ((e = profiled(ANVIL_KERNEL_NORMALIZE, stream, [&] { return launch_normalize(xp, stream); })))
+        return cuda_fail(e, "normalize launch");
+    if (trace && trace->X) {
+        const Geom& G = L.bank[0];
+        if ((e = launch_extract_x(P[0].y[1], trace->X, G.g, G.m, G.n, G.tall, G.s_pad, G.L_pad, stream)))
+            return cuda_fail(e, "trace");
+    }
 
     // ---- the cascade: every phase of every map in one persistent launch (one launch per
     // phase when tracing, with the intermediate values copied out between them)
@@ -421,8 +442,7 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
     cp->nbanks = nbanks;
     cp->sm_count = dev->sm_count;
     cp->chain = reinterpret_cast<unsigned*>(ws + L.off_cnt);
-    cp->norm = cp->chain + L.total_mats;
-    unsigned* sched_ctr = cp->norm + L.total_mats;  // [SCHED_COUNTERS]
+    unsigned* sched_ctr = cp->chain + L.total_mats;  // [SCHED_COUNTERS]
     cp->err = dev->err;
     int order[ANVIL_MAX_BANKS];
     cascade_bank_order(L.bank, nbanks, order);
@@ -459,23 +479,16 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         cudaError_t ee = profiled(kind, stream, [&] { return launch_cascade(*cp, stream); });
         return ee ? cuda_fail(ee, "cascade launch") : ANVIL_OK;
     };
-    if (!trace) {
-        order_normalize_interleaved(cp);
-        return run_range(0, cp->nruns, ANVIL_KERNEL_CASCADE, 0);
-    }
+    if (!trace) return run_range(0, cp->nruns, ANVIL_KERNEL_CASCADE, 0);
 
-    static const int kinds[6] = {ANVIL_KERNEL_GRAM, ANVIL_KERNEL_GRAM_NORM, ANVIL_KERNEL_SQPOLY,
-                                 ANVIL_KERNEL_XUPDATE, ANVIL_KERNEL_XUPDATE_OUT, ANVIL_KERNEL_NORMALIZE};
+    static const int kinds[5] = {ANVIL_KERNEL_GRAM, ANVIL_KERNEL_GRAM_NORM, ANVIL_KERNEL_SQPOLY,
+                                 ANVIL_KERNEL_XUPDATE, ANVIL_KERNEL_XUPDATE_OUT};
     const Geom& G0 = L.bank[0];
     const size_t nx1 = static_cast<size_t>(G0.g) * G0.m * G0.n;
     const size_t na1 = static_cast<size_t>(G0.g) * G0.s * G0.s;
     for (int ph = 0, k = 0; ph < cp->nphases; ++ph) {
         const int op = cp->phase[ph].op;
         if ((st = run_range(phase_run[ph], phase_run[ph + 1], kinds[op], 1 + ph))) return st;
-        if (op == OP_NORMALIZE && trace->X &&
-            (e = launch_extract_x(P[0].y[1], trace->X, G0.g, G0.m, G0.n, G0.tall, G0.s_pad, G0.L_pad,
-                                  stream)))
-            return cuda_fail(e, "trace");
         if ((op == OP_GRAM || op == OP_GRAM_NORM) && trace->A &&
             (e = launch_extract_sq(P[0].a, trace->A + k * na1, G0.g, G0.s, G0.s_pad, stream)))
             return cuda_fail(e, "trace");
@@ -988,7 +1001,7 @@ int anvil_schedule_runs(const anvil_bank_desc* banks, int nbanks, int nmaps, anv
     anvil_map maps[ANVIL_MAX_MAPS];
     for (int k = 0; k < nmaps; ++k) maps[k] = anvil_map{1.f, 0.f, 0.f};  // coefficients do not shape the order
     build_phases(cp, maps, nmaps);
-    order_normalize_interleaved(cp);
+    order_phase_major(cp, nullptr);
     const int nruns = cp->nruns;
     for (int r = 0; r < nruns && r < cap; ++r) {
         const CascadeRun& R = cp->run[r];

@@ -62,6 +62,34 @@ __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
     return (static_cast<uint64_t>(w & 0xffff0000u) << 32) | (w << 16);
 }
 
+// bf16(RN(x / dd)) for four pairs of fp32 x, given rcp2 = (RN(1/dd), RN(1/dd)).  The
+// product q = RN(x * RN(1/dd)) is within 2.5 ulp of RN(x / dd), so both round to the same
+// bf16 unless a bf16 rounding boundary (low 16 bits 0x8000) lies within 8 ulps of q, or q
+// is tiny (exponent < 8), huge or not finite; a chunk with such an element (about one in
+// 1000) takes the correctly rounded division, out of line.
+__device__ __forceinline__ bool near_bf16_boundary(uint32_t b) {
+    return (((b + 8u) & 0xfff0u) == 0x8000u) | ((((b >> 23) + 1u) & 0xffu) < 9u);
+}
+static __device__ __noinline__ uint4 div4_exact(uint64_t x0, uint64_t x1, uint64_t x2, uint64_t x3, float dd) {
+    const uint64_t x[4] = {x0, x1, x2, x3};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        o[e] = f2_to_bf2(f2_pack(__fdiv_rn(__uint_as_float(static_cast<uint32_t>(x[e])), dd),
+                                 __fdiv_rn(__uint_as_float(static_cast<uint32_t>(x[e] >> 32)), dd)));
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+__device__ __forceinline__ uint4 div4_to_bf2(uint64_t x0, uint64_t x1, uint64_t x2, uint64_t x3, uint64_t rcp2,
+                                             float dd) {
+    const uint64_t q0 = f2_mul(x0, rcp2), q1 = f2_mul(x1, rcp2), q2 = f2_mul(x2, rcp2), q3 = f2_mul(x3, rcp2);
+    const bool near = near_bf16_boundary(static_cast<uint32_t>(q0)) | near_bf16_boundary(static_cast<uint32_t>(q0 >> 32)) |
+                      near_bf16_boundary(static_cast<uint32_t>(q1)) | near_bf16_boundary(static_cast<uint32_t>(q1 >> 32)) |
+                      near_bf16_boundary(static_cast<uint32_t>(q2)) | near_bf16_boundary(static_cast<uint32_t>(q2 >> 32)) |
+                      near_bf16_boundary(static_cast<uint32_t>(q3)) | near_bf16_boundary(static_cast<uint32_t>(q3 >> 32));
+    if (__builtin_expect(near, 0)) return div4_exact(x0, x1, x2, x3, dd);
+    return make_uint4(f2_to_bf2(q0), f2_to_bf2(q1), f2_to_bf2(q2), f2_to_bf2(q3));
+}
+
 // ---- programmatic dependent launch ---------------------------------------------------
 // A kernel launched with programmatic stream serialisation may start while the previous
 // kernel of the stream finishes; it must wait here before touching anything that kernel

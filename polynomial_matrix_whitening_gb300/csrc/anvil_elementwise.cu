@@ -3,8 +3,8 @@
 //     track_1_short/optim/anvil.py", anvil_cascade, first block), writing X in the
 //     small-side-major working layout and the per-64-block sums of squares of the bf16
 //     values, from which the first Gram's diagonal (hence the trace) is read;
-//   * norm_d_kernel: d = sqrt(tr) * FROBENIUS_MARGIN + FROBENIUS_EPS per matrix (the
-//     division X / d itself is a phase of the cascade kernel, anvil_gemm.cu);
+//   * norm_d_kernel: d = sqrt(tr) * FROBENIUS_MARGIN + FROBENIUS_EPS per matrix;
+//   * normalize_kernel: the normalised X = bf16(X / d), streamed at HBM rate;
 //   * extraction kernels for the traced (parity-test) path and the wait self-test.
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -217,8 +217,8 @@ __global__ void __launch_bounds__(NORM_THREADS) norm_d_kernel(const __grid_const
         if (gm >= p.bank[i].mat_begin) bi = i;
     const NormBank& B = p.bank[bi];
     const int lm = gm - B.mat_begin;
-    if (threadIdx.x < 2) p.counters[threadIdx.x * p.total_mats + gm] = 0u;
-    if (gm == 0 && threadIdx.x < SCHED_COUNTERS) p.counters[2 * p.total_mats + threadIdx.x] = 0u;
+    if (threadIdx.x == 0) p.counters[gm] = 0u;
+    if (gm == 0 && threadIdx.x < SCHED_COUNTERS) p.counters[p.total_mats + threadIdx.x] = 0u;
     const float* part = B.part + static_cast<size_t>(lm) * B.nlb * B.s_pad;  // [nlb][s_pad]
     float acc = 0.f;
     for (int i = threadIdx.x; i < B.s_pad; i += NORM_THREADS) {
@@ -249,6 +249,53 @@ __global__ void __launch_bounds__(NORM_THREADS) norm_d_kernel(const __grid_const
 
 cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream) {
     return launch_pdl(norm_d_kernel, dim3(p.total_mats), dim3(NORM_THREADS), 0, stream, p);
+}
+
+// X / d (page "modded-nanogpt track_1_short/optim/anvil.py", anvil_cascade, the division
+// of X by its normaliser) over the padded working layout, which is contiguous per bank:
+// chunk k of a bank is elements 8k .. 8k + 7 of its Y0 and Y1.  Each thread converts
+// NX_CHUNKS chunks, every load in flight before the first store; a warp's loads cover 32
+// consecutive chunks (512 bytes).  The quotient is bf16(RN(x / d)), each element rounded
+// as the page's fp32 division then its bf16 cast (div4_to_bf2); the padding stays zero.
+constexpr int NX_THREADS = 256;
+constexpr int NX_CHUNKS = 4;
+__global__ void __launch_bounds__(NX_THREADS) normalize_kernel(const __grid_constant__ NormXParams p) {
+    pdl_allow_next();
+    pdl_wait_previous();  // d (norm_d) and X_raw (momentum)
+    const long long c0 = static_cast<long long>(blockIdx.x) * (NX_THREADS * NX_CHUNKS) + threadIdx.x;
+    uint4 v[NX_CHUNKS];
+    int q[NX_CHUNKS];
+    long long loc[NX_CHUNKS];
+#pragma unroll
+    for (int i = 0; i < NX_CHUNKS; ++i) {
+        const long long c = c0 + static_cast<long long>(i) * NX_THREADS;
+        q[i] = -1;
+        if (c < p.total_chunks) {
+            int b = 0;
+#pragma unroll 1
+            for (int k = 1; k < p.nbanks; ++k)
+                if (c >= p.bank[k].chunk_begin) b = k;
+            q[i] = b;
+            loc[i] = c - p.bank[b].chunk_begin;
+            v[i] = __ldg(reinterpret_cast<const uint4*>(p.bank[b].y0) + loc[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NX_CHUNKS; ++i) {
+        if (q[i] < 0) continue;
+        const NormXBank& B = p.bank[q[i]];
+        const float d = B.d[loc[i] / B.chunks_per_mat];
+        const float rcp = __frcp_rn(d);
+        reinterpret_cast<uint4*>(B.y1)[loc[i]] =
+            div4_to_bf2(bf2_to_f2(v[i].x), bf2_to_f2(v[i].y), bf2_to_f2(v[i].z), bf2_to_f2(v[i].w), f2_pack(rcp, rcp), d);
+    }
+}
+
+cudaError_t launch_normalize(const NormXParams& p, cudaStream_t stream) {
+    if (p.total_chunks <= 0) return cudaSuccess;
+    const long long per_block = NX_THREADS * NX_CHUNKS;
+    const unsigned blocks = static_cast<unsigned>((p.total_chunks + per_block - 1) / per_block);
+    return launch_pdl(normalize_kernel, dim3(blocks), dim3(NX_THREADS), 0, stream, p);
 }
 
 // ---------------------------------------------------------------- tracing

@@ -1,10 +1,8 @@
 // anvil_gemm.cu -- the ANVIL cascade (page "modded-nanogpt track_1_short/optim/anvil.py",
-// anvil_cascade: the XTX / XXT, ba_plus_cAA and baddbmm steps of every spectral map, and
-// the division of X by its normaliser) as ONE persistent tcgen05 kernel for sm_103a that
-// walks every phase of a step:
+// anvil_cascade: the XTX / XXT, ba_plus_cAA and baddbmm steps of every spectral map) as ONE
+// persistent tcgen05 kernel for sm_103a that walks every phase of a step:
 //
 //   OP_GRAM_NORM : A  = bf16(bf16(Y Y^T) / d^2)     (the first Gram, on X_raw)
-//   OP_NORMALIZE : Y1 = bf16(Y0 / d)                (no product: epilogue warps only)
 //   OP_GRAM      : A  = bf16(Y Y^T)
 //   OP_SQPOLY    : B  = bf16(b A + c A A)
 //   OP_XUPDATE   : Y' = bf16(a Y + B Y)             (OP_XUPDATE_OUT: the last, into out)
@@ -138,6 +136,12 @@ struct Work {
     __device__ int bi() const { return static_cast<int>(w1.x); }
     __device__ int bj() const { return static_cast<int>(w1.y); }
     __device__ int map(int k) const { return static_cast<int>(static_cast<int8_t>((w1.z >> (8 * k)) & 0xffu)); }
+    // A diagonal block of a symmetric product (a Gram or A*A block with bi == bj): in each
+    // CTA the A rows and the B columns are the same operand rows, read through the same
+    // maps, so one load serves both descriptors.
+    __device__ bool shared_ab() const {
+        return !op_xupdate(op()) && w1.x == w1.y && ((w1.z ^ (w1.z >> 16)) & 0xffffu) == 0u;
+    }
 };
 
 struct alignas(16) SchedRing {
@@ -236,7 +240,7 @@ __device__ __forceinline__ Work make_work(const CascadeParams& p, int item0, int
     const Item c = decode_item(p, item0 + t);
     const CascadePhase& P = p.phase[c.ph];
     const CascadeBank& bk = p.bank[c.bank];
-    const int nkb = P.op == OP_NORMALIZE ? 0 : (op_gram(P.op) ? bk.L_pad : bk.s_pad) / BK;
+    const int nkb = (op_gram(P.op) ? bk.L_pad : bk.s_pad) / BK;
     w.w0 = make_uint4(static_cast<uint32_t>(t), static_cast<uint32_t>(P.op | (c.bank << 8) | (c.ph << 16)),
                       static_cast<uint32_t>(c.mat), static_cast<uint32_t>(nkb));
     const uint32_t maps = (static_cast<uint32_t>(P.map_a) & 0xffu) | ((static_cast<uint32_t>(P.map_a_t) & 0xffu) << 8) |
@@ -266,11 +270,8 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 // Whether the phases item `it` reads are complete for its matrix (no wait).
 __device__ __forceinline__ bool deps_ready(const CascadeParams& p, const Item& it) {
     const CascadePhase& P = p.phase[it.ph];
-    const unsigned nc = P.need_chain[it.bank], nn = P.need_norm[it.bank];
-    const int m = p.bank[it.bank].mat_begin + it.mat;
-    if (nc && ld_acquire(p.chain + m) < nc) return false;
-    if (nn && ld_acquire(p.norm + m) < nn) return false;
-    return true;
+    const unsigned nc = P.need_chain[it.bank];
+    return !nc || ld_acquire(p.chain + p.bank[it.bank].mat_begin + it.mat) >= nc;
 }
 
 // Waits (bounded) for the same; then orders this thread's later TMA loads after it.
@@ -304,6 +305,7 @@ __device__ __forceinline__ void load_kblock(const CascadeParams& p, const Work& 
     const int bofs = bj * PAIR + TILE * static_cast<int>(rank);
     const int map_a = w.map(0), map_a_t = w.map(1), map_b = w.map(2), map_b_t = w.map(3);
     uint8_t* sb = sa + A_STAGE;
+    const bool shared = w.shared_ab();
     if (map_a_t >= 0 && kb * BK < bi * PAIR) {
         tma_load_3d_pair(sa, &tm[map_a_t], fb, arow, kb * BK, mat);
         tma_load_3d_pair(sa + 8192, &tm[map_a_t], fb, arow + 64, kb * BK, mat);
@@ -311,6 +313,7 @@ __device__ __forceinline__ void load_kblock(const CascadeParams& p, const Work& 
         tma_load_3d_pair(sa, &tm[map_a], fb, kb * BK, arow, mat);
     }
     const bool xu = op_xupdate(w.op());
+    if (shared) return;
     if (xu || (map_b_t >= 0 && kb * BK < bj * PAIR)) {
         const CUtensorMap* tb = &tm[xu ? map_b : map_b_t];
         tma_load_3d_pair(sb, tb, fb, bofs, kb * BK, mat);
@@ -322,35 +325,7 @@ __device__ __forceinline__ void load_kblock(const CascadeParams& p, const Work& 
 
 // The completion counter a finished tile adds to.
 __device__ __forceinline__ unsigned* tile_counter(const CascadeParams& p, const Item& it) {
-    return (p.phase[it.ph].op == OP_NORMALIZE ? p.norm : p.chain) + p.bank[it.bank].mat_begin + it.mat;
-}
-
-// bf16(RN(x / dd)) for four pairs of fp32 x, given rcp2 = (RN(1/dd), RN(1/dd)).  The
-// product q = RN(x * RN(1/dd)) is within 2.5 ulp of RN(x / dd), so both round to the same
-// bf16 unless a bf16 rounding boundary (low 16 bits 0x8000) lies within 8 ulps of q, or q
-// is tiny (exponent < 8), huge or not finite; a chunk with such an element (about one in
-// 1000) takes the correctly rounded division, out of line.
-__device__ __forceinline__ bool near_bf16_boundary(uint32_t b) {
-    return (((b + 8u) & 0xfff0u) == 0x8000u) | ((((b >> 23) + 1u) & 0xffu) < 9u);
-}
-__device__ __noinline__ uint4 div4_exact(uint64_t x0, uint64_t x1, uint64_t x2, uint64_t x3, float dd) {
-    const uint64_t x[4] = {x0, x1, x2, x3};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-        o[e] = f2_to_bf2(f2_pack(__fdiv_rn(__uint_as_float(static_cast<uint32_t>(x[e])), dd),
-                                 __fdiv_rn(__uint_as_float(static_cast<uint32_t>(x[e] >> 32)), dd)));
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-__device__ __forceinline__ uint4 div4_to_bf2(uint64_t x0, uint64_t x1, uint64_t x2, uint64_t x3, uint64_t rcp2,
-                                             float dd) {
-    const uint64_t q0 = f2_mul(x0, rcp2), q1 = f2_mul(x1, rcp2), q2 = f2_mul(x2, rcp2), q3 = f2_mul(x3, rcp2);
-    const bool near = near_bf16_boundary(static_cast<uint32_t>(q0)) | near_bf16_boundary(static_cast<uint32_t>(q0 >> 32)) |
-                      near_bf16_boundary(static_cast<uint32_t>(q1)) | near_bf16_boundary(static_cast<uint32_t>(q1 >> 32)) |
-                      near_bf16_boundary(static_cast<uint32_t>(q2)) | near_bf16_boundary(static_cast<uint32_t>(q2 >> 32)) |
-                      near_bf16_boundary(static_cast<uint32_t>(q3)) | near_bf16_boundary(static_cast<uint32_t>(q3 >> 32));
-    if (__builtin_expect(near, 0)) return div4_exact(x0, x1, x2, x3, dd);
-    return make_uint4(f2_to_bf2(q0), f2_to_bf2(q1), f2_to_bf2(q2), f2_to_bf2(q3));
+    return p.chain + p.bank[it.bank].mat_begin + it.mat;
 }
 
 // The elementwise part of each op's epilogue on a pair: accumulator values v (packed fp32
@@ -544,33 +519,6 @@ __device__ __forceinline__ void epi_tile(const CascadeParams& p, const CascadeBa
     }
 }
 
-// A normalisation tile: Y1 = bf16(Y0 / d) over this CTA's 128 rows and this group's 128
-// of the tile's 256 columns, streamed with coalesced 16-byte loads and stores (a warp
-// covers two 256-byte row segments per access), every load of the thread in flight at
-// once; no staging and no product.
-__device__ __forceinline__ void normalize_tile(const CascadeBank& bk, const Item& c, uint32_t rank, int grp,
-                                               int tid) {
-    const float d = bk.d[c.mat];
-    const float rcp = __frcp_rn(d);
-    const uint64_t rcp2 = f2_pack(rcp, rcp);
-    const size_t row0 = static_cast<size_t>(c.mat) * bk.s_pad + c.bi * PAIR + TILE * rank;
-    const int col0 = c.bj * PAIR + 128 * grp;
-    constexpr int N = 128 * 128 * 2 / 16 / 128;  // 16-byte chunks per thread
-    uint4 v[N];
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const int ch = tid + 128 * i;  // chunk: row ch / 16, 8 columns (ch % 16) * 8
-        const uint4* src = reinterpret_cast<const uint4*>(bk.y0 + (row0 + ch / 16) * bk.L_pad + col0 + (ch % 16) * 8);
-        v[i] = ld_stream_v4(src);
-    }
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const int ch = tid + 128 * i;
-        *reinterpret_cast<uint4*>(bk.y1 + (row0 + ch / 16) * bk.L_pad + col0 + (ch % 16) * 8) =
-            div4_to_bf2(bf2_to_f2(v[i].x), bf2_to_f2(v[i].y), bf2_to_f2(v[i].z), bf2_to_f2(v[i].w), rcp2, d);
-    }
-}
-
 __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_constant__ CascadeParams p) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -642,7 +590,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 if (w.t() == 0x7fffffff) aborted = 1;
                 if (rank == 0) mbar_arrive_relaxed(&sring.taken[k % SDEPTH]);
                 if (w.t() >= nitems) break;
-                if (w.op() == OP_NORMALIZE) continue;
                 // the scheduler saw the item's inputs complete (acquire); these TMA reads follow
                 asm volatile("fence.proxy.async.global;" ::: "memory");
                 const int nkb = w.nkb();
@@ -664,7 +611,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                     tl_wait += clock64() - tl_c0;
                     if (kb == nkb - 1 && rank == 0) TL_PUT(w.t(), TL_PROD_WAIT_CLK, tl_wait);
 #endif
-                    if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], 2 * STAGE);
+                    if (rank == 0) mbar_arrive_expect_tx(&full_bar[s], w.shared_ab() ? 2 * A_STAGE : 2 * STAGE);
                     if (kb == 0 && rank == 0) TL_PUT(w.t(), TL_PROD_FIRST, globaltimer_ns());
                     load_kblock(p, w, kb, rank, smem + s * STAGE, map_to_rank(&full_bar[s], 0));
                     issued = it + 1;
@@ -678,16 +625,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             // ---------------- MMA issuer (leader CTA)
-            int it = 0, mt = 0;
+            // The issuing thread is the k-loop's critical path: between two k-blocks it has
+            // only the time the queued MMAs take, so the next stage's barrier is tested
+            // (without blocking) while this k-block's MMAs run, and a blocking wait happens
+            // only when that test found the stage not yet loaded.
+            const uint32_t stage0 = smem_u32(smem);
+            int s = 0, mt = 0;
+            uint32_t ph = 0;     // parity of stage s's next fill
+            bool ready = false;  // that fill already seen complete
             for (int lt = 0;; ++lt) {
                 const Work w = sched_take(sring, lt, p.err);
                 if (w.t() == 0x7fffffff) aborted = 1;
                 if (w.t() >= nitems) break;
-                if (w.op() == OP_NORMALIZE) continue;
                 const bool xu = op_xupdate(w.op());
                 const int nkb = w.nkb();
-                const int bi = w.bi(), bj = w.bj();
-                const bool a_sym = w.map(1) >= 0, b_sym = w.map(3) >= 0;
+                const bool shared_ab = w.shared_ab();
+                // operands staged MN-major: Y in the X-update, and the k-blocks left of a
+                // symmetric operand's diagonal block, read from the transposed upper block (as
+                // the producer loaded them)
+                const int kb_a_mn = w.map(1) >= 0 ? w.bi() * (PAIR / BK) : 0;
+                const int kb_b_mn = xu ? nkb : (w.map(3) >= 0 ? w.bj() * (PAIR / BK) : 0);
                 const int ab = mt & 1;
                 const uint32_t u = static_cast<uint32_t>(mt >> 1);
                 ++mt;
@@ -703,13 +660,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
 #ifdef ANVIL_TIMELINE
                 unsigned long long tl_wait = 0;
 #endif
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t r = static_cast<uint32_t>(it / STAGES);
+                for (int kb = 0; kb < nkb; ++kb) {
 #ifdef ANVIL_TIMELINE
                     const unsigned long long tl_c0 = clock64();
 #endif
-                    if (!mbar_wait(&full_bar[s], r & 1u, p.err)) {
+                    if (!ready && !mbar_wait(&full_bar[s], ph, p.err)) {
                         ok = false;
                         break;
                     }
@@ -722,12 +677,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                         TL_PUT(w.t(), TL_MMA_FIRST_CLK, clock64());
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(smem + s * STAGE);
-                    const uint32_t b0 = a0 + A_STAGE;
-                    // operands staged MN-major: Y in the X-update, and k-blocks read from the
-                    // transposed upper block of a symmetric operand (as the producer loaded them)
-                    const bool a_mn = a_sym && kb * BK < bi * PAIR;
-                    const bool b_mn = xu || (b_sym && kb * BK < bj * PAIR);
+                    const uint32_t a0 = stage0 + static_cast<uint32_t>(s * STAGE);
+                    const uint32_t b0 = shared_ab ? a0 : a0 + A_STAGE;
+                    const bool a_mn = kb < kb_a_mn, b_mn = kb < kb_b_mn;
                     const uint32_t idesc = idesc_bf16_f32(PAIR, PAIR, a_mn, b_mn);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
@@ -737,11 +689,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                                                  : smem_desc_sw128(b0 + kk * 32, 16, 1024);
                         umma_bf16_pair(dacc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
                     }
+                    const int s_next = s + 1 == STAGES ? 0 : s + 1;
+                    const uint32_t ph_next = s_next == 0 ? ph ^ 1u : ph;
+                    ready = mbar_test_wait(smem_u32(&full_bar[s_next]), ph_next);
                     umma_commit_pair(&empty_bar[s], 3);  // frees stage s in both CTAs
                     if (kb == nkb - 1) {
                         TL_PUT(w.t(), TL_MMA_LAST, globaltimer_ns());
                         TL_PUT(w.t(), TL_MMA_LAST_CLK, clock64());
                     }
+                    s = s_next;
+                    ph = ph_next;
                 }
                 if (!ok) {
                     aborted = 1;
@@ -873,7 +830,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
             const CascadeBank& bk = p.bank[c.bank];
             const int op = w.op();
             const uint32_t in_phase = static_cast<uint32_t>(epi_tiles) & 1u;
-            if (!op_gram(op) && op != OP_NORMALIZE) {
+            if (!op_gram(op)) {
                 // the group's quarters of the tile's input, once the group's earlier TMA
                 // stores have finished reading the boxes
                 if (x.leader) {
@@ -888,37 +845,26 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                 ++epi_tiles;
                 x.last_box = -1;  // every box of the group is now an input box
             }
-            uint32_t tbase = 0, tempty = 0;
-            if (op != OP_NORMALIZE) {
-                const int ab = mt & 1;
-                const uint32_t u = static_cast<uint32_t>(mt >> 1);
-                ++mt;
-                if (!mbar_wait(&tfull_bar[ab], u & 1u, p.err)) x.fail = true;
-                if (x.leader && x.grp == 0 && rank == 0) TL_PUT(w.t(), TL_EPI_START, globaltimer_ns());
-                tc_fence_after();
-                tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(ab * BN);
-                tempty = ab ? tempty_leader1 : tempty_leader0;
-            }
-            if (op == OP_NORMALIZE && x.leader && x.grp == 0 && rank == 0)
-                TL_PUT(w.t(), TL_EPI_START, globaltimer_ns());
+            const int ab = mt & 1;
+            const uint32_t u = static_cast<uint32_t>(mt >> 1);
+            ++mt;
+            if (!mbar_wait(&tfull_bar[ab], u & 1u, p.err)) x.fail = true;
+            if (x.leader && x.grp == 0 && rank == 0) TL_PUT(w.t(), TL_EPI_START, globaltimer_ns());
+            tc_fence_after();
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(ab * BN);
+            const uint32_t tempty = ab ? tempty_leader1 : tempty_leader0;
             switch (op) {
                 case OP_GRAM: epi_tile<OP_GRAM>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
                 case OP_GRAM_NORM: epi_tile<OP_GRAM_NORM>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
                 case OP_SQPOLY: epi_tile<OP_SQPOLY>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
                 case OP_XUPDATE: epi_tile<OP_XUPDATE>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
-                case OP_XUPDATE_OUT: epi_tile<OP_XUPDATE_OUT>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
-                default:
-                    normalize_tile(bk, c, rank, x.grp, quad * 32 + lane);
-                    // the group's plain stores precede its leader's publication of the tile,
-                    // which may come before the next iteration's group barrier
-                    named_barrier_sync(1 + x.grp, 128);
-                    break;
+                default: epi_tile<OP_XUPDATE_OUT>(p, bk, P, c, rank, x, tbase, tempty, in_phase); break;
             }
             if (x.leader && x.grp == 0 && rank == 0) TL_PUT(w.t(), TL_EPI_END, globaltimer_ns());
             // publish the group's previous tile: its stores are older than this tile's two
             // (one per quarter), so they have long completed
             if (x.leader && pending) {
-                if (op != OP_NORMALIZE && (op != OP_XUPDATE_OUT || bk.out_tma)) bulk_wait_all_but_two();
+                if (op != OP_XUPDATE_OUT || bk.out_tma) bulk_wait_all_but_two();
                 else bulk_wait_all();
                 send_done(mbox, x, tile_counter(p, pend), p.err);
             }

@@ -100,12 +100,28 @@ struct NormParams {
     int nbanks, total_mats;
     float margin, eps;
     float* d;  // [total_mats]
-    unsigned* counters;  // [2 * total_mats + SCHED_COUNTERS] cascade counters, zeroed by norm_d
+    unsigned* counters;  // [total_mats + SCHED_COUNTERS] cascade counters, zeroed by norm_d
     unsigned* err;
 };
 // d[mat] = sqrt(sum_i float(bf16(sum of the partials of i))) * margin + eps; also zeroes
 // the matrix's cascade completion counters.
 cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream);
+
+// The normalisation X / d: Y1 = bf16(Y0 / d[mat]) over the padded extent [s_pad, L_pad]
+// of every matrix, in 8-element (16-byte) chunks numbered bank by bank.
+struct NormXBank {
+    const uint16_t* y0;   // [g, s_pad, L_pad] X_raw
+    uint16_t* y1;         // [g, s_pad, L_pad] X / d
+    const float* d;       // [g]
+    long long chunk_begin;
+    long long chunks_per_mat;
+};
+struct NormXParams {
+    NormXBank bank[MAX_BANKS];
+    int nbanks;
+    long long total_chunks;
+};
+cudaError_t launch_normalize(const NormXParams& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- the cascade kernel
 // One persistent tcgen05 kernel walks every phase of the cascade (anvil_gemm.cu).
@@ -114,8 +130,7 @@ enum PhaseOp : int {
     OP_GRAM_NORM = 1,   // A = bf16(bf16(Y Y^T) / d^2)        (the first Gram, on X_raw)
     OP_SQPOLY = 2,      // B = bf16(b A + c A A)              (diagonal and upper 256-blocks)
     OP_XUPDATE = 3,     // Y' = bf16(a Y + B Y)
-    OP_XUPDATE_OUT = 4, // the same, written to out in the natural [m, n] layout
-    OP_NORMALIZE = 5    // Y1 = bf16(Y0 / d)                  (no product)
+    OP_XUPDATE_OUT = 4  // the same, written to out in the natural [m, n] layout
 };
 
 // Tensor maps of one bank (3-D bf16 over [g][rows][cols]).
@@ -133,15 +148,15 @@ enum MapSlot : int {
 };
 
 constexpr int MAX_CASCADE_MAPS = 16;                      // spectral maps per call
-constexpr int MAX_PHASES = 3 * MAX_CASCADE_MAPS + 1;      // GRAM_NORM, NORMALIZE, 3 per map - 1
+constexpr int MAX_PHASES = 3 * MAX_CASCADE_MAPS;          // GRAM_NORM, then 3 per map but the first map's Gram
 
 struct CascadeBank {
     CUtensorMap tm[TM_COUNT];
     uint16_t* a;        // A [g, s_pad, s_pad]
     uint16_t* b;        // B [g, s_pad, s_pad]
     uint16_t* out;      // out [g, m, n]
-    const uint16_t* y0; // X_raw [g, s_pad, L_pad] (the normalisation's input)
-    uint16_t* y1;       // normalised X (its output)
+    const uint16_t* y0; // X_raw [g, s_pad, L_pad] (the first Gram's operand)
+    uint16_t* y1;       // normalised X (the first X-update's input)
     const float* d;     // [g] normaliser of this bank's matrices
     int g, s_pad, L_pad, m, n, tall;
     int out_tma;        // out is written through TM_OUT (rows 16-byte aligned; tall: transposed boxes)
@@ -160,9 +175,8 @@ struct CascadePhase {
     int map_a_t, map_b_t;
     float a, b, c;                      // the map's coefficients
     // before an item of matrix i of bank q loads anything: chain[i] >= need_chain[q]
-    // and norm[i] >= need_norm[q] (0: no wait)
+    // (0: no wait)
     unsigned need_chain[MAX_BANKS];
-    unsigned need_norm[MAX_BANKS];
 };
 
 // The order in which the kernel walks its items: a list of runs, each the tiles of one
@@ -187,10 +201,8 @@ struct CascadeParams {
     int sm_count;
     // Completion counters per matrix, zeroed by norm_d_kernel each step: every finished
     // tile adds one per epilogue warp group per CTA (4 per tile) to chain[] (the chain of
-    // product phases, each of which waits for the one before it) or, for a normalisation
-    // tile, to norm[].
+    // product phases, each of which waits for the one before it).
     unsigned* chain;
-    unsigned* norm;
     // this launch's item counter (zeroed by norm_d_kernel each step): every CTA pair takes
     // its next item with an atomic add
     unsigned* next_item;

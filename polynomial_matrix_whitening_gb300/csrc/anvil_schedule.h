@@ -15,8 +15,5 @@ void build_phases(CascadeParams* cp, const anvil_map_coef* maps, int nmaps);
 // Phase by phase, banks in order, whole banks per run; phase_run (optional, nphases + 1
 // entries) receives each phase's first run.
 void order_phase_major(CascadeParams* cp, int* phase_run);
-// Phase-major, with the normalisation's tiles spread over the product phases before the
-// first X-update (which do not read the normalised X).
-void order_normalize_interleaved(CascadeParams* cp);
 
 }  // namespace anvil

@@ -26,7 +26,7 @@ import numpy as np
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-OPS = {0: "Gram", 1: "first Gram", 2: "bA+cA^2", 3: "X-update", 4: "last X-update", 5: "normalise"}
+OPS = {0: "Gram", 1: "first Gram", 2: "bA+cA^2", 3: "X-update", 4: "last X-update"}
 BANK_NAMES = ("qk", "vo", "mlp")
 (META, TILE, SCHED_TAKE, SCHED_READY, SCHED_PUSH, PROD_FIRST, MMA_TAKEN, MMA_ACC_FREE, MMA_FIRST,
  MMA_LAST, EPI_START, EPI_END, MMA_FIRST_CLK, MMA_LAST_CLK, MMA_WAIT_CLK, PROD_WAIT_CLK) = range(16)
@@ -58,7 +58,7 @@ def kind(it):
 
 
 def analyse(items):
-    prod = [i for i in items if i["op"] != 5 and i["first"] > 0]
+    prod = [i for i in items if i["first"] > 0]
     t0 = min(i["take"] for i in items)
     t1 = max(max(i["epi1"], i["last"]) for i in items)
     span = (t1 - t0) / 1e3
@@ -110,9 +110,8 @@ def analyse(items):
         d = deps.setdefault(OPS[i["op"]], [0, 0.0])
         d[0] += 1
         d[1] += (i["ready"] - i["take"]) / 1e3
-    norm = [(i["epi1"] - i["epi0"]) / 1e3 for i in items if i["op"] == 5 and i["epi1"] > 0]
     return dict(span=span, pairs=n, items=len(items), tiles=len(prod), per_pair=per_pair, rate=rate,
-                by_next=by_next, deps=deps, norm=norm, by_bank={k: v / n for k, v in by_bank.items()})
+                by_next=by_next, deps=deps, by_bank={k: v / n for k, v in by_bank.items()})
 
 
 def report(res, cascade_ms, clocks_note):
@@ -154,10 +153,6 @@ def report(res, cascade_ms, clocks_note):
     out.append("|---|---|---|")
     for k, (cnt, s) in res["deps"].items():
         out.append(f"| {k} | {cnt} | {s:.1f} |")
-    if res["norm"]:
-        out.append("")
-        out.append(f"Normalisation tiles: {len(res['norm'])}, median {statistics.median(res['norm']):.2f} us "
-                   f"each in the epilogue warps.")
     return "\n".join(out)
 
 
