@@ -398,6 +398,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// The same descriptor in two halves, for the MMA issuer's inner loop: the high word (stride
+// offset 1024 bytes, the fixed 1, 128-byte swizzle) is common to every operand here, and
+// the low word (start address >> 4, leading offset >> 4) advances by a k-step's bytes >> 4.
+constexpr uint32_t SW128_DESC_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t lo) {
+    return (static_cast<uint64_t>(SW128_DESC_HI) << 32) | lo;
+}
+
 // Instruction descriptor of tcgen05.mma .kind::f16 with bf16 A and B, fp32 accumulate:
 // D format (bits 4-5) = 1 (f32), A format (7-9) = 1 (bf16), B format (10-12) = 1 (bf16),
 // A major (15) and B major (16): 0 = K-major, 1 = MN-major, N >> 3 in bits 17-22,

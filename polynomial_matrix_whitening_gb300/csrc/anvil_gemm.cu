@@ -681,14 +681,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) cascade_kernel(const __grid_c
                     const uint32_t b0 = shared_ab ? a0 : a0 + A_STAGE;
                     const bool a_mn = kb < kb_a_mn, b_mn = kb < kb_b_mn;
                     const uint32_t idesc = idesc_bf16_f32(PAIR, PAIR, a_mn, b_mn);
+                    // K-major: a 16-deep k-step is 32 bytes along the row; MN-major: 64-element
+                    // chunks 8 KB apart, a k-step is 16 rows of 128 bytes
+                    const uint32_t a_lo = sw128_desc_lo(a0, a_mn ? 8192 : 16);
+                    const uint32_t b_lo = sw128_desc_lo(b0, b_mn ? 8192 : 16);
+                    const uint32_t a_step = a_mn ? 2048 >> 4 : 32 >> 4, b_step = b_mn ? 2048 >> 4 : 32 >> 4;
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = a_mn ? smem_desc_sw128(a0 + kk * 2048, 8192, 1024)
-                                                 : smem_desc_sw128(a0 + kk * 32, 16, 1024);
-                        const uint64_t bd = b_mn ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
-                                                 : smem_desc_sw128(b0 + kk * 32, 16, 1024);
-                        umma_bf16_pair(dacc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        umma_bf16_pair(dacc, sw128_desc(a_lo + kk * a_step), sw128_desc(b_lo + kk * b_step), idesc,
+                                       (kb | kk) != 0 ? 1u : 0u);
                     const int s_next = s + 1 == STAGES ? 0 : s + 1;
                     const uint32_t ph_next = s_next == 0 ? ph ^ 1u : ph;
                     ready = mbar_test_wait(smem_u32(&full_bar[s_next]), ph_next);
