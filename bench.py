@@ -525,7 +525,7 @@ def run_anvil(args, world, rank, local):
     torch.cuda.synchronize()
     mom_link = [t for k, t in prof_l.records if k == "momentum"]
     update_tail_linked = tail_entry(time_tail(links), 12.25,
-                                    "3 launches: lane powers, lane scales, fused equalise + decay gated by the "
+                                    "3 launches: lane powers (2 B/elem), lane scales, fused equalise + decay gated by the "
                                     "slow-rail sign bits the step wrote into the tail link (10.25 B/elem)")
     update_tail_linked["step_cost_ms"] = statistics.mean(mom_link) - mom_ms
     update_tail_linked["step_cost_note"] = ("the momentum kernel's extra time per step for writing the "
