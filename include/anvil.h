@@ -137,10 +137,8 @@ anvil_status anvil_bank_step(const float* grad, float* velocity, int g, int m, i
 /* anvil_bank_step for callers that must not allocate device memory.  The page has no
  * counterpart: this is a deployment convenience.  Some hosts cannot call cudaMalloc
  * from the code that runs the optimizer step: an application whose device memory is
- * all handed out by its own pool or budget, code running while another thread
- * captures a CUDA graph in global capture mode (a cudaMalloc there breaks the
- * capture), or a latency-bound loop where cudaMalloc / cudaFree, which synchronise
- * the device, are not allowed.  This variant takes the same arguments as
+ * all handed out by its own pool or budget, or a latency-bound loop where cudaMalloc /
+ * cudaFree, which synchronise the device, are not allowed.  This variant takes the same arguments as
  * anvil_bank_step but keeps its scratch in a fixed array of
  * ANVIL_STATIC_SCRATCH_BYTES bytes of device memory that the library declares
  * statically: each GPU that loads the library holds that array until the process
