@@ -22,11 +22,11 @@
  * no CPU path.  All calls are asynchronous on the given stream (a
  * cudaStream_t / CUstream handle passed as void*; NULL = legacy default
  * stream).  A step is four kernels on that stream: momentum + cast, the normaliser d,
- * the normalisation X / d, and one persistent kernel for every product of every map.  No call below allocates, frees or synchronises, except
- * anvil_bank_step on its first use of a size (documented there), the error reads
- * anvil_last_device_error (waits for its stream) and anvil_device_error (waits for the
- * device).  Errors are returned as status codes; no
- * exception crosses the ABI.
+ * the normalisation X / d, and one persistent kernel for every product of every map.
+ * No call below allocates, frees or synchronises, except anvil_bank_step on its first
+ * use of a size (documented there), the error reads anvil_last_device_error (waits for
+ * its stream) and anvil_device_error (waits for the device).  Errors are returned as
+ * status codes; no exception crosses the ABI.
  */
 #ifndef ANVIL_H
 #define ANVIL_H
