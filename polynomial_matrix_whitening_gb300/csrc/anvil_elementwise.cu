@@ -253,49 +253,41 @@ cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream) {
 
 // X / d (page "modded-nanogpt track_1_short/optim/anvil.py", anvil_cascade, the division
 // of X by its normaliser) over the padded working layout, which is contiguous per bank:
-// chunk k of a bank is elements 8k .. 8k + 7 of its Y0 and Y1.  Each thread converts
-// NX_CHUNKS chunks, every load in flight before the first store; a warp's loads cover 32
-// consecutive chunks (512 bytes).  The quotient is bf16(RN(x / d)), each element rounded
-// as the page's fp32 division then its bf16 cast (div4_to_bf2); the padding stays zero.
+// chunk k of a bank is elements 8k .. 8k + 7 of its Y0 and Y1.  A block converts
+// NX_BLOCK_CHUNKS chunks of one matrix, so its bank, matrix and d are found once; each
+// thread converts NX_CHUNKS of them, every load in flight before the first store, a warp's
+// loads covering 32 consecutive chunks (512 bytes).  The quotient is bf16(RN(x / d)), each
+// element rounded as the page's fp32 division then its bf16 cast (div4_to_bf2); the
+// padding stays zero.
 constexpr int NX_THREADS = 256;
-constexpr int NX_CHUNKS = 4;
+constexpr int NX_CHUNKS = NX_BLOCK_CHUNKS / NX_THREADS;
 __global__ void __launch_bounds__(NX_THREADS) normalize_kernel(const __grid_constant__ NormXParams p) {
     pdl_allow_next();
     pdl_wait_previous();  // d (norm_d) and X_raw (momentum)
-    const long long c0 = static_cast<long long>(blockIdx.x) * (NX_THREADS * NX_CHUNKS) + threadIdx.x;
-    uint4 v[NX_CHUNKS];
-    int q[NX_CHUNKS];
-    long long loc[NX_CHUNKS];
-#pragma unroll
-    for (int i = 0; i < NX_CHUNKS; ++i) {
-        const long long c = c0 + static_cast<long long>(i) * NX_THREADS;
-        q[i] = -1;
-        if (c < p.total_chunks) {
-            int b = 0;
+    int b = 0;
 #pragma unroll 1
-            for (int k = 1; k < p.nbanks; ++k)
-                if (c >= p.bank[k].chunk_begin) b = k;
-            q[i] = b;
-            loc[i] = c - p.bank[b].chunk_begin;
-            v[i] = __ldg(reinterpret_cast<const uint4*>(p.bank[b].y0) + loc[i]);
-        }
-    }
+    for (int k = 1; k < p.nbanks; ++k)
+        if (static_cast<int>(blockIdx.x) >= p.bank[k].block_begin) b = k;
+    const NormXBank& B = p.bank[b];
+    const int lb = static_cast<int>(blockIdx.x) - B.block_begin;
+    const float d = B.d[lb / B.blocks_per_mat];
+    const float rcp = __frcp_rn(d);
+    const uint64_t rcp2 = f2_pack(rcp, rcp);
+    const size_t c0 = static_cast<size_t>(lb) * NX_BLOCK_CHUNKS + threadIdx.x;
+    const uint4* src = reinterpret_cast<const uint4*>(B.y0) + c0;
+    uint4* dst = reinterpret_cast<uint4*>(B.y1) + c0;
+    uint4 v[NX_CHUNKS];
 #pragma unroll
-    for (int i = 0; i < NX_CHUNKS; ++i) {
-        if (q[i] < 0) continue;
-        const NormXBank& B = p.bank[q[i]];
-        const float d = B.d[loc[i] / B.chunks_per_mat];
-        const float rcp = __frcp_rn(d);
-        reinterpret_cast<uint4*>(B.y1)[loc[i]] =
-            div4_to_bf2(bf2_to_f2(v[i].x), bf2_to_f2(v[i].y), bf2_to_f2(v[i].z), bf2_to_f2(v[i].w), f2_pack(rcp, rcp), d);
-    }
+    for (int i = 0; i < NX_CHUNKS; ++i) v[i] = __ldg(src + i * NX_THREADS);
+#pragma unroll
+    for (int i = 0; i < NX_CHUNKS; ++i)
+        dst[i * NX_THREADS] = div4_to_bf2(bf2_to_f2(v[i].x), bf2_to_f2(v[i].y), bf2_to_f2(v[i].z),
+                                          bf2_to_f2(v[i].w), rcp2, d);
 }
 
 cudaError_t launch_normalize(const NormXParams& p, cudaStream_t stream) {
-    if (p.total_chunks <= 0) return cudaSuccess;
-    const long long per_block = NX_THREADS * NX_CHUNKS;
-    const unsigned blocks = static_cast<unsigned>((p.total_chunks + per_block - 1) / per_block);
-    return launch_pdl(normalize_kernel, dim3(blocks), dim3(NX_THREADS), 0, stream, p);
+    if (p.total_blocks <= 0) return cudaSuccess;
+    return launch_pdl(normalize_kernel, dim3(static_cast<unsigned>(p.total_blocks)), dim3(NX_THREADS), 0, stream, p);
 }
 
 // ---------------------------------------------------------------- tracing

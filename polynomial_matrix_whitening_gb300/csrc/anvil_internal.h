@@ -108,18 +108,21 @@ struct NormParams {
 cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream);
 
 // The normalisation X / d: Y1 = bf16(Y0 / d[mat]) over the padded extent [s_pad, L_pad]
-// of every matrix, in 8-element (16-byte) chunks numbered bank by bank.
+// of every matrix, in 8-element (16-byte) chunks.  A block converts NX_BLOCK_CHUNKS
+// consecutive chunks of one matrix (s_pad and L_pad are multiples of 256, so a matrix is
+// a whole number of blocks); the blocks are numbered bank by bank.
+constexpr int NX_BLOCK_CHUNKS = 1024;
 struct NormXBank {
     const uint16_t* y0;   // [g, s_pad, L_pad] X_raw
     uint16_t* y1;         // [g, s_pad, L_pad] X / d
     const float* d;       // [g]
-    long long chunk_begin;
-    long long chunks_per_mat;
+    int block_begin;      // first block of this bank
+    int blocks_per_mat;   // s_pad * L_pad / 8 / NX_BLOCK_CHUNKS
 };
 struct NormXParams {
     NormXBank bank[MAX_BANKS];
     int nbanks;
-    long long total_chunks;
+    int total_blocks;
 };
 cudaError_t launch_normalize(const NormXParams& p, cudaStream_t stream);
 
