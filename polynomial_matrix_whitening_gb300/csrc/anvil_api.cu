@@ -422,7 +422,7 @@ anvil_status run_step(const anvil_bank_desc* banks, int nbanks, const anvil_scal
         X.y0 = P[i].y[0];
         X.y1 = P[i].y[1];
         X.d = P[i].d;
-        // s_pad and L_pad are multiples of PAIR (256): a matrix is a whole number of blocks
+        // s_pad is a multiple of PAIR and L_pad of LPAD: a matrix is a whole number of blocks
         X.blocks_per_mat = static_cast<int>(static_cast<long long>(G.s_pad) * G.L_pad / 8 / NX_BLOCK_CHUNKS);
         X.block_begin = xp.total_blocks;
         xp.total_blocks += G.g * X.blocks_per_mat;

@@ -112,7 +112,7 @@ cudaError_t launch_norm_d(const NormParams& p, cudaStream_t stream);
 // consecutive chunks of one matrix (s_pad and L_pad are multiples of 256, so a matrix is
 // a whole number of blocks); the blocks are numbered bank by bank.
 constexpr int NX_BLOCK_CHUNKS = 1024;
-static_assert((PAIR * PAIR / 8) % NX_BLOCK_CHUNKS == 0, "a padded matrix is a whole number of X / d blocks");
+static_assert((PAIR * LPAD / 8) % NX_BLOCK_CHUNKS == 0, "a padded matrix is a whole number of X / d blocks");
 struct NormXBank {
     const uint16_t* y0;   // [g, s_pad, L_pad] X_raw
     uint16_t* y1;         // [g, s_pad, L_pad] X / d
