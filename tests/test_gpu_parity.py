@@ -430,16 +430,15 @@ def test_eight_banks_in_one_call(A):
 
 
 @pytest.mark.parametrize("shapes", [
-    # 400 matrices: the normalisation interleaved with the first products, one run per
-    # matrix and phase before the first X-update (about 1260 runs)
+    # 400 and 1000 matrices in three banks of tiny shapes: thousands of one-tile items per
+    # phase, walked phase by phase
     [(200, 24, 16), (120, 8, 40), (80, 20, 20)],
-    # 1000 matrices: past the run table, the plain phase-major order
     [(500, 24, 16), (300, 8, 40), (200, 20, 20)],
 ], ids=["400_matrices", "1000_matrices"])
 def test_many_matrices_item_order(A, shapes):
-    """The item order of a call with hundreds of matrices (one run per matrix near the
-    run table's capacity, and the fallback past it): the grouped call equals one call per
-    bank bit for bit, and sampled matrices match the oracle."""
+    """Calls with hundreds of matrices (thousands of items in each phase, so pairs move
+    between phases of different matrices all the time): the grouped call equals one call
+    per bank bit for bit, and sampled matrices match the oracle."""
     banks, solo, cases = [], [], []
     for j, (g, m, n) in enumerate(shapes):
         grad, vel = W.random_case(900 + j, g, m, n)
