@@ -194,7 +194,7 @@ struct CascadeRun {
     uint16_t mat0;    // first matrix (within the bank)
     uint32_t nmat;    // matrices in the run
 };
-constexpr int MAX_RUNS = 1400;
+constexpr int MAX_RUNS = MAX_PHASES * MAX_BANKS;  // phase by phase, one run per bank
 
 struct CascadeParams {
     CascadeBank bank[MAX_BANKS];
