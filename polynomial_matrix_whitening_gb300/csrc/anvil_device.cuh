@@ -152,15 +152,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
-// 16-byte global load that does not allocate in L1 (streamed data).
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
 // Non-blocking test of the phase with this parity.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
