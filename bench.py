@@ -260,7 +260,7 @@ def workload_config(world):
             "scalars": "post-engage: momentum 0.95, fast_beta 0.85, fast_weight 0.4385, "
                        "slow_beta 0.98",
             "maps": "6 ANVIL_MAPS",
-            "graph": "the timed steps captured as one CUDA graph (3 kernels per step)",
+            "graph": "the timed steps captured as one CUDA graph (4 kernels per step)",
             "l2": "inputs larger than L2 (grads 260 MB + rails 520 MB per step)",
             "parallelism": f"replicas x{world}"}
 
