@@ -48,6 +48,11 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+// Negation of both halves (exact).  A difference a - b is taken as f2_add(a, f2_neg(b)):
+// a packed subtract whose operand is a packed product was measured to come out as one
+// fused rounding (1 ulp off in about 2.4% of elements), the addition of the negated product
+// as two roundings, like the scalar operations.
+__device__ __forceinline__ uint64_t f2_neg(uint64_t a) { return a ^ 0x8000000080000000ull; }
 // two bf16 (round to nearest even) of a packed fp32 pair
 __device__ __forceinline__ uint32_t f2_to_bf2(uint64_t v) {
     uint32_t d;

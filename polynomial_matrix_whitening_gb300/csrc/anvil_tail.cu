@@ -24,17 +24,19 @@ namespace anvil {
 
 // ---------------------------------------------------------------- lane powers
 // One grid over every bank (a block finds its bank from power_begin).
-// Lanes along rows (m >= n): each warp sums POWER_ROWS consecutive rows of the bank (rows
-// of consecutive matrices are contiguous); with the vector layout (n % 8 == 0, 16-byte
+// Lanes along rows (m >= n): a warp sums groups of POWER_ROWS consecutive rows of the bank
+// (rows of consecutive matrices are contiguous), the bank's power_nblk blocks walking its
+// groups with a stride of their warps; with the vector layout (n % 8 == 0, 16-byte
 // aligned) lane k takes 8-element chunks k, k + 32, ... of every row, POWER_CHUNKS chunks
-// of each of the warp's rows loaded before any is summed (one memory round trip for rows
-// of up to 768 elements), otherwise single elements; a fixed shuffle tree adds each row's
-// 32 partial sums.
+// of each of the group's rows loaded before any is summed (one memory round trip for rows
+// of up to 768 elements, and then the next group's loads go out before this group's sums
+// are reduced), otherwise single elements; a fixed shuffle tree adds each row's 32
+// partial sums.
 // Lanes along columns (m < n): a block covers 256 columns of one matrix (8 per thread with
 // the vector layout, else 32 columns) with 8 row slices; slice k sums rows k, k + 8, ...;
 // the slice sums of a column are added in slice order.
 constexpr int POWER_COLS = 256;  // columns per block, lanes along columns, vector layout
-constexpr int POWER_ROWS = 4;    // rows per warp, lanes along rows
+constexpr int POWER_ROWS = 2;    // rows per group, lanes along rows
 constexpr int POWER_CHUNKS = 3;  // 16-byte chunks of each row a lane loads before summing
 __device__ __forceinline__ float sumsq8(uint4 q, float s) {
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -45,8 +47,11 @@ __device__ __forceinline__ float sumsq8(uint4 q, float s) {
     }
     return s;
 }
+__host__ __device__ inline long long power_groups(const TailBank& B) {
+    return (static_cast<long long>(B.g) * B.m + POWER_ROWS - 1) / POWER_ROWS;
+}
 __host__ __device__ inline long long power_blocks(const TailBank& B) {
-    if (B.m >= B.n) return (static_cast<long long>(B.g) * B.m + 8 * POWER_ROWS - 1) / (8 * POWER_ROWS);
+    if (B.m >= B.n) return B.power_nblk;
     const int span = B.vec8 ? POWER_COLS : 32;
     return static_cast<long long>(B.g) * ((B.n + span - 1) / span);
 }
@@ -63,13 +68,54 @@ __global__ void __launch_bounds__(256, 4) lane_power_kernel(const __grid_constan
     if (B.m >= B.n) {
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const long long nrows = static_cast<long long>(B.g) * B.m;
-        const long long row0 = (lb * 8 + warp) * POWER_ROWS;  // row (mat * m + row) of the bank
-        if (row0 >= nrows) return;  // whole warp
+        const long long ngroups = power_groups(B), gstride = static_cast<long long>(B.power_nblk) * 8;
+        long long grp = lb * 8 + warp;
+        if (grp >= ngroups) return;  // whole warp
+        const int nc = B.n / 8;
+        // the group's row sums, reduced across the warp and stored (lane 0)
+        auto finish = [&](long long row0, float (&s)[POWER_ROWS]) {
+#pragma unroll
+            for (int k = 0; k < POWER_ROWS; ++k) {
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) s[k] = __fadd_rn(s[k], __shfl_xor_sync(0xffffffffu, s[k], off));
+                if (lane == 0 && row0 + k < nrows) B.power[row0 + k] = __fdiv_rn(s[k], static_cast<float>(B.n));
+            }
+        };
+        if (B.vec8 && nc <= 32 * POWER_CHUNKS) {
+            // one load round per group: group grp + gstride's loads go out before grp's reduction
+            uint4 q[POWER_CHUNKS][POWER_ROWS];
+            auto load = [&](long long row0) {
+#pragma unroll
+                for (int u = 0; u < POWER_CHUNKS; ++u)
+#pragma unroll
+                    for (int k = 0; k < POWER_ROWS; ++k)
+                        q[u][k] = (lane + 32 * u < nc && row0 + k < nrows)
+                                      ? __ldcs(reinterpret_cast<const uint4*>(B.update + static_cast<size_t>(row0 + k) * B.n) + lane + 32 * u)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+            };
+            load(grp * POWER_ROWS);
+            for (;;) {
+                float s[POWER_ROWS];
+#pragma unroll
+                for (int k = 0; k < POWER_ROWS; ++k) s[k] = 0.f;
+#pragma unroll
+                for (int u = 0; u < POWER_CHUNKS; ++u)
+#pragma unroll
+                    for (int k = 0; k < POWER_ROWS; ++k) s[k] = sumsq8(q[u][k], s[k]);
+                const long long nxt = grp + gstride;
+                if (nxt < ngroups) load(nxt * POWER_ROWS);
+                finish(grp * POWER_ROWS, s);
+                if (nxt >= ngroups) break;
+                grp = nxt;
+            }
+            return;
+        }
+        for (; grp < ngroups; grp += gstride) {
+        const long long row0 = grp * POWER_ROWS;  // row (mat * m + row) of the bank
         float s[POWER_ROWS];
 #pragma unroll
         for (int k = 0; k < POWER_ROWS; ++k) s[k] = 0.f;
         if (B.vec8) {
-            const int nc = B.n / 8;
             for (int j0 = lane; j0 < nc; j0 += 32 * POWER_CHUNKS) {
                 uint4 q[POWER_CHUNKS][POWER_ROWS];
 #pragma unroll
@@ -95,11 +141,7 @@ __global__ void __launch_bounds__(256, 4) lane_power_kernel(const __grid_constan
                 }
             }
         }
-#pragma unroll
-        for (int k = 0; k < POWER_ROWS; ++k) {
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) s[k] = __fadd_rn(s[k], __shfl_xor_sync(0xffffffffu, s[k], off));
-            if (lane == 0 && row0 + k < nrows) B.power[row0 + k] = __fdiv_rn(s[k], static_cast<float>(B.n));
+        finish(row0, s);
         }
     } else {
         __shared__ float part[8][POWER_COLS + 1];
@@ -319,11 +361,6 @@ __device__ __forceinline__ void tail_element_gated(float v, float scale, bool al
     mt = static_cast<uint16_t>(bits & 0xffffu);
 }
 
-// With the tail link: the decay gate [slow rail * w >= 0] of an element follows from the
-// sign bits (the product of two numbers of magnitude at least 2^-100 and 2^-40 is not zero
-// and has the sign of their signs) unless the link flags the rail value (zero, below
-// 2^-100, not finite) or w is outside [2^-40, FLT_MAX] (its exponent field outside
-// [87, 254]): then the fp32 rail is read.  Bit k of the result: element k is aligned.
 // The 8 bits of columns 4 t .. 4 t + 7 of a link word (bit 16 q + t is column 4 t + q), in
 // column order: the bits at 0, 16, 32, 48 of (w >> t) gathered by one multiply.
 __device__ __forceinline__ unsigned link_bits8(uint64_t w, int t) {
@@ -332,20 +369,46 @@ __device__ __forceinline__ unsigned link_bits8(uint64_t w, int t) {
     return static_cast<unsigned>(((lo * M) >> 48) & 0xfu) | (static_cast<unsigned>(((hi * M) >> 48) & 0xfu) << 4);
 }
 
+
+// The gate bits of a chunk, in the order the link words give them up cheaply: element k
+// of the chunk at bit gate_pos(k).  Before the last fold the bits sit "spread" at bit
+// 16 (k & 1) + 2 ((k >> 1) & 1) + (k >> 2) of a word, which gathers them from a link word
+// (bit 16 q + t of the word is column 4 t + q of its 64 columns) with two 32-bit shifts.
+__host__ __device__ constexpr int gate_pos(int k) { return 4 * (k & 1) + 2 * ((k >> 1) & 1) + (k >> 2); }
+// The spread bits of chunk j (columns 8 j .. 8 j + 7) of a link word.
+__device__ __forceinline__ uint32_t link_spread(uint64_t w, int j) {
+    const uint32_t a = static_cast<uint32_t>(w) >> (2 * j), b = static_cast<uint32_t>(w >> 32) >> (2 * j);
+    return (a & 0x00030003u) | ((b & 0x00030003u) << 2);
+}
+// The spread sign bits of the chunk's master weights (bit 15 and 31 of each param word
+// are the signs of elements 2 q and 2 q + 1).
+__device__ __forceinline__ uint32_t sign_spread(const uint32_t (&pw)[4]) {
+    return ((pw[0] >> 15) & 0x00010001u) | ((pw[2] >> 14) & 0x00020002u) | ((pw[1] >> 13) & 0x00040004u) |
+           ((pw[3] >> 12) & 0x00080008u);
+}
+__device__ __forceinline__ unsigned fold_spread(uint32_t x) { return (x | (x >> 12)) & 0xffu; }
+
+// With the tail link: the decay gate [slow rail * w >= 0] of an element follows from the
+// sign bits (the product of two numbers of magnitude at least 2^-100 and 2^-40 is not zero
+// and has the sign of their signs) unless the link flags the rail value (zero, below
+// 2^-100, not finite) or w is outside [2^-40, FLT_MAX] (its exponent field outside
+// [87, 254]): then the fp32 rail is read.  Result: element k aligned at bit gate_pos(k).
 __device__ __forceinline__ unsigned link_gates(ulonglong2 sx, int c0, const float* rail, const uint32_t (&pw)[4],
                                                const uint32_t (&mw)[4]) {
-    const int t = (c0 & 63) >> 2;  // the chunk's columns 4 t .. 4 t + 7 of its 64
-    const unsigned g8 = link_bits8(sx.x, t);
-    bool need_rail = link_bits8(sx.y, t) != 0u;
-    // w's sign bits (bit 15 and 31 of each param word hold elements 2q and 2q + 1)
-    const unsigned w8 = ((pw[0] >> 15) & 1u) | ((pw[0] >> 30) & 2u) | ((pw[1] >> 13) & 4u) | ((pw[1] >> 28) & 8u) |
-                        ((pw[2] >> 11) & 16u) | ((pw[2] >> 26) & 32u) | ((pw[3] >> 9) & 64u) | ((pw[3] >> 24) & 128u);
+    const int j = (c0 & 63) >> 3;  // the chunk's 8 of the link word's 64 columns
+    const uint32_t g = link_spread(sx.x, j);
+    bool need_rail = link_spread(sx.y, j) != 0u;
+    // exponent fields e of both halves of every param word: e + 169 reaches bit 8 iff
+    // e >= 87, e + 1 iff e = 255 (no carry crosses into the upper half)
+    uint32_t ge87 = 0xffffffffu, is255 = 0u;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const unsigned e2 = (pw[q] >> 7) & 0x00ff00ffu;  // both halves' exponent fields
-        need_rail |= __vcmpgtu2(__vsub2(e2, 0x00570057u), 0x00a700a7u) != 0u;
+        const uint32_t e2 = (pw[q] >> 7) & 0x00ff00ffu;
+        ge87 &= e2 + 0x00a900a9u;
+        is255 |= e2 + 0x00010001u;
     }
-    if (!need_rail) return ~(g8 ^ w8) & 0xffu;
+    need_rail |= ((~ge87 | is255) & 0x01000100u) != 0u;
+    if (!need_rail) return fold_spread(~(g ^ sign_spread(pw)) & 0x000f000fu);
     const float4 r0 = __ldcs(reinterpret_cast<const float4*>(rail));
     const float4 r1 = __ldcs(reinterpret_cast<const float4*>(rail + 4));
     const float rv[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
@@ -354,17 +417,57 @@ __device__ __forceinline__ unsigned link_gates(ulonglong2 sx, int c0, const floa
     for (int k = 0; k < 8; ++k) {
         const int q = k >> 1, hi = k & 1;
         const float w = __uint_as_float((hi ? (pw[q] & 0xffff0000u) : (pw[q] << 16)) | (hi ? (mw[q] >> 16) : (mw[q] & 0xffffu)));
-        gk |= (__fmul_rn(rv[k], w) >= 0.f ? 1u : 0u) << k;
+        gk |= (__fmul_rn(rv[k], w) >= 0.f ? 1u : 0u) << gate_pos(k);
     }
     return gk;
 }
 
+// Lane scales of a chunk as pairs: the row's scale sr (lanes along rows), else the
+// chunk's 8 column scales at S (16-byte aligned).
+__device__ __forceinline__ void scale_pairs(uint64_t (&sc2)[4], bool rows_lanes, float sr, const float* S) {
+    if (rows_lanes) {
+        const uint64_t r2 = f2_pack(sr, sr);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sc2[q] = r2;
+    } else {
+        const float4 s0 = *reinterpret_cast<const float4*>(S);
+        const float4 s1 = *reinterpret_cast<const float4*>(S + 4);
+        sc2[0] = f2_pack(s0.x, s0.y);
+        sc2[1] = f2_pack(s0.z, s0.w);
+        sc2[2] = f2_pack(s1.x, s1.y);
+        sc2[3] = f2_pack(s1.z, s1.w);
+    }
+}
+
+// Eight elements of one row chunk (bf16 update words vw, master-weight words pw and mw,
+// lane-scale pairs sc2, gate bits gk at gate_pos), updated in place, two elements per
+// packed fp32 operation (each half an IEEE round-to-nearest operation, in the order of
+// tail_element_gated): u = bf16(v s); w <- (w - w [gate] wd lr) - u lr.
+__device__ __forceinline__ void apply8_gated(const uint32_t (&vw)[4], uint32_t (&pw)[4], uint32_t (&mw)[4],
+                                             const uint64_t (&sc2)[4], unsigned gk, float wd, float lr) {
+    const uint64_t wd2 = f2_pack(wd, wd), lr2 = f2_pack(lr, lr);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint64_t u2 = bf2_to_f2(f2_to_bf2(f2_mul(bf2_to_f2(vw[q]), sc2[q])));
+        // w of elements 2 q and 2 q + 1: param bits above, mantissa below
+        const uint32_t w0 = __byte_perm(mw[q], pw[q], 0x5410), w1 = __byte_perm(mw[q], pw[q], 0x7632);
+        const uint64_t w2 = (static_cast<uint64_t>(w1) << 32) | w0;
+        const uint64_t al2 = f2_pack((gk >> gate_pos(2 * q)) & 1u ? 1.f : 0.f, (gk >> gate_pos(2 * q + 1)) & 1u ? 1.f : 0.f);
+        const uint64_t decay = f2_mul(f2_mul(f2_mul(w2, al2), wd2), lr2);
+        const uint64_t r = f2_add(f2_add(w2, f2_neg(decay)), f2_neg(f2_mul(u2, lr2)));
+        const uint32_t r0 = static_cast<uint32_t>(r), r1 = static_cast<uint32_t>(r >> 32);
+        pw[q] = __byte_perm(r0, r1, 0x7632);
+        mw[q] = __byte_perm(r0, r1, 0x5410);
+    }
+}
+
 // With every bank's link: one warp per row at a time (grid-stride over the call's rows),
 // lane l taking the 8-element chunks l, l + 32, ... of the row, ROW_CHUNKS of them loaded
-// before any is computed.  The row's matrix, learning rate and
-// (rows as lanes) scale are found once per row.
-constexpr int ROW_CHUNKS = 2;
-__global__ void __launch_bounds__(256, 4) tail_apply_rows_kernel(const __grid_constant__ TailParams p) {
+// before any is computed (one: more chunks per lane need more registers than five blocks
+// per SM leave, and spilled or cost occupancy; both measured slower).  The row's matrix,
+// learning rate and (rows as lanes) scale are found once per row.
+constexpr int ROW_CHUNKS = 1;
+__global__ void __launch_bounds__(256, 5) tail_apply_rows_kernel(const __grid_constant__ TailParams p) {
     pdl_allow_next();
     pdl_wait_previous();
     const int lane = threadIdx.x & 31;
@@ -376,8 +479,10 @@ __global__ void __launch_bounds__(256, 4) tail_apply_rows_kernel(const __grid_co
         for (int i = 1; i < p.nbanks; ++i)
             if (rw >= p.bank[i].row_begin) bi = i;
         const TailBank& B = p.bank[bi];
-        const long long lrow = rw - B.row_begin;
-        const int mat = static_cast<int>(lrow / B.m), row = static_cast<int>(lrow - static_cast<long long>(mat) * B.m);
+        // a bank has at most ANVIL_MAX_BATCH * ANVIL_MAX_DIM < 2^31 rows: 32-bit division
+        const unsigned lrow = static_cast<unsigned>(rw - B.row_begin);
+        const int mat = static_cast<int>(lrow / static_cast<unsigned>(B.m));
+        const int row = static_cast<int>(lrow - static_cast<unsigned>(mat) * static_cast<unsigned>(B.m));
         const size_t rbase = (static_cast<size_t>(mat) * B.m + row) * B.n;
         const float lr = B.eff_lr[mat];
         const bool rows_lanes = B.m >= B.n;
@@ -410,26 +515,9 @@ __global__ void __launch_bounds__(256, 4) tail_apply_rows_kernel(const __grid_co
                     uint32_t mw[4] = {mu[u].x, mu[u].y, mu[u].z, mu[u].w};
                     const uint32_t vw[4] = {vu[u].x, vu[u].y, vu[u].z, vu[u].w};
                     const unsigned gk = link_gates(sx[u], c0, rail + c0, pw, mw);
-                    float sc[8];
-                    if (rows_lanes) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) sc[k] = srow;
-                    } else {
-                        const float4 s0 = *reinterpret_cast<const float4*>(S + c0);
-                        const float4 s1 = *reinterpret_cast<const float4*>(S + c0 + 4);
-                        sc[0] = s0.x; sc[1] = s0.y; sc[2] = s0.z; sc[3] = s0.w;
-                        sc[4] = s1.x; sc[5] = s1.y; sc[6] = s1.z; sc[7] = s1.w;
-                    }
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int q = k >> 1, hi = k & 1;
-                        const float v = bf2f(static_cast<uint16_t>(hi ? vw[q] >> 16 : vw[q] & 0xffffu));
-                        uint16_t pp = static_cast<uint16_t>(hi ? pw[q] >> 16 : pw[q] & 0xffffu);
-                        uint16_t mm = static_cast<uint16_t>(hi ? mw[q] >> 16 : mw[q] & 0xffffu);
-                        tail_element_gated(v, sc[k], (gk >> k) & 1u, B.eff_wd, lr, pp, mm);
-                        pw[q] = hi ? ((pw[q] & 0xffffu) | (static_cast<uint32_t>(pp) << 16)) : ((pw[q] & 0xffff0000u) | pp);
-                        mw[q] = hi ? ((mw[q] & 0xffffu) | (static_cast<uint32_t>(mm) << 16)) : ((mw[q] & 0xffff0000u) | mm);
-                    }
+                    uint64_t sc2[4];
+                    scale_pairs(sc2, rows_lanes, srow, S + c0);
+                    apply8_gated(vw, pw, mw, sc2, gk, B.eff_wd, lr);
                     *reinterpret_cast<uint4*>(B.param + rbase + c0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
                     *reinterpret_cast<uint4*>(B.mantissa + rbase + c0) = make_uint4(mw[0], mw[1], mw[2], mw[3]);
                 } else {
@@ -454,8 +542,39 @@ __global__ void __launch_bounds__(256, 4) tail_apply_rows_kernel(const __grid_co
     }
 }
 
+// Blocks of the lane-power kernel resident at once on each device (cached per device).
+static int g_power_blocks[64];
+
 cudaError_t launch_tail_power(const TailParams& p, cudaStream_t stream) {
     TailParams q = p;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e) return e;
+    int& resident = g_power_blocks[dev & 63];
+    if (resident == 0) {
+        int per_sm = 0, sms = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, lane_power_kernel, 256, 0))) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) return e;
+        resident = per_sm > 0 && sms > 0 ? per_sm * sms : 152;
+    }
+    // Lanes along rows: the resident blocks left beside the lanes-along-columns blocks, shared
+    // between the banks by their row groups (at least one block each, at most one warp per group).
+    long long col_blocks = 0, groups = 0;
+    for (int i = 0; i < q.nbanks; ++i) {
+        if (q.bank[i].m >= q.bank[i].n)
+            groups += power_groups(q.bank[i]);
+        else
+            col_blocks += power_blocks(q.bank[i]);
+    }
+    const long long budget = resident - col_blocks > resident / 2 ? resident - col_blocks : resident / 2;
+    for (int i = 0; i < q.nbanks; ++i) {
+        TailBank& B = q.bank[i];
+        if (B.m < B.n) continue;
+        const long long gb = power_groups(B), most = (gb + 7) / 8;
+        long long nb = (budget * gb + groups / 2) / groups;
+        nb = nb < 1 ? 1 : (nb > most ? most : nb);
+        B.power_nblk = static_cast<int>(nb);
+    }
     long long blocks = 0;
     for (int i = 0; i < q.nbanks; ++i) {
         q.bank[i].power_begin = blocks;

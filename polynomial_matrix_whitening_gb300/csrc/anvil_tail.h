@@ -19,6 +19,7 @@ struct TailBank {
     long long chunk_begin;    // first 8-element row chunk of this bank in the call
     long long row_begin;      // first row of this bank in the call (g * m rows per bank)
     long long power_begin;    // first block of this bank in the lane-power grid (set by its launcher)
+    int power_nblk;           // lanes along rows: blocks of this bank in the lane-power grid (set by its launcher)
     int vec8;                 // n % 8 == 0 and 16-byte aligned buffers: vector path
     float* power;             // workspace [g, nl]: lane powers
     float* scale;             // workspace [g, nl]: bf16-rounded lane scales

@@ -194,12 +194,14 @@ def test_linked_step_then_tail_matches_oracle(A, shape):
     np.testing.assert_allclose(le_l, le_o, rtol=2e-2)
 
 
-def test_link_gate_on_zero_tiny_and_huge_values(A):
+@pytest.mark.parametrize("n", [36, 40])
+def test_link_gate_on_zero_tiny_and_huge_values(A, n):
     """The decay gate [slow rail * w >= 0] from the link's sign bits equals the one computed
     from the fp32 rail on every element, where the rail is zero, subnormal or huge and the
     master weight is zero, negative zero, tiny or huge (the cases the link sends back to the
-    fp32 rail): bit-identical."""
-    g, m, n = 2, 64, 36
+    fp32 rail): bit-identical.  n = 36 takes the apply's element-by-element path, n = 40
+    its 16-byte chunk path (vector layout)."""
+    g, m = 2, 64
     rng = np.random.default_rng(77)
     grad = (rng.standard_normal((g, m, n)) * 0.02).astype(np.float32)
     vel = np.zeros((2, g, m, n), np.float32)
@@ -236,6 +238,32 @@ def test_link_gate_on_zero_tiny_and_huge_values(A):
     assert A.device_error() == A.OK
     for a, b in zip(*res):
         np.testing.assert_array_equal(a, b)
+
+
+def test_linked_tail_over_banks_equals_unlinked(A):
+    """One linked tail call over banks of several shapes in the vector layout (lanes along
+    rows and along columns, rows of 8 to 6144 elements) equals the unlinked tail of each
+    bank alone, bit for bit."""
+    shapes = [(4, 256, 768), (3, 1000, 264), (2, 5, 8), (1, 5, 6144), (2, 70, 64)]
+    dev = torch.device("cuda")
+    steps = [linked_step(A, s, 900 + j) for j, s in enumerate(shapes)]
+    ins = [tail_inputs(950 + j, *s) for j, s in enumerate(shapes)]
+
+    def tails(link):
+        return [A.Tail(b.out, b.velocity, to_dev(le), to_dev(p), torch.from_numpy(mt.view(np.int16)).cuda(),
+                       to_dev(lr), 0.1, 0.95, tail_link=b.tail_link if link else None)
+                for (b, _, _, _), (_, _, le, p, mt, lr) in zip(steps, ins)]
+    grouped = tails(True)
+    A.update_tail(grouped, torch.empty(A.tail_workspace_bytes(shapes), dtype=torch.uint8, device=dev))
+    solo = tails(False)
+    for t, s in zip(solo, shapes):
+        A.update_tail([t], torch.empty(A.tail_workspace_bytes([s]), dtype=torch.uint8, device=dev))
+    torch.cuda.synchronize()
+    assert A.device_error() == A.OK
+    for a, b in zip(grouped, solo):
+        assert torch.equal(a.param.view(torch.int16), b.param.view(torch.int16))
+        assert torch.equal(a.mantissa, b.mantissa)
+        assert torch.equal(a.lane_energy, b.lane_energy)
 
 
 # --------------------------------------------------------------------------- Adam
