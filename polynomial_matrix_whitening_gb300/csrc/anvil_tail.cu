@@ -10,8 +10,11 @@
 //   tail_apply_kernel : u = bf16(v * scale[lane]); on the fp32 master weight w (bf16 bits
 //                       p, uint16 mantissa): w <- (w - w [gate w >= 0] wd lr) - u lr, split
 //                       back into p and mantissa (gate: the slow rail)
+//   tail_apply_rows_kernel : the same, the gate taken from the sign bits that the step
+//                       left in the tail link (the fp32 rail only where they cannot decide)
 //
-// Every rounding follows the page's fp32 tensor operations one at a time (no FMA).
+// Every rounding follows the page's fp32 tensor operations one at a time (no FMA; the
+// linked apply takes two elements per packed fp32 operation, two such roundings).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
