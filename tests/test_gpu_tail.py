@@ -73,7 +73,7 @@ def check(p_g, mt_g, le_g, p_o, mt_o, le_o, upd, lr):
 
 
 @pytest.mark.parametrize("shape", [(22, 256, 768), (22, 768, 768), (22, 2816, 768), (3, 130, 300),
-                                   (3, 300, 130), (2, 1, 17), (2, 40, 8)],
+                                   (3, 300, 130), (2, 1, 17), (2, 40, 8), (2, 1000, 800)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_tail_matches_oracle(A, shape):
     upd, vel, le, p, mt, lr = tail_inputs(sum(shape), *shape)
@@ -244,7 +244,7 @@ def test_linked_tail_over_banks_equals_unlinked(A):
     """One linked tail call over banks of several shapes in the vector layout (lanes along
     rows and along columns, rows of 8 to 6144 elements) equals the unlinked tail of each
     bank alone, bit for bit."""
-    shapes = [(4, 256, 768), (3, 1000, 264), (2, 5, 8), (1, 5, 6144), (2, 70, 64)]
+    shapes = [(4, 256, 768), (3, 1000, 264), (2, 5, 8), (1, 5, 6144), (2, 70, 64), (2, 900, 800)]
     dev = torch.device("cuda")
     steps = [linked_step(A, s, 900 + j) for j, s in enumerate(shapes)]
     ins = [tail_inputs(950 + j, *s) for j, s in enumerate(shapes)]
