@@ -49,7 +49,7 @@ GEMM_KINDS = ("gram", "gram_norm", "sqpoly", "xupdate", "xupdate_out", "cascade"
 # full three-bank step (not measured by this run); valid only while the kernel source
 # hashes to the recorded value, reported as null otherwise.
 NCU_TRAFFIC = {
-    "cascade": {"bytes_per_launch": 3019.9e6, "source_hash": "cd854491146301da"},
+    "cascade": {"bytes_per_launch": 2868.7e6, "source_hash": "7c85ec962766be48"},
 }
 
 

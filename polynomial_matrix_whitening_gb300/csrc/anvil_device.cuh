@@ -209,6 +209,16 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_
         "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
 }
+// tma_store_3d with an L2 evict-last policy on the stored lines (data that the next
+// phases read again).
+__device__ __forceinline__ void tma_store_3d_keep(const void* tmap, const void* smem_src, int c0, int c1, int c2) {
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_last.b64 pol, 1.0;\n\t"
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], pol;\n\t}"
+        ::"l"(tmap), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
